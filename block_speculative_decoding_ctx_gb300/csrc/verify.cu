@@ -1,0 +1,495 @@
+// Verification and sampling kernels (greedy prefix match, rejection sampling
+// with residual and bonus, row draws, temperature / top-p preparation).
+//
+// Method: "DFlash vs DFlash 2" (blog), section "The problem: one expensive
+// token at a time" — accept y ~ q with probability min(1, p(y)/q(y)); at the
+// first rejection draw from the normalised [p - q]+; if every draft survives
+// draw a bonus token from the target's next distribution.  Sampling settings
+// (temperature 0.7, top-p 0.99): model card "Beam-1.0-501B-A23B-DFlash2",
+// section "Acceptance length".
+//
+// Design: every vocabulary row is split into chunks of kRowChunk floats, one
+// CTA per (chunk, row), so that even one request keeps many SMs streaming.
+// Each CTA reduces its chunk (a packed argmax key, or fixed-point masses) and
+// the last CTA of a request — found with an atomic ticket after a memory
+// fence — finishes the request: prefix match, or the integer inverse-CDF
+// draw, which re-reads only the one chunk that holds the sampled index.  The
+// tickets are reset by that last CTA, so the scratch needs no clearing
+// between calls.  All draws are integer arithmetic on floor(w * 2^45), which
+// makes them independent of summation order.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dfl {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
+  return ((unsigned long long)ordered_key(v) << 32) | (uint32_t)(~(uint32_t)idx);
+}
+
+// Fixed-point mass of `wfn(v)` over [v0, v1), strided by the block.
+template <class WFn>
+__device__ __forceinline__ unsigned long long chunk_mass(const WFn& wfn, int v0, int v1) {
+  unsigned long long z = 0;
+  int v = v0 + threadIdx.x;
+  for (; v + 3 * kThreads < v1; v += 4 * kThreads) {
+    const float a = wfn(v), b = wfn(v + kThreads), c = wfn(v + 2 * kThreads),
+                d = wfn(v + 3 * kThreads);
+    z += to_fixed45(a) + to_fixed45(b) + to_fixed45(c) + to_fixed45(d);
+  }
+  for (; v < v1; v += kThreads) z += to_fixed45(wfn(v));
+  return z;
+}
+
+// Smallest v in [v0, v1) whose running fixed-point mass (from v0) exceeds T.
+// Requires T < mass([v0, v1)).  Result on all threads (-1 if not found).
+template <class WFn>
+__device__ int find_in_chunk(const WFn& wfn, int v0, int v1, unsigned long long T,
+                             unsigned long long* scratch, int* s_found) {
+  const int len = v1 - v0;
+  const int seg = (len + kThreads - 1) / kThreads;
+  const int s0 = min(v1, v0 + (int)threadIdx.x * seg);
+  const int s1 = min(v1, s0 + seg);
+  unsigned long long local = 0;
+  for (int v = s0; v < s1; ++v) local += to_fixed45(wfn(v));
+  unsigned long long total;
+  const unsigned long long excl = block_exclusive_scan(local, scratch, &total);
+  if (threadIdx.x == 0) *s_found = -1;
+  __syncthreads();
+  if (local > 0 && T >= excl && T < excl + local) {
+    unsigned long long acc = excl;
+    for (int v = s0; v < s1; ++v) {
+      acc += to_fixed45(wfn(v));
+      if (acc > T) {
+        *s_found = v;
+        break;
+      }
+    }
+  }
+  __syncthreads();
+  return *s_found;
+}
+
+// ------------------------------------------------------------------ greedy
+
+__global__ void __launch_bounds__(kThreads)
+    verify_greedy_kernel(const float* __restrict__ target, const int32_t* __restrict__ draft,
+                         int gamma, int V, int chunks, int32_t* __restrict__ accept_len,
+                         int32_t* __restrict__ tokens, int* counters, unsigned long long* keys) {
+  __shared__ unsigned long long red[33];
+  __shared__ int s_last;
+  const int c = blockIdx.x;
+  const int r = blockIdx.y;  // b * gamma + i
+  const int b = r / gamma;
+  const float* row = target + (size_t)r * V;
+  const int v0 = c * kRowChunk;
+  const int v1 = min(V, v0 + kRowChunk);
+
+  unsigned long long best = 0ull;
+  int v = v0 + threadIdx.x;
+  for (; v + 3 * kThreads < v1; v += 4 * kThreads) {
+    const float a = __ldg(row + v), bb = __ldg(row + v + kThreads),
+                cc = __ldg(row + v + 2 * kThreads), d = __ldg(row + v + 3 * kThreads);
+    unsigned long long k0 = argmax_key(a, v), k1 = argmax_key(bb, v + kThreads),
+                       k2 = argmax_key(cc, v + 2 * kThreads), k3 = argmax_key(d, v + 3 * kThreads);
+    k0 = k1 > k0 ? k1 : k0;
+    k2 = k3 > k2 ? k3 : k2;
+    k0 = k2 > k0 ? k2 : k0;
+    best = k0 > best ? k0 : best;
+  }
+  for (; v < v1; v += kThreads) {
+    const unsigned long long k = argmax_key(__ldg(row + v), v);
+    best = k > best ? k : best;
+  }
+  best = block_max_u64(best, red);
+  if (threadIdx.x == 0) {
+    atomicMax(&keys[r], best);
+    __threadfence();
+    s_last = (atomicAdd(&counters[b], 1) == chunks * gamma - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int G = gamma - 1;
+    int n = 0;
+    bool match = true;
+    for (int i = 0; i < gamma; ++i) {
+      const unsigned long long k = atomicExch(&keys[b * gamma + i], 0ull);
+      const int a = (int)(~(uint32_t)(k & 0xFFFFFFFFull));
+      int32_t t = -1;
+      if (match) {
+        t = a;
+        if (i < G && draft[b * G + i] == a)
+          n = i + 1;
+        else
+          match = false;
+      }
+      tokens[b * gamma + i] = t;
+    }
+    accept_len[b] = n;
+    atomicExch(&counters[b], 0);
+  }
+}
+
+// ----------------------------------------------------------------- sampled
+
+struct ResidW {
+  const float* p;
+  const float* q;
+  __device__ __forceinline__ float operator()(int v) const {
+    return fmaxf(__fsub_rn(__ldg(p + v), __ldg(q + v)), 0.0f);
+  }
+};
+struct RowW {
+  const float* p;
+  __device__ __forceinline__ float operator()(int v) const { return __ldg(p + v); }
+};
+
+__global__ void __launch_bounds__(kThreads)
+    verify_sampled_kernel(const float* __restrict__ p, const float* __restrict__ q,
+                          const int32_t* __restrict__ draft, const uint64_t* __restrict__ seeds,
+                          uint64_t step, int gamma, int V, int chunks,
+                          int32_t* __restrict__ accept_len, int32_t* __restrict__ tokens,
+                          int* counters, unsigned long long* zsum, int* status) {
+  __shared__ unsigned long long red[33];
+  __shared__ int s_n, s_last, s_chunk, s_use_resid, s_found;
+  __shared__ unsigned long long s_T;
+  const int c = blockIdx.x, b = blockIdx.y, G = gamma - 1;
+  const uint64_t seed = seeds[b];
+
+  // Accept tests: every CTA of the request derives the same n.
+  if (threadIdx.x == 0) {
+    int n = G;
+    for (int i = 0; i < G; ++i) {
+      const int y = draft[b * G + i];
+      if (y < 0 || y >= V) {
+        report_status(status, DFLASH_ERR_ARG);
+        n = i;
+        break;
+      }
+      const uint4 w = philox_draw(seed, step, (uint32_t)i, kPurposeAccept);
+      const double u = (double)(w.x >> 8) * 0x1p-24;
+      const double qy = (double)q[((size_t)b * G + i) * V + y];
+      const double py = (double)p[((size_t)b * gamma + i) * V + y];
+      if (!(u * qy < py)) {  // exact: 24-bit x 24-bit mantissas
+        n = i;
+        break;
+      }
+    }
+    s_n = n;
+  }
+  __syncthreads();
+  const int n = s_n;
+  const bool rejected = n < G;
+  const float* prow = p + ((size_t)b * gamma + n) * V;
+  const float* qrow = q + ((size_t)b * G + (rejected ? n : 0)) * V;
+  const int v0 = c * kRowChunk, v1 = min(V, v0 + kRowChunk);
+
+  unsigned long long zr = 0, zp;
+  zp = chunk_mass(RowW{prow}, v0, v1);
+  if (rejected) zr = chunk_mass(ResidW{prow, qrow}, v0, v1);
+  zp = block_sum(zp, red);
+  zr = block_sum(zr, red);
+  if (threadIdx.x == 0) {
+    zsum[((size_t)b * chunks + c) * 2 + 0] = zr;
+    zsum[((size_t)b * chunks + c) * 2 + 1] = zp;
+    __threadfence();
+    s_last = (atomicAdd(&counters[b], 1) == chunks - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (threadIdx.x == 0) {
+    unsigned long long Zr = 0, Zp = 0;
+    for (int k = 0; k < chunks; ++k) {
+      Zr += __ldcg(&zsum[((size_t)b * chunks + k) * 2 + 0]);
+      Zp += __ldcg(&zsum[((size_t)b * chunks + k) * 2 + 1]);
+    }
+    const int use_r = rejected && Zr > 0;
+    const unsigned long long Z = use_r ? Zr : Zp;
+    const uint4 w = philox_draw(seed, step, (uint32_t)n, kPurposeResidual);
+    const unsigned long long u64 = ((unsigned long long)w.y << 32) | w.z;
+    const unsigned long long T = __umul64hi(u64, Z);
+    unsigned long long acc = 0;
+    int ck = -1;
+    for (int k = 0; k < chunks; ++k) {
+      const unsigned long long z = __ldcg(&zsum[((size_t)b * chunks + k) * 2 + (use_r ? 0 : 1)]);
+      if (T < acc + z) {
+        ck = k;
+        break;
+      }
+      acc += z;
+    }
+    if (Z == 0) report_status(status, DFLASH_ERR_ARG);
+    s_use_resid = use_r;
+    s_chunk = ck;
+    s_T = T - acc;
+  }
+  __syncthreads();
+  int tok = -1;
+  if (s_chunk >= 0) {
+    const int c0 = s_chunk * kRowChunk, c1 = min(V, c0 + kRowChunk);
+    tok = s_use_resid ? find_in_chunk(ResidW{prow, qrow}, c0, c1, s_T, red, &s_found)
+                      : find_in_chunk(RowW{prow}, c0, c1, s_T, red, &s_found);
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < gamma; ++i) {
+      int32_t t = -1;
+      if (i < n) t = draft[b * G + i];
+      if (i == n) t = tok;
+      tokens[b * gamma + i] = t;
+    }
+    accept_len[b] = n;
+    atomicExch(&counters[b], 0);
+  }
+}
+
+// --------------------------------------------------------------- row draws
+
+__global__ void __launch_bounds__(kThreads)
+    sample_rows_kernel(const float* __restrict__ w, long long row_stride, int V, int chunks,
+                       int rows_per_req, const uint64_t* __restrict__ seeds, uint64_t step,
+                       uint32_t purpose, int32_t* __restrict__ out, long long out_stride,
+                       int* counters, unsigned long long* zsum, int* status) {
+  __shared__ unsigned long long red[33];
+  __shared__ int s_last, s_chunk, s_found;
+  __shared__ unsigned long long s_T;
+  const int c = blockIdx.x, r = blockIdx.y;
+  const float* row = w + (size_t)r * row_stride;
+  const int v0 = c * kRowChunk, v1 = min(V, v0 + kRowChunk);
+  unsigned long long z = block_sum(chunk_mass(RowW{row}, v0, v1), red);
+  if (threadIdx.x == 0) {
+    zsum[(size_t)r * chunks + c] = z;
+    __threadfence();
+    s_last = (atomicAdd(&counters[r], 1) == chunks - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int b = r / rows_per_req, i = r % rows_per_req;
+  if (threadIdx.x == 0) {
+    unsigned long long Z = 0;
+    for (int k = 0; k < chunks; ++k) Z += __ldcg(&zsum[(size_t)r * chunks + k]);
+    const uint4 wd = philox_draw(seeds[b], step, (uint32_t)i, purpose);
+    const unsigned long long u64 = ((unsigned long long)wd.y << 32) | wd.z;
+    const unsigned long long T = __umul64hi(u64, Z);
+    unsigned long long acc = 0;
+    int ck = -1;
+    for (int k = 0; k < chunks; ++k) {
+      const unsigned long long zk = __ldcg(&zsum[(size_t)r * chunks + k]);
+      if (T < acc + zk) {
+        ck = k;
+        break;
+      }
+      acc += zk;
+    }
+    if (Z == 0) report_status(status, DFLASH_ERR_ARG);
+    s_chunk = ck;
+    s_T = T - acc;
+  }
+  __syncthreads();
+  int tok = -1;
+  if (s_chunk >= 0) {
+    const int c0 = s_chunk * kRowChunk, c1 = min(V, c0 + kRowChunk);
+    tok = find_in_chunk(RowW{row}, c0, c1, s_T, red, &s_found);
+  }
+  if (threadIdx.x == 0) {
+    out[(size_t)b * out_stride + i] = tok;
+    atomicExch(&counters[r], 0);
+  }
+}
+
+// -------------------------------------------------- temperature and top-p
+
+constexpr int kProbThreads = 1024;
+
+struct SoftmaxRow {
+  const float* row;
+  float invT, M, S;
+  // z = l / T - M (one fused rounding), e = exp(z), p = e / S: the same
+  // instruction sequence wherever a probability is needed.
+  __device__ __forceinline__ float operator()(int v) const {
+    return __fdiv_rn(expf(__fmaf_rn(__ldg(row + v), invT, -M)), S);
+  }
+};
+
+// Warp-aggregated add of (mass, count) into a 256-bin shared histogram.
+__device__ __forceinline__ void hist_add(unsigned long long* hist, unsigned* histc, bool active,
+                                         uint32_t digit, unsigned long long mass) {
+  const unsigned act = __ballot_sync(0xffffffffu, active);
+  if (!active) return;
+  const unsigned grp = __match_any_sync(act, digit);
+  const unsigned lo = __reduce_add_sync(grp, (unsigned)(mass & 0x7FFFFFu));
+  const unsigned hi = __reduce_add_sync(grp, (unsigned)(mass >> 23));
+  const int lane = threadIdx.x & 31;
+  if (lane == __ffs(grp) - 1) {
+    atomicAdd(&hist[digit], ((unsigned long long)hi << 23) + lo);
+    atomicAdd(&histc[digit], (unsigned)__popc(grp));
+  }
+}
+
+__global__ void __launch_bounds__(kProbThreads)
+    probs_kernel(const float* __restrict__ logits, int V, float invT, float top_p,
+                 float* __restrict__ probs) {
+  __shared__ float redf[33];
+  __shared__ unsigned long long redu[33];
+  __shared__ unsigned long long hist[256];
+  __shared__ unsigned histc[256];
+  __shared__ unsigned long long s_above, s_thr;
+  __shared__ uint32_t s_prefix, s_mask, s_ntie;
+  const int r = blockIdx.x;
+  const float* row = logits + (size_t)r * V;
+  float* out = probs + (size_t)r * V;
+
+  // max of l / T, then the normaliser
+  float m = -INFINITY;
+  for (int v = threadIdx.x; v < V; v += kProbThreads) m = fmaxf(m, __ldg(row + v) * invT);
+  m = warp_max_f(m);
+  if ((threadIdx.x & 31) == 0) redf[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float t = redf[threadIdx.x];
+    t = warp_max_f(t);
+    if (threadIdx.x == 0) redf[32] = t;
+  }
+  __syncthreads();
+  const float M = redf[32];
+  float s = 0.0f;
+  for (int v = threadIdx.x; v < V; v += kProbThreads)
+    s += expf(__fmaf_rn(__ldg(row + v), invT, -M));
+  s = block_sum(s, redf);
+  const SoftmaxRow P{row, invT, M, s};
+
+  if (!(top_p < 1.0f)) {
+    for (int v = threadIdx.x; v < V; v += kProbThreads) out[v] = P(v);
+    return;
+  }
+
+  // Fixed-point total and the nucleus threshold thr = ceil(top_p * Z).
+  unsigned long long Z = 0;
+  for (int v = threadIdx.x; v < V; v += kProbThreads) Z += to_fixed45(P(v));
+  Z = block_sum(Z, redu);
+  if (threadIdx.x == 0) {
+    unsigned long long thr = (unsigned long long)ceil((double)top_p * (double)Z);
+    if (thr == 0) thr = 1;
+    if (thr > Z) thr = Z;
+    s_thr = thr;
+    s_above = 0;
+    s_prefix = 0;
+    s_mask = 0;
+  }
+  __syncthreads();
+
+  // Radix select, 8 bits per pass, on the bit pattern of p (p >= 0, so the
+  // pattern orders like the value): find the largest key t* whose mass of
+  // {key >= t*} reaches thr.  s_above ends as the mass of {key > t*}.
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += kProbThreads) {
+      hist[i] = 0;
+      histc[i] = 0;
+    }
+    __syncthreads();
+    const uint32_t prefix = s_prefix, mask = s_mask;
+    for (int v0 = 0; v0 < V; v0 += kProbThreads) {
+      const int v = v0 + threadIdx.x;
+      float pv = 0.0f;
+      if (v < V) pv = P(v);
+      const uint32_t key = __float_as_uint(pv);
+      const bool act = (v < V) && ((key & mask) == prefix);
+      hist_add(hist, histc, act, (key >> shift) & 255u, to_fixed45(pv));
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      unsigned long long cum = s_above;
+      int sel = 0;
+      for (int d = 255; d >= 0; --d) {
+        if (cum + hist[d] >= s_thr) {
+          sel = d;
+          break;
+        }
+        cum += hist[d];
+      }
+      s_above = cum;
+      s_prefix = prefix | ((uint32_t)sel << shift);
+      s_mask = mask | (255u << shift);
+      s_ntie = histc[sel];
+    }
+    __syncthreads();
+  }
+  const uint32_t tstar = s_prefix;
+  const unsigned long long above = s_above;
+  const unsigned long long pstar = to_fixed45(__uint_as_float(tstar));
+  const unsigned n_tie = s_ntie;
+  unsigned long long k_tie = (s_thr - above + pstar - 1) / pstar;  // pstar > 0 by construction
+  if (k_tie > n_tie) k_tie = n_tie;
+  const unsigned long long kept = above + k_tie * pstar;
+  const float Sk = (float)((double)kept * 0x1p-45);
+
+  if (k_tie == n_tie) {
+    for (int v = threadIdx.x; v < V; v += kProbThreads) {
+      const float pv = P(v);
+      out[v] = (__float_as_uint(pv) >= tstar) ? __fdiv_rn(pv, Sk) : 0.0f;
+    }
+    return;
+  }
+  // Some ties at t* are dropped: keep the lowest ids.  Contiguous segments
+  // per thread give an id-ordered rank through one block scan.
+  const int seg = (V + kProbThreads - 1) / kProbThreads;
+  const int s0 = min(V, (int)threadIdx.x * seg), s1 = min(V, s0 + seg);
+  unsigned long long nt = 0;
+  for (int v = s0; v < s1; ++v) nt += (__float_as_uint(P(v)) == tstar);
+  unsigned long long tot;
+  unsigned long long rank = block_exclusive_scan(nt, redu, &tot);
+  for (int v = s0; v < s1; ++v) {
+    const float pv = P(v);
+    const uint32_t key = __float_as_uint(pv);
+    bool keep = key > tstar;
+    if (key == tstar) keep = (rank++ < k_tie);
+    out[v] = keep ? __fdiv_rn(pv, Sk) : 0.0f;
+  }
+}
+
+}  // namespace
+
+int launch_verify_greedy(int B, int gamma, int V, const float* target, const int32_t* draft,
+                         int32_t* accept_len, int32_t* tokens, int* counters,
+                         unsigned long long* keys, int* /*status*/, cudaStream_t s) {
+  const int chunks = row_chunks(V);
+  dim3 grid(chunks, B * gamma);
+  verify_greedy_kernel<<<grid, kThreads, 0, s>>>(target, draft, gamma, V, chunks, accept_len,
+                                                 tokens, counters, keys);
+  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_LAUNCH;
+}
+
+int launch_verify_sampled(int B, int gamma, int V, const float* p, const float* q,
+                          const int32_t* draft, const uint64_t* seeds, uint64_t step,
+                          int32_t* accept_len, int32_t* tokens, int* counters,
+                          unsigned long long* zsum, int* status, cudaStream_t s) {
+  const int chunks = row_chunks(V);
+  dim3 grid(chunks, B);
+  verify_sampled_kernel<<<grid, kThreads, 0, s>>>(p, q, draft, seeds, step, gamma, V, chunks,
+                                                  accept_len, tokens, counters, zsum, status);
+  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_LAUNCH;
+}
+
+int launch_sample_rows(int rows, int V, const float* w, long long row_stride, int rows_per_req,
+                       const uint64_t* seeds, uint64_t step, uint32_t purpose, int32_t* out,
+                       long long out_stride, int* counters, unsigned long long* zsum, int* status,
+                       cudaStream_t s) {
+  const int chunks = row_chunks(V);
+  dim3 grid(chunks, rows);
+  sample_rows_kernel<<<grid, kThreads, 0, s>>>(w, row_stride, V, chunks, rows_per_req, seeds, step,
+                                               purpose, out, out_stride, counters, zsum, status);
+  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_LAUNCH;
+}
+
+int launch_probs(int rows, int V, const float* logits, float temperature, float top_p,
+                 float* probs, cudaStream_t s) {
+  probs_kernel<<<rows, kProbThreads, 0, s>>>(logits, V, 1.0f / temperature, top_p, probs);
+  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_LAUNCH;
+}
+
+}  // namespace dfl

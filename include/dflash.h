@@ -1,0 +1,247 @@
+/*
+ * dflash.h — C ABI of libdflash.so: single-pass block drafting with target
+ * context injection, plus lossless verification, on one GB300 (sm_103a).
+ *
+ * What the library computes (sources are the three pages this build follows):
+ *   - "DFlash vs DFlash 2" (blog), section "Conditioning on the target model":
+ *       H_t = RMSNorm(W_c [H^(l1); ...; H^(l5)]),
+ *       Q_i = W^Q_i H_d,  K_i = [W^K_i H_t ; W^K_i H_d],  V_i = [W^V_i H_t ; W^V_i H_d];
+ *     target features enter only through keys and values; block positions
+ *     attend to one another non-causally.
+ *   - same page, section "DFlash: generate the block all at once": one
+ *     masked, bidirectional pass over [anchor, MASK, MASK, ...] through a
+ *     small stack of Qwen-style layers, shared embedding and LM head.
+ *   - same page, section "The problem: one expensive token at a time":
+ *     greedy verification accepts drafts that match the target's choice;
+ *     sampled verification accepts y ~ q with probability min(1, p(y)/q(y)),
+ *     resamples from the normalised [p - q]+ at the first rejection and emits
+ *     a bonus token from the target's next distribution when every draft
+ *     survives.
+ *   - "Speculative decoding" (product doc), section "How it works", and the
+ *     model card "Beam-1.0-501B-A23B-DFlash2", section "Model": a 4,096-token
+ *     sliding window over the context, top candidates kept per position,
+ *     5 layers, hidden 5120, 40 query / 8 KV heads of dim 128, SwiGLU 17,408,
+ *     vocabulary 151,936.
+ *
+ * Conventions this library fixes where the pages are silent:
+ *   - RoPE (rotate-half pairs (j, j + hd/2), inv_freq_j = theta^(-2j/hd)) on
+ *     queries and keys at absolute positions; context keys are stored rotated.
+ *   - Pre-norm layers; RMSNorm(x) = x / sqrt(mean(x^2) + eps) * g; SwiGLU MLP
+ *     W_down(silu(W_gate h) * W_up h); final RMSNorm before the LM head.
+ *   - A context of length L (positions 0..L-1 have target features) puts the
+ *     block at positions L..L+gamma-1; the context key at position s is visible
+ *     iff L - W <= s < L; block row j >= 1 predicts the token at L + j, so the
+ *     LM head runs on the gamma - 1 MASK rows.
+ *   - Randomness: Philox-4x32-10 keyed by a per-request 64-bit seed, counter
+ *     (step_lo, step_hi, position, purpose), purpose 0 = draft draw, 1 = accept
+ *     test, 2 = residual / bonus draw.  Accept iff (u24 * 2^-24) * q(y) < p(y)
+ *     evaluated exactly; every draw is an integer inverse CDF over
+ *     floor(weight * 2^45).
+ *
+ * Memory and ownership.  Every pointer argument, unless it says "host", is
+ * device memory owned by the caller.  The handle holds only host metadata
+ * (sizes and TMA descriptors of the caller's weights); no call allocates
+ * device memory.  Calls are asynchronous on the given stream, never
+ * synchronise the host, and may be captured into a CUDA graph.
+ *
+ * Workspace.  draft_block, ctx_append, probs and verify take a caller-owned
+ * device workspace of at least the size the matching *_workspace_bytes
+ * function returns, 256-byte aligned, ZERO-FILLED BEFORE ITS FIRST USE.  The
+ * library leaves the workspace's counter region zeroed after every call, so
+ * it can be reused without clearing.  The first 4 bytes of every workspace are
+ * a device status word: 0, or a DFLASH_ERR_* code written by a kernel (for
+ * example a bounded wait that gave up).  Calls that share one workspace must
+ * not overlap on the GPU.
+ *
+ * Errors.  Every function returns DFLASH_OK (0) or a negative DFLASH_ERR_*
+ * code after validating its arguments on the host; nothing is launched when
+ * validation fails.  No C++ exception crosses this boundary.
+ */
+#ifndef DFLASH_H_
+#define DFLASH_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dflash_stream_t; /* a cudaStream_t */
+
+enum {
+  DFLASH_OK = 0,
+  DFLASH_ERR_ARG = -1,            /* null pointer or invalid scalar argument */
+  DFLASH_ERR_SHAPE = -2,          /* sizes out of range or inconsistent */
+  DFLASH_ERR_ALIGN = -3,          /* a pointer is not 16-byte aligned */
+  DFLASH_ERR_UNSUPPORTED = -4,    /* a configuration the kernels do not cover */
+  DFLASH_ERR_LAUNCH = -5,         /* a kernel launch failed */
+  DFLASH_ERR_DEVICE_TIMEOUT = -6, /* device status: a bounded wait gave up */
+  DFLASH_ERR_WORKSPACE = -7,      /* workspace missing or too small */
+  DFLASH_ERR_CUDA = -8            /* a CUDA runtime / driver call failed */
+};
+
+enum { DFLASH_VERIFY_GREEDY = 0, DFLASH_VERIFY_SAMPLED = 1 };
+
+/* Drafter dimensions.  Constraints checked by dflash_create: head_dim is 64
+ * or 128; hidden, ffn, n_q_heads*head_dim and n_feat*feat_dim are multiples
+ * of 64; n_q_heads is a multiple of n_kv_heads; 1 <= gamma_max <= 16;
+ * 1 <= topk_max <= 16; window >= 1. */
+typedef struct dflash_config {
+  int hidden;      /* d */
+  int n_q_heads;   /* Hq */
+  int n_kv_heads;  /* Hkv */
+  int head_dim;    /* hd */
+  int ffn;         /* SwiGLU width F */
+  int vocab;       /* V */
+  int n_layers;    /* NL */
+  int n_feat;      /* number of target layers read (5) */
+  int feat_dim;    /* width of each target feature */
+  int window;      /* W, sliding-window length of the context cache */
+  int gamma_max;   /* largest block size any call will use */
+  int topk_max;    /* largest per-position top-k any call will use */
+  int batch_max;   /* largest B any draft_block / ctx_append call will use */
+  int append_max;  /* largest rows per request of one ctx_append call */
+  float rope_theta;
+  float eps;
+  int mask_id;     /* MASK token id; -1 selects vocab - 1 */
+} dflash_config;
+
+/* One drafter layer.  Matrices are bf16 row-major [out, in] (the torch Linear
+ * layout), gains are float32.  All device pointers, 16-byte aligned. */
+typedef struct dflash_layer_weights {
+  const void* g_attn; /* float32 [d] */
+  const void* w_qkv;  /* bf16 [(Hq + 2 Hkv) hd, d]: q rows, then k rows, then v rows */
+  const void* w_o;    /* bf16 [d, Hq hd] */
+  const void* g_mlp;  /* float32 [d] */
+  const void* w_gate; /* bf16 [F, d] */
+  const void* w_up;   /* bf16 [F, d] */
+  const void* w_down; /* bf16 [d, F] */
+} dflash_layer_weights;
+
+typedef struct dflash_weights {
+  const void* embed;   /* bf16 [V, d], shared with the target */
+  const void* lm_head; /* bf16 [V, d], shared with the target */
+  const void* w_c;     /* bf16 [d, n_feat * feat_dim] */
+  const void* g_c;     /* float32 [d], gain of the RMSNorm that forms H_t */
+  const void* g_final; /* float32 [d] */
+  const dflash_layer_weights* layers; /* HOST array of n_layers entries */
+} dflash_weights;
+
+typedef struct dflash_handle dflash_handle;
+
+/* Validate cfg, record the weight pointers and encode their TMA descriptors.
+ * The weights must stay alive and unchanged while the handle is used.
+ * Must be called with the weights' device current.  Returns DFLASH_OK and
+ * *out, or an error (then *out is NULL). */
+int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_handle** out);
+int dflash_destroy(dflash_handle* h);
+
+/* Bytes of workspace each call needs for the handle's limits. */
+size_t dflash_draft_workspace_bytes(const dflash_handle* h);
+size_t dflash_append_workspace_bytes(const dflash_handle* h);
+size_t dflash_verify_workspace_bytes(int batch, int gamma, int vocab);
+size_t dflash_probs_workspace_bytes(int rows, int vocab);
+
+/* Context injection ("Conditioning on the target model": H_t equation and the
+ * K/V injection equation).  For every request b and row j < n_new[b]:
+ *   pos = ctx_len[b] + j,
+ *   H_t = RMSNorm(W_c concat(feats[b, j, 0..nf-1, :])),
+ *   for each layer i: ring_k[i, slot(b), :, pos mod W, :] = RoPE(W^K_i H_t, pos),
+ *                     ring_v[i, slot(b), :, pos mod W, :] = W^V_i H_t,
+ * then ctx_len[b] += n_new[b].  Rows j >= n_new[b] are ignored.  To append
+ * only the last W positions of a long prompt, set ctx_len[b] to the position
+ * of the first appended row before the call.
+ *   B            requests in this call, 1..batch_max
+ *   n_max        rows per request in feats, 1..append_max
+ *   feats        bf16 [B, n_max, n_feat, feat_dim]
+ *   n_new        int32 [B], each in [0, n_max]
+ *   ctx_len      int64 [B], in/out
+ *   req_slot     int32 [B] ring row of each request, or NULL for slot(b) = b
+ *   ring_k/v     bf16 [n_layers, ring_batch, Hkv, W, hd]
+ */
+int dflash_ctx_append(dflash_handle* h, int B, int n_max, const void* feats,
+                      const int32_t* n_new, int64_t* ctx_len, const int32_t* req_slot,
+                      void* ring_k, void* ring_v, int ring_batch,
+                      void* workspace, size_t ws_bytes, dflash_stream_t stream);
+
+/* Sampling parameters of draft_block (host struct).  temperature > 0. */
+typedef struct dflash_sampling {
+  float temperature;     /* logits are divided by it before the softmax */
+  float top_p;           /* nucleus mass in (0, 1]; 1 disables it */
+  const uint64_t* seeds; /* device [B] Philox keys, one per request */
+  uint64_t step;         /* Philox step (counter words 0-1) */
+} dflash_sampling;
+
+/* Outputs of draft_block (host struct of device pointers; NULL = not wanted). */
+typedef struct dflash_draft_out {
+  int32_t* topk_ids; /* int32 [B, gamma-1, topk], descending logit, ties to lower id */
+  float* topk_vals;  /* float32 [B, gamma-1, topk] logits of those ids */
+  float* lse;        /* float32 [B, gamma-1] log-sum-exp of each row's logits */
+  float* logits;     /* float32 [B, gamma-1, V] raw logits */
+  float* q;          /* float32 [B, gamma-1, V] q = top_p(softmax(logits / T));
+                        requires sampling */
+  int32_t* draft;    /* int32 [B, gamma-1] proposed tokens: the top-1 id, or
+                        with sampling y ~ q (Philox purpose 0, position j) */
+} dflash_draft_out;
+
+/* One single-pass block draft per request ("DFlash: generate the block all at
+ * once"; "Conditioning on the target model").  Block ids are
+ * [anchor[b], MASK x (gamma-1)] at positions ctx_len[b] .. ctx_len[b]+gamma-1;
+ * every layer attends over [visible context window ; whole block].
+ *   B          1..batch_max;  gamma 2..gamma_max;  topk 0..topk_max
+ *   anchor     int32 [B];  ctx_len int64 [B] (0 allowed: the block alone)
+ *   req_slot   int32 [B] or NULL;  ring_k/v as in ctx_append
+ *   sampling   host pointer or NULL (greedy drafting)
+ */
+int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor,
+                       const int64_t* ctx_len, const int32_t* req_slot,
+                       const void* ring_k, const void* ring_v, int ring_batch, int topk,
+                       const dflash_sampling* sampling, const dflash_draft_out* out,
+                       void* workspace, size_t ws_bytes, dflash_stream_t stream);
+
+/* Sampling distribution of raw logits: probs = top_p(softmax(logits / T)),
+ * renormalised (model card "Beam-1.0-501B-A23B-DFlash2", section "Acceptance
+ * length": temperature 0.7, top-p 0.99).  Nucleus: ids ordered by
+ * (probability desc, id asc), the shortest prefix whose mass reaches top_p.
+ *   logits, probs  float32 [rows, V] (may not alias) */
+int dflash_probs(int rows, int vocab, const float* logits, float temperature, float top_p,
+                 float* probs, void* workspace, size_t ws_bytes, dflash_stream_t stream);
+
+/* Verification ("The problem: one expensive token at a time").
+ *   mode GREEDY:  target = target logits float32 [B, gamma, V]; q, seeds unused.
+ *                 n = longest prefix with draft[b, i] == argmax target[b, i]
+ *                 (ties to the lowest id); tokens[n] = argmax target[b, n].
+ *   mode SAMPLED: target = p float32 [B, gamma, V], q float32 [B, gamma-1, V],
+ *                 rows normalised; accept draft i iff
+ *                 (u24_i * 2^-24) q_i(y_i) < p_i(y_i) (Philox purpose 1,
+ *                 position i); at the first rejection j draw from
+ *                 max(0, p_j - q_j) (float32), or from p_j if that has zero
+ *                 mass; if all survive draw the bonus from p_{gamma-1}
+ *                 (Philox purpose 2, position n).
+ *   draft      int32 [B, gamma-1]
+ *   accept_len int32 [B] out: n in [0, gamma-1]; tau = n + 1
+ *   tokens     int32 [B, gamma] out: drafts 0..n-1, the correction or bonus
+ *              at n, -1 after. */
+int dflash_verify(int mode, int B, int gamma, int vocab, const float* target, const float* q,
+                  const int32_t* draft, const uint64_t* seeds, uint64_t step,
+                  int32_t* accept_len, int32_t* tokens,
+                  void* workspace, size_t ws_bytes, dflash_stream_t stream);
+
+/* Copy the workspace status word to the host (synchronises the stream). */
+int dflash_read_status(const void* workspace, int32_t* status_host, dflash_stream_t stream);
+
+const char* dflash_strerror(int code);
+
+/* Self-test of the bounded-wait machinery every pipelined kernel uses: one
+ * CTA waits on a shared-memory mbarrier that nothing arrives on, gives up
+ * after `limit_ns` nanoseconds (clamped to 1 s) and writes
+ * DFLASH_ERR_DEVICE_TIMEOUT into the workspace status word.  The GPU context
+ * stays usable.  workspace: >= 256 bytes, its status word is overwritten. */
+int dflash_selftest_timeout(void* workspace, long long limit_ns, dflash_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH_H_ */
