@@ -96,6 +96,8 @@ def lib():
         "dflash_read_status": (_I, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
         "dflash_strerror": (ctypes.c_char_p, [_I]),
         "dflash_selftest_timeout": (_I, [_P, ctypes.c_longlong, _P]),
+        "dflash_sample_draft": (_I, [_I, _I, _I, _P, _P, ctypes.c_uint64, _P, _P, _SZ, _P]),
+        "dflash_sample_workspace_bytes": (_SZ, [_I, _I]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -252,3 +254,15 @@ def dflash_read_status(ws, stream=None):
 def dflash_selftest_timeout(ws, limit_ns=1_000_000, stream=None):
     _check(lib().dflash_selftest_timeout(_ptr(ws), int(limit_ns), _stream(stream)),
            "dflash_selftest_timeout")
+
+
+def dflash_sample_workspace_bytes(rows, vocab):
+    return int(lib().dflash_sample_workspace_bytes(rows, vocab))
+
+
+def dflash_sample_draft(q, seeds, step, y, ws, stream=None):
+    """q float32 [B, G, V]; seeds uint64 (as int64) [B]; y int32 [B, G] out."""
+    B, G, V = q.shape
+    _check(lib().dflash_sample_draft(B, G, V, _ptr(q), _ptr(seeds), ctypes.c_uint64(int(step) & (2 ** 64 - 1)),
+                                     _ptr(y), _ptr(ws), ws.numel(), _stream(stream)),
+           "dflash_sample_draft")

@@ -1,24 +1,51 @@
 // C ABI: handle, context injection and the single-pass block draft.
 // See include/dflash.h for the contract of every entry point.
+//
+// ctx_append  ("DFlash vs DFlash 2" blog, section "Conditioning on the target
+//              model", H_t equation and K/V injection equation):
+//   W_c GEMM (fp32 out) -> RMSNorm(g_c) -> per-layer K/V GEMM whose epilogue
+//   rotates K and scatters K and V into ring slot pos mod W -> ctx_len += n.
+// draft_block ("DFlash: generate the block all at once"):
+//   embed [anchor, MASK...] + RMSNorm -> for each layer: QKV GEMM (+RoPE) ->
+//   block attention over [ring window ; block] -> O GEMM (+residual) ->
+//   RMSNorm -> gate|up GEMM (+SwiGLU) -> down GEMM (+residual) -> RMSNorm
+//   (final RMSNorm gathers the gamma-1 MASK rows) -> LM head GEMM (fp32
+//   logits) -> top-k + log-sum-exp [-> q = top_p(softmax(logits / T)) ->
+//   y ~ q].
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <new>
 #include <vector>
 
+#include "attention.h"
 #include "common.cuh"
+#include "gemm.h"
 #include "kernels.h"
+#include "rowops.h"
 
 using namespace dfl;
+
+struct LayerMaps {
+  CUtensorMap qkv, o, gate, up, down;
+};
 
 struct dflash_handle {
   dflash_config cfg;
   dflash_weights w;
   std::vector<dflash_layer_weights> layers;
+  std::vector<LayerMaps> maps;
+  CUtensorMap lm_head, w_c;
+  int num_sms;
+  int mask_id;
 };
 
 namespace {
 
-bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) % 16) == 0; }
+constexpr size_t kGemmPartialFloats = 4u << 20;  // split-K partial tiles (16 MiB)
+constexpr int kGemmCounters = 8192;
+
+bool aligned(const void* p, size_t a) { return p && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int validate_config(const dflash_config& c) {
   if (c.hidden < 64 || c.hidden % 64) return DFLASH_ERR_UNSUPPORTED;
@@ -36,7 +63,127 @@ int validate_config(const dflash_config& c) {
   if (c.append_max < 1 || c.append_max > 8192) return DFLASH_ERR_UNSUPPORTED;
   if (!(c.eps > 0.0f) || !(c.rope_theta > 0.0f)) return DFLASH_ERR_ARG;
   if (c.mask_id < -1 || c.mask_id >= c.vocab) return DFLASH_ERR_ARG;
+  // query-group rows of one KV head must fit the attention kernel's tiles
+  if (attn_row_tiles(c.n_q_heads, c.n_kv_heads, c.gamma_max) > 6) return DFLASH_ERR_UNSUPPORTED;
   return DFLASH_OK;
+}
+
+int attn_splits(const dflash_handle* h, int B) {
+  const int bh = B * h->cfg.n_kv_heads;
+  const int tiles = (h->cfg.window + 63) / 64;
+  int s = (h->num_sms + bh - 1) / bh;
+  if (s > tiles) s = tiles;
+  if (s > 64) s = 64;
+  return s < 1 ? 1 : s;
+}
+
+struct DraftWs {
+  int* status;
+  int* gemm_counters;
+  int* attn_counters;
+  int* topk_counters;
+  int* samp_counters;
+  float* x;
+  void* h;
+  void* qkv;
+  void* attn;
+  void* mlp;
+  void* hf;
+  float* logits;
+  float* gemm_partial;
+  float* attn_part;
+  float* attn_ml;
+  unsigned long long* topk_keys;
+  float* topk_ml;
+  unsigned long long* samp_zsum;
+  size_t bytes;
+};
+
+DraftWs draft_layout(const dflash_handle* h, void* base) {
+  const dflash_config& c = h->cfg;
+  const size_t M = (size_t)c.batch_max * c.gamma_max;
+  const size_t R = (size_t)c.batch_max * (c.gamma_max - 1);
+  const int qkv_dim = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
+  const int q_dim = c.n_q_heads * c.head_dim;
+  const int chunks = row_chunks(c.vocab);
+  const int mq = 16 * attn_row_tiles(c.n_q_heads, c.n_kv_heads, c.gamma_max);
+  size_t attn_rows = 0;  // (request, KV head, split) triples that write partials
+  for (int B = 1; B <= c.batch_max; ++B) {
+    const int S = attn_splits(h, B);
+    if (S > 1 && (size_t)B * c.n_kv_heads * S > attn_rows) attn_rows = (size_t)B * c.n_kv_heads * S;
+  }
+  Carve cv(base, kWsHeader);
+  DraftWs w;
+  w.status = static_cast<int*>(base);
+  w.gemm_counters = cv.take<int>(kGemmCounters);
+  w.attn_counters = cv.take<int>((size_t)c.batch_max * c.n_kv_heads);
+  w.topk_counters = cv.take<int>(R);
+  w.samp_counters = cv.take<int>(R);
+  w.x = cv.take<float>(M * c.hidden);
+  w.h = cv.take<uint16_t>(M * c.hidden);
+  w.qkv = cv.take<uint16_t>(M * qkv_dim);
+  w.attn = cv.take<uint16_t>(M * q_dim);
+  w.mlp = cv.take<uint16_t>(M * c.ffn);
+  w.hf = cv.take<uint16_t>(R * c.hidden);
+  w.logits = cv.take<float>(R * c.vocab);
+  w.gemm_partial = cv.take<float>(kGemmPartialFloats);
+  w.attn_part = cv.take<float>(attn_rows * mq * c.head_dim);
+  w.attn_ml = cv.take<float>(attn_rows * mq * 2);
+  w.topk_keys = cv.take<unsigned long long>(R * chunks * 16);
+  w.topk_ml = cv.take<float>(R * chunks * 2);
+  w.samp_zsum = cv.take<unsigned long long>(R * chunks);
+  w.bytes = cv.off;
+  return w;
+}
+
+struct AppendWs {
+  int* status;
+  int* gemm_counters;
+  float* fused;
+  void* ht;
+  float* gemm_partial;
+  size_t bytes;
+};
+
+AppendWs append_layout(const dflash_handle* h, void* base) {
+  const dflash_config& c = h->cfg;
+  const size_t M = (size_t)c.batch_max * c.append_max;
+  Carve cv(base, kWsHeader);
+  AppendWs w;
+  w.status = static_cast<int*>(base);
+  w.gemm_counters = cv.take<int>(kGemmCounters);
+  w.fused = cv.take<float>(M * c.hidden);
+  w.ht = cv.take<uint16_t>(M * c.hidden);
+  w.gemm_partial = cv.take<float>(kGemmPartialFloats);
+  w.bytes = cv.off;
+  return w;
+}
+
+GemmAOpts single_map() {
+  GemmAOpts o;
+  o.n_maps = 1;
+  o.tiles_per_map = 1 << 30;
+  o.row_offset = 0;
+  o.dual = 0;
+  return o;
+}
+
+GemmEpi epi_base(int kind, int M, int N, void* out, long long ld) {
+  GemmEpi e;
+  std::memset(&e, 0, sizeof(e));
+  e.kind = kind;
+  e.M = M;
+  e.N = N;
+  e.out = out;
+  e.ld = ld;
+  return e;
+}
+
+int splits_for(const dflash_handle* h, int n_tiles, int M, int K) {
+  const int BN = gemm_token_tile(M);
+  const int m_tiles = (M + BN - 1) / BN;
+  const int per_sm = BN <= 64 ? 2 : 1;
+  return gemm_plan_splits(n_tiles * m_tiles, K, h->num_sms * per_sm);
 }
 
 }  // namespace
@@ -51,12 +198,12 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
   if (rc) return rc;
   const void* top[] = {w->embed, w->lm_head, w->w_c, w->g_c, w->g_final};
   for (const void* p : top)
-    if (!aligned16(p)) return p ? DFLASH_ERR_ALIGN : DFLASH_ERR_ARG;
+    if (!aligned(p, 16)) return p ? DFLASH_ERR_ALIGN : DFLASH_ERR_ARG;
   for (int l = 0; l < cfg->n_layers; ++l) {
     const dflash_layer_weights& L = w->layers[l];
     const void* ps[] = {L.g_attn, L.w_qkv, L.w_o, L.g_mlp, L.w_gate, L.w_up, L.w_down};
     for (const void* p : ps)
-      if (!aligned16(p)) return p ? DFLASH_ERR_ALIGN : DFLASH_ERR_ARG;
+      if (!aligned(p, 16)) return p ? DFLASH_ERR_ALIGN : DFLASH_ERR_ARG;
   }
   dflash_handle* h = new (std::nothrow) dflash_handle;
   if (!h) return DFLASH_ERR_ARG;
@@ -64,6 +211,32 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
   h->w = *w;
   h->layers.assign(w->layers, w->layers + cfg->n_layers);
   h->w.layers = h->layers.data();
+  h->mask_id = cfg->mask_id < 0 ? cfg->vocab - 1 : cfg->mask_id;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    delete h;
+    return DFLASH_ERR_CUDA;
+  }
+  const dflash_config& c = *cfg;
+  const uint64_t d = c.hidden, F = c.ffn, qd = (uint64_t)c.n_q_heads * c.head_dim;
+  const uint64_t qkv_rows = (uint64_t)(c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
+  h->maps.resize(c.n_layers);
+  rc = encode_bf16_2d(&h->lm_head, w->lm_head, d, c.vocab, 64, 128);
+  if (!rc) rc = encode_bf16_2d(&h->w_c, w->w_c, (uint64_t)c.n_feat * c.feat_dim, d, 64, 128);
+  for (int l = 0; l < c.n_layers && !rc; ++l) {
+    const dflash_layer_weights& L = h->layers[l];
+    LayerMaps& m = h->maps[l];
+    rc = encode_bf16_2d(&m.qkv, L.w_qkv, d, qkv_rows, 64, 128);
+    if (!rc) rc = encode_bf16_2d(&m.o, L.w_o, qd, d, 64, 128);
+    if (!rc) rc = encode_bf16_2d(&m.gate, L.w_gate, d, F, 64, 64);
+    if (!rc) rc = encode_bf16_2d(&m.up, L.w_up, d, F, 64, 64);
+    if (!rc) rc = encode_bf16_2d(&m.down, L.w_down, F, d, 64, 128);
+  }
+  if (rc) {
+    delete h;
+    return rc;
+  }
   *out = h;
   return DFLASH_OK;
 }
@@ -73,15 +246,78 @@ int dflash_destroy(dflash_handle* h) {
   return DFLASH_OK;
 }
 
-size_t dflash_draft_workspace_bytes(const dflash_handle* h) { return h ? kWsHeader : 0; }
-size_t dflash_append_workspace_bytes(const dflash_handle* h) { return h ? kWsHeader : 0; }
+size_t dflash_draft_workspace_bytes(const dflash_handle* h) {
+  return h ? draft_layout(h, nullptr).bytes : 0;
+}
+
+size_t dflash_append_workspace_bytes(const dflash_handle* h) {
+  return h ? append_layout(h, nullptr).bytes : 0;
+}
 
 int dflash_ctx_append(dflash_handle* h, int B, int n_max, const void* feats, const int32_t* n_new,
                       int64_t* ctx_len, const int32_t* req_slot, void* ring_k, void* ring_v,
                       int ring_batch, void* workspace, size_t ws_bytes, dflash_stream_t stream) {
-  (void)h; (void)B; (void)n_max; (void)feats; (void)n_new; (void)ctx_len; (void)req_slot;
-  (void)ring_k; (void)ring_v; (void)ring_batch; (void)workspace; (void)ws_bytes; (void)stream;
-  return DFLASH_ERR_UNSUPPORTED;
+  if (!h) return DFLASH_ERR_ARG;
+  const dflash_config& c = h->cfg;
+  if (B < 1 || B > c.batch_max || n_max < 1 || n_max > c.append_max) return DFLASH_ERR_SHAPE;
+  if (ring_batch < 1 || (!req_slot && ring_batch < B)) return DFLASH_ERR_SHAPE;
+  if (!feats || !n_new || !ctx_len || !ring_k || !ring_v) return DFLASH_ERR_ARG;
+  if (!aligned(feats, 16) || !aligned(ring_k, 16) || !aligned(ring_v, 16) || !aligned(n_new, 4) ||
+      !aligned(ctx_len, 8) || (req_slot && !aligned(req_slot, 4)))
+    return DFLASH_ERR_ALIGN;
+  if (!aligned(workspace, 256)) return DFLASH_ERR_WORKSPACE;
+  AppendWs ws = append_layout(h, workspace);
+  if (ws_bytes < ws.bytes) return DFLASH_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  GemmScratch scratch{ws.gemm_partial, kGemmPartialFloats, ws.gemm_counters, kGemmCounters, ws.status};
+  const int M = B * n_max;
+  const int d = c.hidden;
+  const int Kc = c.n_feat * c.feat_dim;
+  int rc;
+
+  // H_t before normalisation: fused = concat(features) W_c^T (fp32)
+  {
+    GemmAMaps A;
+    A.map[0] = h->w_c;
+    GemmEpi e = epi_base(EPI_F32, M, d, ws.fused, d);
+    const int nt = (d + 127) / 128;
+    rc = launch_gemm(A, single_map(), nt, feats, M, Kc, e, scratch, splits_for(h, nt, M, Kc), s, true);
+    if (rc) return rc;
+  }
+  rc = launch_rmsnorm(ws.fused, M, d, static_cast<const float*>(h->w.g_c), c.eps, 0, ws.ht, s);
+  if (rc) return rc;
+  // K/V of every layer into the ring, up to kMaxAMaps layers per launch
+  const int kvd = c.n_kv_heads * c.head_dim;
+  const int tiles_per_layer = 2 * kvd / 128;
+  for (int l0 = 0; l0 < c.n_layers; l0 += kMaxAMaps) {
+    const int nl = c.n_layers - l0 < kMaxAMaps ? c.n_layers - l0 : kMaxAMaps;
+    GemmAMaps A;
+    for (int i = 0; i < nl; ++i) A.map[i] = h->maps[l0 + i].qkv;
+    GemmAOpts ao;
+    ao.n_maps = nl;
+    ao.tiles_per_map = tiles_per_layer;
+    ao.row_offset = c.n_q_heads * c.head_dim;
+    ao.dual = 0;
+    GemmEpi e = epi_base(EPI_KV_RING, M, nl * 2 * kvd, nullptr, 0);
+    e.ctx_len = ctx_len;
+    e.rope_theta = c.rope_theta;
+    e.hd = c.head_dim;
+    e.ring_k = ring_k;
+    e.ring_v = ring_v;
+    e.ring_batch = ring_batch;
+    e.window = c.window;
+    e.n_kv = c.n_kv_heads;
+    e.kv_dim = kvd;
+    e.n_max = n_max;
+    e.n_new = n_new;
+    e.req_slot = req_slot;
+    e.layer0 = l0;
+    e.status = ws.status;
+    const int nt = nl * tiles_per_layer;
+    rc = launch_gemm(A, ao, nt, ws.ht, M, d, e, scratch, splits_for(h, nt, M, d), s, true);
+    if (rc) return rc;
+  }
+  return launch_add_lengths(B, n_new, ctx_len, s);
 }
 
 int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor,
@@ -89,10 +325,146 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
                        const void* ring_v, int ring_batch, int topk, const dflash_sampling* sampling,
                        const dflash_draft_out* out, void* workspace, size_t ws_bytes,
                        dflash_stream_t stream) {
-  (void)h; (void)B; (void)gamma; (void)anchor; (void)ctx_len; (void)req_slot; (void)ring_k;
-  (void)ring_v; (void)ring_batch; (void)topk; (void)sampling; (void)out; (void)workspace;
-  (void)ws_bytes; (void)stream;
-  return DFLASH_ERR_UNSUPPORTED;
+  if (!h || !out) return DFLASH_ERR_ARG;
+  const dflash_config& c = h->cfg;
+  if (B < 1 || B > c.batch_max || gamma < 2 || gamma > c.gamma_max) return DFLASH_ERR_SHAPE;
+  if (topk < 0 || topk > c.topk_max || topk > c.vocab) return DFLASH_ERR_SHAPE;
+  if (ring_batch < 1 || (!req_slot && ring_batch < B)) return DFLASH_ERR_SHAPE;
+  if (!anchor || !ctx_len || !ring_k || !ring_v) return DFLASH_ERR_ARG;
+  if (topk == 0 && (out->topk_ids || out->topk_vals)) return DFLASH_ERR_ARG;
+  if (sampling) {
+    if (!(sampling->temperature > 0.0f) || !(sampling->top_p > 0.0f) || !(sampling->top_p <= 1.0f) ||
+        !sampling->seeds || !out->q)
+      return DFLASH_ERR_ARG;
+    if (!aligned(sampling->seeds, 8) || !aligned(out->q, 4)) return DFLASH_ERR_ALIGN;
+  } else if (out->q) {
+    return DFLASH_ERR_ARG;
+  }
+  if (!aligned(ring_k, 16) || !aligned(ring_v, 16) || !aligned(anchor, 4) || !aligned(ctx_len, 8) ||
+      (req_slot && !aligned(req_slot, 4)))
+    return DFLASH_ERR_ALIGN;
+  const void* outs[] = {out->topk_ids, out->topk_vals, out->lse, out->logits, out->draft};
+  for (const void* p : outs)
+    if (p && !aligned(p, 4)) return DFLASH_ERR_ALIGN;
+  if (!aligned(workspace, 256)) return DFLASH_ERR_WORKSPACE;
+  DraftWs ws = draft_layout(h, workspace);
+  if (ws_bytes < ws.bytes) return DFLASH_ERR_WORKSPACE;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  GemmScratch scratch{ws.gemm_partial, kGemmPartialFloats, ws.gemm_counters, kGemmCounters, ws.status};
+  const int M = B * gamma;
+  const int R = B * (gamma - 1);
+  const int d = c.hidden, hd = c.head_dim;
+  const int qd = c.n_q_heads * hd;
+  const int qkv_dim = (c.n_q_heads + 2 * c.n_kv_heads) * hd;
+  const size_t ring_layer = (size_t)ring_batch * c.n_kv_heads * c.window * hd;
+  int rc;
+
+  rc = launch_embed_norm(h->w.embed, anchor, B, gamma, h->mask_id, c.vocab, d,
+                         static_cast<const float*>(h->layers[0].g_attn), c.eps, ws.x, ws.h,
+                         ws.status, s);
+  if (rc) return rc;
+  AttnArgs aa;
+  aa.qkv = static_cast<const __nv_bfloat16*>(ws.qkv);
+  aa.ld_qkv = qkv_dim;
+  aa.out = static_cast<__nv_bfloat16*>(ws.attn);
+  aa.ld_out = qd;
+  aa.ctx_len = ctx_len;
+  aa.req_slot = req_slot;
+  aa.gamma = gamma;
+  aa.n_q = c.n_q_heads;
+  aa.n_kv = c.n_kv_heads;
+  aa.hd = hd;
+  aa.window = c.window;
+  aa.ring_batch = ring_batch;
+  aa.splits = attn_splits(h, B);
+  aa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)hd));
+  aa.part = ws.attn_part;
+  aa.part_ml = ws.attn_ml;
+  aa.counters = ws.attn_counters;
+  aa.status = ws.status;
+
+  for (int l = 0; l < c.n_layers; ++l) {
+    const LayerMaps& lm = h->maps[l];
+    const dflash_layer_weights& L = h->layers[l];
+    {  // QKV (+RoPE on q and k)
+      GemmAMaps A;
+      A.map[0] = lm.qkv;
+      GemmEpi e = epi_base(EPI_QKV, M, qkv_dim, ws.qkv, qkv_dim);
+      e.ctx_len = ctx_len;
+      e.gamma = gamma;
+      e.rope_theta = c.rope_theta;
+      e.rope_rows = (c.n_q_heads + c.n_kv_heads) * hd;
+      e.hd = hd;
+      const int nt = (qkv_dim + 127) / 128;
+      rc = launch_gemm(A, single_map(), nt, ws.h, M, d, e, scratch, splits_for(h, nt, M, d), s, true);
+      if (rc) return rc;
+    }
+    rc = launch_attention(static_cast<const char*>(ring_k) + l * ring_layer * 2,
+                          static_cast<const char*>(ring_v) + l * ring_layer * 2, aa, B, s);
+    if (rc) return rc;
+    {  // O projection + residual
+      GemmAMaps A;
+      A.map[0] = lm.o;
+      GemmEpi e = epi_base(EPI_RESID, M, d, ws.x, d);
+      const int nt = (d + 127) / 128;
+      rc = launch_gemm(A, single_map(), nt, ws.attn, M, qd, e, scratch, splits_for(h, nt, M, qd), s, true);
+      if (rc) return rc;
+    }
+    rc = launch_rmsnorm(ws.x, M, d, static_cast<const float*>(L.g_mlp), c.eps, 0, ws.h, s);
+    if (rc) return rc;
+    {  // gate | up + SwiGLU
+      GemmAMaps A;
+      A.map[0] = lm.gate;
+      A.map[1] = lm.up;
+      GemmAOpts ao = single_map();
+      ao.n_maps = 2;
+      ao.dual = 1;
+      GemmEpi e = epi_base(EPI_SWIGLU, M, c.ffn, ws.mlp, c.ffn);
+      const int nt = c.ffn / 64;
+      rc = launch_gemm(A, ao, nt, ws.h, M, d, e, scratch, splits_for(h, nt, M, d), s, true);
+      if (rc) return rc;
+    }
+    {  // down + residual
+      GemmAMaps A;
+      A.map[0] = lm.down;
+      GemmEpi e = epi_base(EPI_RESID, M, d, ws.x, d);
+      const int nt = (d + 127) / 128;
+      rc = launch_gemm(A, single_map(), nt, ws.mlp, M, c.ffn, e, scratch,
+                       splits_for(h, nt, M, c.ffn), s, true);
+      if (rc) return rc;
+    }
+    if (l + 1 < c.n_layers)
+      rc = launch_rmsnorm(ws.x, M, d, static_cast<const float*>(h->layers[l + 1].g_attn), c.eps, 0,
+                          ws.h, s);
+    else
+      rc = launch_rmsnorm(ws.x, R, d, static_cast<const float*>(h->w.g_final), c.eps, gamma, ws.hf, s);
+    if (rc) return rc;
+  }
+  float* logits = out->logits ? out->logits : ws.logits;
+  {  // shared LM head on the gamma - 1 MASK rows
+    GemmAMaps A;
+    A.map[0] = h->lm_head;
+    GemmEpi e = epi_base(EPI_F32, R, c.vocab, logits, c.vocab);
+    const int nt = (c.vocab + 127) / 128;
+    rc = launch_gemm(A, single_map(), nt, ws.hf, R, d, e, scratch, splits_for(h, nt, R, d), s, true);
+    if (rc) return rc;
+  }
+  const int k_eff = topk > 0 ? topk : 1;
+  rc = launch_topk_lse(logits, R, c.vocab, k_eff, ws.topk_keys, ws.topk_ml, ws.topk_counters,
+                       topk > 0 ? out->topk_ids : nullptr, topk > 0 ? out->topk_vals : nullptr,
+                       out->lse, sampling ? nullptr : out->draft, s);
+  if (rc) return rc;
+  if (sampling) {
+    rc = launch_probs(R, c.vocab, logits, sampling->temperature, sampling->top_p, out->q, s);
+    if (rc) return rc;
+    if (out->draft) {
+      rc = launch_sample_rows(R, c.vocab, out->q, c.vocab, gamma - 1, sampling->seeds, sampling->step,
+                              0u, out->draft, gamma - 1, ws.samp_counters, ws.samp_zsum, ws.status, s);
+      if (rc) return rc;
+    }
+  }
+  return DFLASH_OK;
 }
 
 }  // extern "C"

@@ -82,6 +82,31 @@ int dflash_probs(int rows, int vocab, const float* logits, float temperature, fl
                       reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t dflash_sample_workspace_bytes(int rows, int vocab) {
+  if (rows < 1 || vocab < 1) return 0;
+  Carve c(nullptr, kWsHeader);
+  c.take<int>(rows);
+  c.take<unsigned long long>((size_t)rows * row_chunks(vocab));
+  return c.off;
+}
+
+int dflash_sample_draft(int B, int G, int vocab, const float* q, const uint64_t* seeds,
+                        uint64_t step, int32_t* y, void* workspace, size_t ws_bytes,
+                        dflash_stream_t stream) {
+  if (B < 1 || G < 1 || (long long)B * G > 65535 || vocab < 1 || vocab > kMaxVocab)
+    return DFLASH_ERR_SHAPE;
+  if (!q || !seeds || !y) return DFLASH_ERR_ARG;
+  if (!aligned(q, 4) || !aligned(seeds, 8) || !aligned(y, 4)) return DFLASH_ERR_ALIGN;
+  if (!workspace || !aligned(workspace, 256)) return DFLASH_ERR_WORKSPACE;
+  const int rows = B * G;
+  if (ws_bytes < dflash_sample_workspace_bytes(rows, vocab)) return DFLASH_ERR_WORKSPACE;
+  Carve c(workspace, kWsHeader);
+  int* counters = c.take<int>(rows);
+  unsigned long long* zsum = c.take<unsigned long long>((size_t)rows * row_chunks(vocab));
+  return launch_sample_rows(rows, vocab, q, vocab, G, seeds, step, kPurposeDraft, y, G, counters,
+                            zsum, static_cast<int*>(workspace), reinterpret_cast<cudaStream_t>(stream));
+}
+
 int dflash_read_status(const void* workspace, int32_t* status_host, dflash_stream_t stream) {
   if (!workspace || !status_host) return DFLASH_ERR_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -1,0 +1,440 @@
+// Block attention of the drafter: the gamma block queries of every query
+// head attend over [context window ; whole block], non-causally inside the
+// block ("DFlash vs DFlash 2" blog, section "Conditioning on the target
+// model": K_i = [W^K H_t ; W^K H_d], V_i = [W^V H_t ; W^V H_d]; block
+// positions attend to one another non-causally; model card
+// "Beam-1.0-501B-A23B-DFlash2", section "Model": 4,096-token sliding window,
+// 40 query / 8 KV heads).
+//
+// One CTA serves one (request, KV head, key split).  The group of query heads
+// that share the KV head times the gamma block positions (5 x 8 = 40 rows at
+// the full size) is packed into 16-row MMA tiles, one consumer warp per tile,
+// so every K/V byte read from HBM is used by all query heads of its group.
+// A producer warp streams 64-key K/V tiles of the context ring into shared
+// memory with TMA (128-byte swizzle, evict-first), STAGES deep.  Scores and
+// P.V run on mma.sync bf16 with fp32 accumulation; the softmax is online
+// (running max and sum per row, reduced with warp shuffles); the window and
+// block masks are arithmetic (context slot j is visible iff j < min(L, W),
+// every block key is visible).  Splits of the key range write unnormalised
+// partials, and the last CTA of a (request, KV head) merges them in split
+// order — deterministic.
+#include <cmath>
+
+#include "attention.h"
+#include "common.cuh"
+#include "gemm.h"
+
+namespace dfl {
+namespace {
+
+constexpr int kKeys = 64;      // keys per context tile
+constexpr int kStages = 3;
+
+// Byte offset of element (row, col) in a [rows][64] bf16 tile with the
+// 128-byte swizzle (16-byte chunk index XOR row % 8).
+__device__ __forceinline__ uint32_t swz(int row, int col) {
+  return (uint32_t)(row * 128 + ((((col >> 3) ^ row) & 7) << 4) + ((col & 7) << 1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void named_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+template <int HD>
+struct WarpState {
+  static constexpr int NT = HD / 8;  // output n-tiles of 8 dims
+  float o[NT][4];
+  float m[2], l[2];
+  uint32_t qa[HD / 16][4];           // Q fragments (A operand), k-steps of 16 dims
+};
+
+// Scores, online softmax and P.V of one key tile held in shared memory as
+// HD/64 swizzled halves [NK keys][64 dims] for K and for V.
+template <int HD, int NK>
+__device__ __forceinline__ void process_tile(WarpState<HD>& st, uint32_t k_base, uint32_t v_base,
+                                             int n_valid, float scale_log2) {
+  constexpr int NT_S = NK / 8;
+  constexpr uint32_t kHalf = NK * 128;  // bytes of one 64-dim half
+  const int lane = threadIdx.x & 31;
+  float s[NT_S][4];
+#pragma unroll
+  for (int j = 0; j < NT_S; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.0f;
+
+  // S = Q K^T: pairs of 8-key n-tiles per ldmatrix.x4
+#pragma unroll
+  for (int kp = 0; kp < NT_S / 2; ++kp) {
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+      const int key = kp * 16 + (lane & 7) + ((lane >> 4) << 3);
+      const int dim = kk * 16 + (((lane >> 3) & 1) << 3);
+      const uint32_t addr = k_base + (dim >> 6) * kHalf + swz(key, dim & 63);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(addr, b0, b1, b2, b3);
+      mma_bf16(s[2 * kp], st.qa[kk][0], st.qa[kk][1], st.qa[kk][2], st.qa[kk][3], b0, b1);
+      mma_bf16(s[2 * kp + 1], st.qa[kk][0], st.qa[kk][1], st.qa[kk][2], st.qa[kk][3], b2, b3);
+    }
+  }
+  // mask and scale; rows r0 = lane/4 (regs 0,1) and r1 = lane/4 + 8 (regs 2,3)
+  float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int j = 0; j < NT_S; ++j) {
+    const int key = j * 8 + ((lane & 3) << 1);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const bool ok = (key + (e & 1)) < n_valid;
+      s[j][e] = ok ? s[j][e] * scale_log2 : -INFINITY;
+      mx[e >> 1] = fmaxf(mx[e >> 1], s[j][e]);
+    }
+  }
+  float corr[2], mnew[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+    mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+    mnew[h] = fmaxf(st.m[h], mx[h]);
+    const float base = mnew[h] == -INFINITY ? 0.0f : mnew[h];
+    corr[h] = exp2f(st.m[h] - base);
+    st.m[h] = mnew[h];
+    mnew[h] = base;
+    st.l[h] *= corr[h];
+  }
+#pragma unroll
+  for (int t = 0; t < WarpState<HD>::NT; ++t) {
+    st.o[t][0] *= corr[0];
+    st.o[t][1] *= corr[0];
+    st.o[t][2] *= corr[1];
+    st.o[t][3] *= corr[1];
+  }
+#pragma unroll
+  for (int j = 0; j < NT_S; ++j) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      s[j][e] = exp2f(s[j][e] - mnew[e >> 1]);
+      st.l[e >> 1] += s[j][e];
+    }
+  }
+  // O += P V: k-steps of 16 keys; V^T fragments through ldmatrix.trans
+#pragma unroll
+  for (int ks = 0; ks < NK / 16; ++ks) {
+    const uint32_t a0 = pack_bf16(s[2 * ks][0], s[2 * ks][1]);
+    const uint32_t a1 = pack_bf16(s[2 * ks][2], s[2 * ks][3]);
+    const uint32_t a2 = pack_bf16(s[2 * ks + 1][0], s[2 * ks + 1][1]);
+    const uint32_t a3 = pack_bf16(s[2 * ks + 1][2], s[2 * ks + 1][3]);
+#pragma unroll
+    for (int dp = 0; dp < HD / 16; ++dp) {
+      const int key = ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+      const int dim = dp * 16 + ((lane >> 4) << 3);
+      const uint32_t addr = v_base + (dim >> 6) * kHalf + swz(key, dim & 63);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(addr, b0, b1, b2, b3);
+      mma_bf16(st.o[2 * dp], a0, a1, a2, a3, b0, b1);
+      mma_bf16(st.o[2 * dp + 1], a0, a1, a2, a3, b2, b3);
+    }
+  }
+}
+
+template <int HD, int MT>
+__global__ void __launch_bounds__((MT + 1) * 32)
+    attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                const AttnArgs a) {
+  constexpr int kTileBytes = kKeys * HD * 2;     // one of K or V, all halves
+  constexpr int kStageBytes = 2 * kTileBytes;
+  constexpr int kMq = MT * 16;
+  constexpr int kBlkKeys = 16;
+  constexpr int kConsumers = MT * 32;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages];
+  __shared__ int abort_sh, last_sh;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* q_s = smem + kStages * kStageBytes;            // [kMq][HD] swizzled halves
+  uint8_t* bk_s = q_s + kMq * HD * 2;                     // block K [16][HD]
+  uint8_t* bv_s = bk_s + kBlkKeys * HD * 2;               // block V [16][HD]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int S = gridDim.x;
+  const int group = a.n_q / a.n_kv;
+  const int rows = group * a.gamma;                       // valid query rows
+  const long long L = a.ctx_len[b];
+  const int n_valid = (int)(L < (long long)a.window ? (L < 0 ? 0 : L) : a.window);
+  const int tiles = (n_valid + kKeys - 1) / kKeys;
+  const int t0 = (int)((long long)split * tiles / S), t1 = (int)((long long)(split + 1) * tiles / S);
+  const int nt = t1 - t0;
+  const bool do_block = split == S - 1;
+  int slot_b = a.req_slot ? a.req_slot[b] : b;
+  if (slot_b < 0 || slot_b >= a.ring_batch) {
+    // reads then fall outside the ring and come back as zeros (TMA bounds check)
+    if (threadIdx.x == 0 && split == 0) report_status(a.status, DFLASH_ERR_ARG);
+    slot_b = a.ring_batch;
+  }
+  const int row_base = (slot_b * a.n_kv + g) * a.window;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], MT);
+    }
+    abort_sh = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && nt > 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const uint64_t pol = policy_evict_first();
+      int issued = 0;
+      for (int i = 0; i < nt; ++i) {
+        const int s = i % kStages;
+        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+        if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1u, &abort_sh, a.status)) break;
+        uint8_t* ks = smem + s * kStageBytes;
+        uint8_t* vs = ks + kTileBytes;
+        mbar_arrive_expect_tx(&full_bar[s], kStageBytes);
+        const int row = row_base + (t0 + i) * kKeys;
+#pragma unroll
+        for (int h = 0; h < HD / 64; ++h) {
+          tma_load_2d(ks + h * (kKeys * 128), &tmK, &full_bar[s], h * 64, row, pol);
+          tma_load_2d(vs + h * (kKeys * 128), &tmV, &full_bar[s], h * 64, row, pol);
+        }
+        issued = i + 1;
+      }
+      if (abort_sh) {
+        // a wait gave up: let the copies in flight land before exiting
+        int dummy = 0;
+        for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
+          (void)mbar_wait_bounded(&full_bar[i % kStages], (uint32_t)(i / kStages) & 1u, &dummy,
+                                  nullptr, 100000000ull);
+      }
+    }
+  } else {
+    // ----------------------------------------------------------- consumers
+    const int ctid = threadIdx.x - 32;
+    // Q rows ri = hh * gamma + i  <-  qkv row b*gamma + i, column (g*group + hh) * hd
+    for (int idx = ctid; idx < kMq * (HD / 8); idx += kConsumers) {
+      const int ri = idx / (HD / 8), ch = idx % (HD / 8);
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (ri < rows) {
+        const int hh = ri / a.gamma, i = ri % a.gamma;
+        v = *reinterpret_cast<const uint4*>(a.qkv + (size_t)(b * a.gamma + i) * a.ld_qkv +
+                                            (size_t)(g * group + hh) * HD + ch * 8);
+      }
+      const int col = ch * 8;
+      *reinterpret_cast<uint4*>(q_s + (col >> 6) * (kMq * 128) + swz(ri, col & 63)) = v;
+    }
+    if (do_block) {
+      const size_t kcol = (size_t)a.n_q * HD + (size_t)g * HD;
+      const size_t vcol = (size_t)(a.n_q + a.n_kv) * HD + (size_t)g * HD;
+      for (int idx = ctid; idx < kBlkKeys * (HD / 8); idx += kConsumers) {
+        const int r = idx / (HD / 8), ch = idx % (HD / 8);
+        uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+        if (r < a.gamma) {
+          const __nv_bfloat16* row = a.qkv + (size_t)(b * a.gamma + r) * a.ld_qkv;
+          kv = *reinterpret_cast<const uint4*>(row + kcol + ch * 8);
+          vv = *reinterpret_cast<const uint4*>(row + vcol + ch * 8);
+        }
+        const int col = ch * 8;
+        const uint32_t off = (col >> 6) * (kBlkKeys * 128) + swz(r, col & 63);
+        *reinterpret_cast<uint4*>(bk_s + off) = kv;
+        *reinterpret_cast<uint4*>(bv_s + off) = vv;
+      }
+    }
+    named_sync(1, kConsumers);
+
+    WarpState<HD> st;
+    const int mt = warp - 1;
+    {
+      const uint32_t qb = smem_u32(q_s);
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const int row = mt * 16 + (lane & 15);
+        const int col = kk * 16 + ((lane >> 4) << 3);
+        ldsm_x4(qb + (col >> 6) * (kMq * 128) + swz(row, col & 63), st.qa[kk][0], st.qa[kk][1],
+                st.qa[kk][2], st.qa[kk][3]);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < WarpState<HD>::NT; ++t) st.o[t][0] = st.o[t][1] = st.o[t][2] = st.o[t][3] = 0.f;
+    st.m[0] = st.m[1] = -INFINITY;
+    st.l[0] = st.l[1] = 0.0f;
+
+    if (do_block)
+      process_tile<HD, kBlkKeys>(st, smem_u32(bk_s), smem_u32(bv_s), a.gamma, a.scale_log2);
+
+    for (int i = 0; i < nt; ++i) {
+      const int s = i % kStages;
+      const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+      if (!mbar_wait_bounded(&full_bar[s], ph, &abort_sh, a.status)) break;
+      uint8_t* ks = smem + s * kStageBytes;
+      uint8_t* vs = ks + kTileBytes;
+      const int slot0 = (t0 + i) * kKeys;
+      const int valid = n_valid - slot0 < kKeys ? n_valid - slot0 : kKeys;
+      if (valid < kKeys) {
+        // slots past the visible window may hold anything: clear their V rows
+        named_sync(2, kConsumers);
+        for (int idx = ctid; idx < (kKeys - valid) * (HD / 8); idx += kConsumers) {
+          const int r = valid + idx / (HD / 8), col = (idx % (HD / 8)) * 8;
+          *reinterpret_cast<uint4*>(vs + (col >> 6) * (kKeys * 128) + swz(r, col & 63)) =
+              make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        named_sync(2, kConsumers);
+      }
+      process_tile<HD, kKeys>(st, smem_u32(ks), smem_u32(vs), valid, a.scale_log2);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[s]);
+    }
+
+    // full row sums
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      st.l[h] += __shfl_xor_sync(0xffffffffu, st.l[h], 1);
+      st.l[h] += __shfl_xor_sync(0xffffffffu, st.l[h], 2);
+    }
+    const int r0 = mt * 16 + (lane >> 2), r1 = r0 + 8;
+    const int bg = b * a.n_kv + g;
+    if (S == 1) {
+      // final output directly
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int ri = h ? r1 : r0;
+        if (ri < rows) {
+          const float inv = 1.0f / st.l[h];
+          const int hh = ri / a.gamma, i = ri % a.gamma;
+          __nv_bfloat16* dst = a.out + (size_t)(b * a.gamma + i) * a.ld_out + (size_t)(g * group + hh) * HD;
+#pragma unroll
+          for (int t = 0; t < WarpState<HD>::NT; ++t) {
+            const int d = t * 8 + ((lane & 3) << 1);
+            *reinterpret_cast<__nv_bfloat162*>(dst + d) =
+                __floats2bfloat162_rn(st.o[t][2 * h] * inv, st.o[t][2 * h + 1] * inv);
+          }
+        }
+      }
+    } else {
+      float* part = a.part + ((size_t)bg * S + split) * kMq * HD;
+      float* ml = a.part_ml + ((size_t)bg * S + split) * kMq * 2;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int ri = h ? r1 : r0;
+#pragma unroll
+        for (int t = 0; t < WarpState<HD>::NT; ++t) {
+          const int d = t * 8 + ((lane & 3) << 1);
+          *reinterpret_cast<float2*>(part + (size_t)ri * HD + d) = make_float2(st.o[t][2 * h], st.o[t][2 * h + 1]);
+        }
+        if ((lane & 3) == 0) {
+          ml[ri * 2 + 0] = st.m[h];
+          ml[ri * 2 + 1] = st.l[h];
+        }
+      }
+    }
+  }
+  if (S == 1) return;
+
+  // ------------------------------------------------ merge the key splits
+  __threadfence();
+  __syncthreads();
+  const int bg = b * a.n_kv + g;
+  if (threadIdx.x == 0) last_sh = (atomicAdd(&a.counters[bg], 1) == S - 1);
+  __syncthreads();
+  if (!last_sh) return;
+  __threadfence();
+  const float* part = a.part + (size_t)bg * S * kMq * HD;
+  const float* ml = a.part_ml + (size_t)bg * S * kMq * 2;
+  for (int idx = threadIdx.x; idx < rows * HD; idx += blockDim.x) {
+    const int ri = idx / HD, d = idx % HD;
+    float M = -INFINITY;
+    for (int s = 0; s < S; ++s) M = fmaxf(M, __ldcg(ml + ((size_t)s * kMq + ri) * 2));
+    float num = 0.0f, den = 0.0f;
+    for (int s = 0; s < S; ++s) {
+      const float ms = __ldcg(ml + ((size_t)s * kMq + ri) * 2);
+      const float w = ms == -INFINITY ? 0.0f : exp2f(ms - M);
+      num += w * __ldcg(part + ((size_t)s * kMq + ri) * HD + d);
+      den += w * __ldcg(ml + ((size_t)s * kMq + ri) * 2 + 1);
+    }
+    const int hh = ri / a.gamma, i = ri % a.gamma;
+    a.out[(size_t)(b * a.gamma + i) * a.ld_out + (size_t)(g * group + hh) * HD + d] =
+        __float2bfloat16_rn(num / den);
+  }
+  if (threadIdx.x == 0) atomicExch(&a.counters[bg], 0);
+}
+
+template <int HD, int MT>
+int launch_t(const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a, int B, cudaStream_t s) {
+  constexpr size_t smem = 1024 + (size_t)kStages * 2 * kKeys * HD * 2 + (size_t)MT * 16 * HD * 2 +
+                          2 * 16 * HD * 2;
+  auto kern = attn_kernel<HD, MT>;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return DFLASH_ERR_LAUNCH;
+    attr = true;
+  }
+  dim3 grid(a.splits, a.n_kv, B);
+  kern<<<grid, (MT + 1) * 32, smem, s>>>(tk, tv, a);
+  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_LAUNCH;
+}
+
+}  // namespace
+
+int attn_row_tiles(int n_q, int n_kv, int gamma) { return (n_q / n_kv * gamma + 15) / 16; }
+
+int launch_attention(const void* ring_k_layer, const void* ring_v_layer, const AttnArgs& a, int B,
+                     cudaStream_t s) {
+  CUtensorMap tk, tv;
+  const uint64_t rows = (uint64_t)a.ring_batch * a.n_kv * a.window;
+  int rc = encode_bf16_2d(&tk, ring_k_layer, (uint64_t)a.hd, rows, 64, kKeys);
+  if (rc) return rc;
+  rc = encode_bf16_2d(&tv, ring_v_layer, (uint64_t)a.hd, rows, 64, kKeys);
+  if (rc) return rc;
+  const int mt = attn_row_tiles(a.n_q, a.n_kv, a.gamma);
+  if (a.hd == 128) {
+    switch (mt) {
+      case 1: return launch_t<128, 1>(tk, tv, a, B, s);
+      case 2: return launch_t<128, 2>(tk, tv, a, B, s);
+      case 3: return launch_t<128, 3>(tk, tv, a, B, s);
+      case 4: return launch_t<128, 4>(tk, tv, a, B, s);
+      case 5: return launch_t<128, 5>(tk, tv, a, B, s);
+      case 6: return launch_t<128, 6>(tk, tv, a, B, s);
+      default: return DFLASH_ERR_UNSUPPORTED;
+    }
+  }
+  switch (mt) {
+    case 1: return launch_t<64, 1>(tk, tv, a, B, s);
+    case 2: return launch_t<64, 2>(tk, tv, a, B, s);
+    case 3: return launch_t<64, 3>(tk, tv, a, B, s);
+    case 4: return launch_t<64, 4>(tk, tv, a, B, s);
+    case 5: return launch_t<64, 5>(tk, tv, a, B, s);
+    case 6: return launch_t<64, 6>(tk, tv, a, B, s);
+    default: return DFLASH_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace dfl

@@ -1,0 +1,33 @@
+// Internal interface of the block-attention kernel (attention.cu).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dfl {
+
+struct AttnArgs {
+  const __nv_bfloat16* qkv;  // [B*gamma, (Hq + 2 Hkv) hd]: rotated q, rotated k, v
+  long long ld_qkv;
+  __nv_bfloat16* out;        // [B*gamma, Hq hd]
+  long long ld_out;
+  const int64_t* ctx_len;    // [B] context lengths L
+  const int32_t* req_slot;   // [B] ring rows or nullptr
+  int gamma, n_q, n_kv, hd, window, ring_batch;
+  int splits;                // key-range splits per (request, KV head)
+  float scale_log2;          // log2(e) / sqrt(hd)
+  float* part;               // [B*Hkv][splits][16*row_tiles][hd]
+  float* part_ml;            // [B*Hkv][splits][16*row_tiles][2]
+  int* counters;             // [B*Hkv], zero between launches
+  int* status;
+};
+
+// 16-row MMA tiles needed for the (query group x gamma) rows.
+int attn_row_tiles(int n_q, int n_kv, int gamma);
+
+// ring_*_layer: the layer's slice of the ring, bf16 [ring_batch, Hkv, W, hd].
+int launch_attention(const void* ring_k_layer, const void* ring_v_layer, const AttnArgs& a, int B,
+                     cudaStream_t s);
+
+}  // namespace dfl

@@ -1,0 +1,457 @@
+// Dense contractions of the drafter on the 5th-generation tensor cores.
+//
+// Every linear layer of the pass (QKV, O, gate/up, down, LM head, W_c and the
+// per-layer context K/V projections) is Y[tokens, rows] = X[tokens, K] W[rows,
+// K]^T with few tokens (8 at batch 1) and many weight rows.  The kernel is
+// therefore "swap-AB": the weight tile is the 128-row A operand of
+// tcgen05.mma, the tokens are the N side (16..128 columns), and the fp32
+// accumulator lives in tensor memory as 128 lanes (weight rows) x BN columns
+// (tokens).
+//
+// Pipeline (one CTA = 4 warps):
+//   warp 0 lane 0   TMA producer: 128x64 weight box + BNx64 token box per
+//                   stage, 128-byte swizzle, weights marked evict-first;
+//   warp 1          allocates TMEM; lane 0 issues 4 MMAs (K = 16 each) per
+//                   stage and commits the stage back to the producer;
+//   all 4 warps     epilogue: tcgen05.ld of their 32-lane quarter, then the
+//                   fused epilogue of the layer (RoPE, residual add, SwiGLU,
+//                   fp32 logits, or scatter into the context ring).
+// Split-K: the grid's z dimension partitions K; each split stores its fp32
+// partial tile, and the last split to arrive (atomic ticket after a fence)
+// sums the partials in split order — deterministic — and runs the epilogue.
+// All waits are bounded (see mbar_wait_bounded).
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+#include "gemm.h"
+
+namespace dfl {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kBK = 64;                   // K elements per stage (128 bytes of bf16)
+constexpr int kABytes = 128 * kBK * 2;    // weight box per stage
+
+__device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
+
+// Rotation angle pos * inv_freq reduced to [-pi, pi] with float-float
+// arithmetic: inv_freq = hi + lo (from a double), the product error is
+// recovered with an FMA, and 2*pi is split into two floats (Cody-Waite).
+__device__ __forceinline__ void rope_sincos(float pos, float inv_hi, float inv_lo, float* s,
+                                            float* c) {
+  const float a = pos * inv_hi;
+  const float e = fmaf(pos, inv_hi, -a) + pos * inv_lo;
+  const float k = rintf(a * 0.159154943091895336f);
+  float r = fmaf(-k, 6.28318548202514648f, a);
+  r = fmaf(-k, -1.74845560007448828e-7f, r);
+  r += e;
+  sincosf(r, s, c);
+}
+
+struct RopeRow {
+  float inv_hi, inv_lo;
+  bool first_half;
+};
+__device__ __forceinline__ RopeRow rope_row(int d, int hd, float theta) {
+  const int half = hd >> 1;
+  const int j = d % half;
+  const double inv = pow((double)theta, -2.0 * (double)j / (double)hd);
+  RopeRow rr;
+  rr.inv_hi = (float)inv;
+  rr.inv_lo = (float)(inv - (double)rr.inv_hi);
+  rr.first_half = d < half;
+  return rr;
+}
+
+__device__ __forceinline__ float rope_apply(float x, float partner, const RopeRow& rr, float pos) {
+  float s, c;
+  rope_sincos(pos, rr.inv_hi, rr.inv_lo, &s, &c);
+  return rr.first_half ? fmaf(x, c, -partner * s) : fmaf(x, c, partner * s);
+}
+
+// Epilogue of 16 consecutive tokens of this thread's row.  `xchg` holds the
+// chunk as [16][128] floats so that partner rows can be read.  Every thread
+// of the CTA calls it (it synchronises).
+__device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const float (&v)[16],
+                               int tok_base, int tile_n, int r, float* xchg) {
+  const int kind = e.kind;
+  const bool needs_xchg = (kind == EPI_QKV || kind == EPI_SWIGLU || kind == EPI_KV_RING);
+  if (needs_xchg) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) xchg[j * 128 + r] = v[j];
+    __syncthreads();
+  }
+  if (kind == EPI_F32 || kind == EPI_BF16 || kind == EPI_RESID) {
+    const int n = tile_n * 128 + r;
+    if (n < e.N) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int tok = tok_base + j;
+        if (tok < e.M) {
+          const size_t o = (size_t)tok * e.ld + n;
+          if (kind == EPI_F32)
+            static_cast<float*>(e.out)[o] = v[j];
+          else if (kind == EPI_BF16)
+            static_cast<__nv_bfloat16*>(e.out)[o] = __float2bfloat16_rn(v[j]);
+          else
+            static_cast<float*>(e.out)[o] += v[j];
+        }
+      }
+    }
+  } else if (kind == EPI_QKV) {
+    const int n = tile_n * 128 + r;
+    if (n < e.N) {
+      const bool rot = n < e.rope_rows;
+      const int d = n % e.hd;
+      const RopeRow rr = rope_row(d, e.hd, e.rope_theta);
+      const int pr = r ^ (e.hd >> 1);
+#pragma unroll 4
+      for (int j = 0; j < 16; ++j) {
+        const int tok = tok_base + j;
+        if (tok < e.M) {
+          float y = v[j];
+          if (rot) {
+            const float pos = (float)(e.ctx_len[tok / e.gamma] + tok % e.gamma);
+            y = rope_apply(v[j], xchg[j * 128 + pr], rr, pos);
+          }
+          static_cast<__nv_bfloat16*>(e.out)[(size_t)tok * e.ld + n] = __float2bfloat16_rn(y);
+        }
+      }
+    }
+  } else if (kind == EPI_SWIGLU) {
+    const int f = tile_n * 64 + r;
+    if (r < 64 && f < e.N) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int tok = tok_base + j;
+        if (tok < e.M) {
+          const float g = v[j], u = xchg[j * 128 + r + 64];
+          static_cast<__nv_bfloat16*>(e.out)[(size_t)tok * e.ld + f] =
+              __float2bfloat16_rn(silu(g) * u);
+        }
+      }
+    }
+  } else if (kind == EPI_KV_RING) {
+    const int local = (tile_n % ao.tiles_per_map) * 128 + r;
+    const int layer = e.layer0 + tile_n / ao.tiles_per_map;
+    const int kv = local / e.kv_dim;            // 0 = K, 1 = V
+    const int g = (local % e.kv_dim) / e.hd;
+    const int d = local % e.hd;
+    const RopeRow rr = rope_row(d, e.hd, e.rope_theta);
+    const int pr = r ^ (e.hd >> 1);
+    __nv_bfloat16* ring = static_cast<__nv_bfloat16*>(kv ? e.ring_v : e.ring_k);
+#pragma unroll 4
+    for (int j = 0; j < 16; ++j) {
+      const int tok = tok_base + j;
+      if (tok < e.M) {
+        const int b = tok / e.n_max, jr = tok % e.n_max;
+        if (jr < e.n_new[b]) {
+          const long long pos = e.ctx_len[b] + jr;
+          const int slot_b = e.req_slot ? e.req_slot[b] : b;
+          if (pos < 0 || slot_b < 0 || slot_b >= e.ring_batch) {
+            report_status(e.status, DFLASH_ERR_ARG);
+            continue;
+          }
+          float y = v[j];
+          if (kv == 0) y = rope_apply(v[j], xchg[j * 128 + pr], rr, (float)pos);
+          const size_t o =
+              ((((size_t)layer * e.ring_batch + slot_b) * e.n_kv + g) * e.window + (size_t)(pos % e.window)) *
+                  e.hd + d;
+          ring[o] = __float2bfloat16_rn(y);
+        }
+      }
+    }
+  }
+  if (needs_xchg) __syncthreads();
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_bf16_tc_kernel(const __grid_constant__ GemmAMaps A, const __grid_constant__ CUtensorMap tmB,
+                        const GemmAOpts ao, const GemmArgs args, const GemmEpi epi) {
+  constexpr int kBBytes = BN * kBK * 2;
+  constexpr int kStage = kABytes + kBBytes;
+  constexpr uint32_t kTmemCols = BN < 32 ? 32 : BN;
+  static_assert(kStage % 1024 == 0, "stage buffers must keep 1024-byte alignment");
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t acc_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  __shared__ int last_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile_n = blockIdx.x, tile_m = blockIdx.y, split = blockIdx.z;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int kb_total = (args.K + kBK - 1) / kBK;
+  const int kb0 = (int)((long long)split * kb_total / args.splits);
+  const int kb1 = (int)((long long)(split + 1) * kb_total / args.splits);
+  const int nkb = kb1 - kb0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(&acc_bar, 1);
+    abort_sh = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < ao.n_maps; ++i) tma_prefetch_desc(&A.map[i]);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  int issued = 0;
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------- producer
+    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_x = policy_evict_last();
+    int map_i = 0, row0;
+    if (ao.dual) {
+      row0 = ao.row_offset + tile_n * 64;
+    } else {
+      map_i = tile_n / ao.tiles_per_map;
+      row0 = ao.row_offset + (tile_n % ao.tiles_per_map) * 128;
+    }
+    const int tok0 = tile_m * BN;
+    // weights do not depend on the previous kernel: start streaming them
+    // before waiting for it (programmatic dependent launch)
+    const int pre = nkb < STAGES ? nkb : STAGES;
+    for (int i = 0; i < pre; ++i) {
+      uint8_t* sa = smem + i * kStage;
+      mbar_arrive_expect_tx(&full_bar[i], kStage);
+      const int kc = (kb0 + i) * kBK;
+      if (ao.dual) {
+        tma_load_2d(sa, &A.map[0], &full_bar[i], kc, row0, pol_w);
+        tma_load_2d(sa + 64 * 128, &A.map[1], &full_bar[i], kc, row0, pol_w);
+      } else {
+        tma_load_2d(sa, &A.map[map_i], &full_bar[i], kc, row0, pol_w);
+      }
+    }
+    grid_dependency_wait();
+    for (int i = 0; i < pre; ++i)
+      tma_load_2d(smem + i * kStage + kABytes, &tmB, &full_bar[i], (kb0 + i) * kBK, tok0, pol_x);
+    issued = pre;
+    for (int i = pre; i < nkb; ++i) {
+      const int s = i % STAGES;
+      const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
+      if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1u, &abort_sh, args.status)) break;
+      uint8_t* sa = smem + s * kStage;
+      mbar_arrive_expect_tx(&full_bar[s], kStage);
+      const int kc = (kb0 + i) * kBK;
+      if (ao.dual) {
+        tma_load_2d(sa, &A.map[0], &full_bar[s], kc, row0, pol_w);
+        tma_load_2d(sa + 64 * 128, &A.map[1], &full_bar[s], kc, row0, pol_w);
+      } else {
+        tma_load_2d(sa, &A.map[map_i], &full_bar[s], kc, row0, pol_w);
+      }
+      tma_load_2d(sa + kABytes, &tmB, &full_bar[s], kc, tok0, pol_x);
+      issued = i + 1;
+    }
+  } else if (warp == 1 && lane == 0) {
+    // --------------------------------------------------------- MMA issuer
+    constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % STAGES;
+      const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
+      if (!mbar_wait_bounded(&full_bar[s], ph, &abort_sh, args.status)) break;
+      tc_fence_after();
+      const uint32_t a_addr = smem_u32(smem + s * kStage);
+      const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+      for (int k = 0; k < kBK / 16; ++k)
+        tc_mma_bf16(tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), idesc,
+                    (i | k) ? 1u : 0u);
+      tc_commit(&empty_bar[s]);
+    }
+    tc_commit(&acc_bar);
+  }
+  __syncwarp();
+
+  // ----------------------------------------------------------- epilogue
+  const bool acc_ok = mbar_wait_bounded(&acc_bar, 0, &abort_sh, args.status);
+  tc_fence_after();
+  if (warp == 0 && lane == 0 && abort_sh) {
+    // a wait gave up: let this CTA's copies in flight land before exiting
+    int dummy = 0;
+    for (int i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
+      (void)mbar_wait_bounded(&full_bar[i % STAGES], (uint32_t)(i / STAGES) & 1u, &dummy, nullptr,
+                              100000000ull);
+  }
+  __syncthreads();
+  const int r = warp * 32 + lane;
+  const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
+  float* xchg = reinterpret_cast<float*>(smem);
+  const bool aborted = abort_sh != 0 || !acc_ok;
+
+  if (!aborted) {
+    if (args.splits == 1) {
+      for (int c = 0; c < BN / 16; ++c) {
+        uint32_t raw[16];
+        tmem_ld_x16(t_row + c * 16, raw);
+        tc_wait_ld();
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]);
+        epilogue_chunk(epi, ao, v, tile_m * BN + c * 16, tile_n, r, xchg);
+      }
+    } else {
+      const int tile_lin = tile_m * gridDim.x + tile_n;
+      float* part = args.partial + (size_t)tile_lin * args.splits * (BN * 128);
+      float* mine = part + (size_t)split * (BN * 128);
+      for (int c = 0; c < BN / 16; ++c) {
+        uint32_t raw[16];
+        tmem_ld_x16(t_row + c * 16, raw);
+        tc_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) mine[(c * 16 + j) * 128 + r] = __uint_as_float(raw[j]);
+      }
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) last_sh = (atomicAdd(&args.counters[tile_lin], 1) == args.splits - 1);
+      __syncthreads();
+      if (last_sh) {
+        __threadfence();
+        for (int c = 0; c < BN / 16; ++c) {
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+          for (int s = 0; s < args.splits; ++s) {
+            const float* ps = part + (size_t)s * (BN * 128);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] += __ldcg(ps + (c * 16 + j) * 128 + r);
+          }
+          epilogue_chunk(epi, ao, v, tile_m * BN + c * 16, tile_n, r, xchg);
+        }
+        if (threadIdx.x == 0) atomicExch(&args.counters[tile_lin], 0);
+      }
+    }
+  }
+  grid_dependents_launch();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------ host
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+template <int BN, int STAGES>
+constexpr size_t smem_bytes() {
+  return (size_t)STAGES * (kABytes + BN * kBK * 2) + 1024;
+}
+
+template <int BN, int STAGES>
+int launch_one(const GemmAMaps& A, const CUtensorMap& tmB, const GemmAOpts& ao, const GemmArgs& args,
+               const GemmEpi& epi, dim3 grid, cudaStream_t s, bool pdl) {
+  auto kern = gemm_bf16_tc_kernel<BN, STAGES>;
+  constexpr size_t smem = smem_bytes<BN, STAGES>();
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return DFLASH_ERR_LAUNCH;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, kern, A, tmB, ao, args, epi) != cudaSuccess) return DFLASH_ERR_LAUNCH;
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+int encode_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
+                   uint32_t box_inner, uint32_t box_outer) {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return DFLASH_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) || (inner * 2) % 16) return DFLASH_ERR_ALIGN;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_ERR_CUDA;
+}
+
+int gemm_token_tile(int M) {
+  if (M <= 16) return 16;
+  if (M <= 64) return 64;
+  return 128;
+}
+
+int gemm_plan_splits(int tiles, int K, int target_ctas) {
+  const int kb = (K + kBK - 1) / kBK;
+  int s = (target_ctas + tiles - 1) / tiles;
+  const int max_s = kb / 4 > 0 ? kb / 4 : 1;  // at least 4 k-blocks per split
+  if (s > max_s) s = max_s;
+  if (s < 1) s = 1;
+  return s;
+}
+
+int launch_gemm(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void* x, int M, int K,
+                const GemmEpi& epi, const GemmScratch& scratch, int splits, cudaStream_t s,
+                bool pdl) {
+  const int BN = gemm_token_tile(M);
+  CUtensorMap tmB;
+  int rc = encode_bf16_2d(&tmB, x, (uint64_t)K, (uint64_t)M, kBK, (uint32_t)BN);
+  if (rc) return rc;
+  const int m_tiles = (M + BN - 1) / BN;
+  const int kb = (K + kBK - 1) / kBK;
+  if (splits < 1) splits = 1;
+  if (splits > kb) splits = kb;
+  const size_t tiles = (size_t)n_tiles * m_tiles;
+  if (splits > 1) {
+    if (tiles > (size_t)scratch.counters_cap) splits = 1;
+    while (splits > 1 && tiles * splits * BN * 128 > scratch.partial_cap_floats) --splits;
+  }
+  GemmArgs args;
+  args.K = K;
+  args.splits = splits;
+  args.partial = scratch.partial;
+  args.counters = scratch.counters;
+  args.status = scratch.status;
+  dim3 grid(n_tiles, m_tiles, splits);
+  switch (BN) {
+    case 16: return launch_one<16, 6>(A, tmB, ao, args, epi, grid, s, pdl);
+    case 64: return launch_one<64, 4>(A, tmB, ao, args, epi, grid, s, pdl);
+    default: return launch_one<128, 6>(A, tmB, ao, args, epi, grid, s, pdl);
+  }
+}
+
+}  // namespace dfl

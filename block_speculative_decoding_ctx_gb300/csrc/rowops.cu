@@ -1,0 +1,255 @@
+// Row-wise support kernels of the draft pass: block embedding + RMSNorm,
+// RMSNorm (optionally gathering the MASK rows of each block), per-position
+// top-k with log-sum-exp over the LM-head logits, and the context-length
+// update of ctx_append.
+//
+// Sources: "DFlash vs DFlash 2" blog, section "DFlash: generate the block all
+// at once" (draft input [anchor, MASK, MASK, ...]; shared embedding and LM
+// head) and section "The candidate selector" (top-k candidates kept per
+// position); product doc "Speculative decoding", section "How it works".
+#include "common.cuh"
+#include "rowops.h"
+
+namespace dfl {
+namespace {
+
+constexpr int kNormThreads = 256;
+
+// One CTA per block row m = b * gamma + i: x[m] = embed[id] (fp32 residual
+// stream), h[m] = bf16(RMSNorm(x[m]) * g), id = anchor[b] for i = 0, MASK after.
+__global__ void __launch_bounds__(kNormThreads)
+    embed_norm_kernel(const __nv_bfloat16* __restrict__ embed, const int32_t* __restrict__ anchor,
+                      int gamma, int mask_id, int vocab, int d, const float* __restrict__ g, float eps,
+                      float* __restrict__ x, __nv_bfloat16* __restrict__ h, int* status) {
+  __shared__ float red[33];
+  const int m = blockIdx.x;
+  const int b = m / gamma, i = m % gamma;
+  int id = i == 0 ? anchor[b] : mask_id;
+  if (id < 0 || id >= vocab) {
+    if (threadIdx.x == 0) report_status(status, DFLASH_ERR_ARG);
+    id = 0;
+  }
+  const __nv_bfloat16* e = embed + (size_t)id * d;
+  float ss = 0.0f;
+  for (int c = threadIdx.x; c < d; c += kNormThreads) {
+    const float v = __bfloat162float(e[c]);
+    x[(size_t)m * d + c] = v;
+    ss += v * v;
+  }
+  ss = block_sum(ss, red);
+  const float rs = rsqrtf(ss / (float)d + eps);
+  for (int c = threadIdx.x; c < d; c += kNormThreads)
+    h[(size_t)m * d + c] = __float2bfloat16_rn(__bfloat162float(e[c]) * rs * g[c]);
+}
+
+// out row r = bf16(RMSNorm(x[src(r)]) * g).  gather_gamma = 0: src(r) = r;
+// otherwise the MASK rows: src(r) = (r / (G - 1)) * G + r % (G - 1) + 1.
+__global__ void __launch_bounds__(kNormThreads)
+    rmsnorm_kernel(const float* __restrict__ x, int d, const float* __restrict__ g, float eps,
+                   int gather_gamma, __nv_bfloat16* __restrict__ out) {
+  __shared__ float red[33];
+  const int r = blockIdx.x;
+  int src = r;
+  if (gather_gamma > 0) src = (r / (gather_gamma - 1)) * gather_gamma + r % (gather_gamma - 1) + 1;
+  const float* xr = x + (size_t)src * d;
+  float ss = 0.0f;
+  for (int c = threadIdx.x; c < d; c += kNormThreads) {
+    const float v = xr[c];
+    ss += v * v;
+  }
+  ss = block_sum(ss, red);
+  const float rs = rsqrtf(ss / (float)d + eps);
+  for (int c = threadIdx.x; c < d; c += kNormThreads)
+    out[(size_t)r * d + c] = __float2bfloat16_rn(xr[c] * rs * g[c]);
+}
+
+// ------------------------------------------------------ top-k and LSE
+
+constexpr int kTopkThreads = 256;
+
+// (value, id) packed so that a larger key is a larger value, ties to the lower id.
+__device__ __forceinline__ unsigned long long vkey(float v, int id) {
+  return ((unsigned long long)ordered_key(v) << 32) | (uint32_t)(~(uint32_t)id);
+}
+
+template <int KT>
+__device__ __forceinline__ void insert_key(unsigned long long (&top)[KT], unsigned long long k) {
+  if (k <= top[KT - 1]) return;
+  top[KT - 1] = k;
+#pragma unroll
+  for (int j = KT - 1; j > 0; --j) {
+    if (top[j] > top[j - 1]) {
+      const unsigned long long t = top[j];
+      top[j] = top[j - 1];
+      top[j - 1] = t;
+    }
+  }
+}
+
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) {
+    m = m2;
+    s = s2;
+    return;
+  }
+  if (m2 > m) {
+    s = s * expf(m - m2) + s2;
+    m = m2;
+  } else {
+    s += s2 * expf(m2 - m);
+  }
+}
+
+// Select the k largest of n keys in `cand` (shared memory), in order, by
+// repeated warp-wide maxima; taken entries are zeroed.  Warp 0 only.
+__device__ void select_topk(unsigned long long* cand, int n, int k, unsigned long long* out) {
+  const int lane = threadIdx.x & 31;
+  for (int j = 0; j < k; ++j) {
+    unsigned long long best = 0;
+    int where = -1;
+    for (int i = lane; i < n; i += 32) {
+      if (cand[i] > best) {
+        best = cand[i];
+        where = i;
+      }
+    }
+    const unsigned long long wbest = warp_max_u64(best);
+    const unsigned ball = __ballot_sync(0xffffffffu, best == wbest && where >= 0);
+    if (lane == __ffs(ball) - 1 && ball) cand[where] = 0;
+    if (lane == 0) out[j] = wbest;
+    __syncwarp();
+  }
+}
+
+template <int KT>
+__global__ void __launch_bounds__(kTopkThreads)
+    topk_lse_kernel(const float* __restrict__ logits, int V, int k, int chunks,
+                    unsigned long long* __restrict__ part_keys, float* __restrict__ part_ml,
+                    int* counters, int32_t* __restrict__ ids, float* __restrict__ vals,
+                    float* __restrict__ lse, int32_t* __restrict__ draft) {
+  __shared__ unsigned long long cand[kTopkThreads * KT];
+  __shared__ unsigned long long sel[KT];
+  __shared__ float redm[32], reds[32];
+  __shared__ int s_last;
+  const int c = blockIdx.x, r = blockIdx.y;
+  const float* row = logits + (size_t)r * V;
+  const int v0 = c * kRowChunk, v1 = min(V, v0 + kRowChunk);
+
+  unsigned long long top[KT];
+#pragma unroll
+  for (int j = 0; j < KT; ++j) top[j] = 0;
+  float m = -INFINITY, s = 0.0f;
+  for (int v = v0 + threadIdx.x; v < v1; v += kTopkThreads) {
+    const float x = __ldg(row + v);
+    insert_key<KT>(top, vkey(x, v));
+    if (x > m) {
+      s = (m == -INFINITY ? 0.0f : s * expf(m - x)) + 1.0f;
+      m = x;
+    } else {
+      s += expf(x - m);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < KT; ++j) cand[threadIdx.x * KT + j] = top[j];
+  // (m, s) across the block
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    lse_merge(m, s, m2, s2);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    redm[threadIdx.x >> 5] = m;
+    reds[threadIdx.x >> 5] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float mm = threadIdx.x < kTopkThreads / 32 ? redm[threadIdx.x] : -INFINITY;
+    float ssum = threadIdx.x < kTopkThreads / 32 ? reds[threadIdx.x] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, mm, o), s2 = __shfl_xor_sync(0xffffffffu, ssum, o);
+      lse_merge(mm, ssum, m2, s2);
+    }
+    select_topk(cand, kTopkThreads * KT, k, sel);
+    if (threadIdx.x == 0) {
+      unsigned long long* pk = part_keys + ((size_t)r * chunks + c) * KT;
+      for (int j = 0; j < k; ++j) pk[j] = sel[j];
+      part_ml[((size_t)r * chunks + c) * 2 + 0] = mm;
+      part_ml[((size_t)r * chunks + c) * 2 + 1] = ssum;
+      __threadfence();
+      s_last = (atomicAdd(&counters[r], 1) == chunks - 1);
+    }
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // merge the chunks of row r
+  const int n = chunks * k;
+  for (int i = threadIdx.x; i < n; i += kTopkThreads)
+    cand[i] = __ldcg(part_keys + ((size_t)r * chunks + i / k) * KT + i % k);
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    select_topk(cand, n, k, sel);
+    if (threadIdx.x == 0) {
+      float M = -INFINITY, S = 0.0f;
+      for (int cc = 0; cc < chunks; ++cc)
+        lse_merge(M, S, __ldcg(part_ml + ((size_t)r * chunks + cc) * 2),
+                  __ldcg(part_ml + ((size_t)r * chunks + cc) * 2 + 1));
+      if (lse) lse[r] = M + logf(S);
+      for (int j = 0; j < k; ++j) {
+        const unsigned long long key = sel[j];
+        if (ids) ids[(size_t)r * k + j] = (int32_t)(~(uint32_t)(key & 0xFFFFFFFFull));
+        if (vals) vals[(size_t)r * k + j] = key_to_float((uint32_t)(key >> 32));
+      }
+      if (draft) draft[r] = (int32_t)(~(uint32_t)(sel[0] & 0xFFFFFFFFull));
+      atomicExch(&counters[r], 0);
+    }
+  }
+}
+
+__global__ void add_lengths_kernel(int B, const int32_t* __restrict__ n_new, int64_t* ctx_len) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B) ctx_len[b] += n_new[b];
+}
+
+}  // namespace
+
+int launch_embed_norm(const void* embed, const int32_t* anchor, int B, int gamma, int mask_id,
+                      int vocab, int d, const float* g, float eps, float* x, void* h, int* status,
+                      cudaStream_t s) {
+  embed_norm_kernel<<<B * gamma, kNormThreads, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(embed), anchor, gamma, mask_id, vocab, d, g, eps, x,
+      static_cast<__nv_bfloat16*>(h), status);
+  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_LAUNCH;
+}
+
+int launch_rmsnorm(const float* x, int rows, int d, const float* g, float eps, int gather_gamma,
+                   void* out, cudaStream_t s) {
+  rmsnorm_kernel<<<rows, kNormThreads, 0, s>>>(x, d, g, eps, gather_gamma,
+                                               static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_LAUNCH;
+}
+
+int topk_slots(int k) { return k <= 4 ? 4 : 16; }
+
+int launch_topk_lse(const float* logits, int rows, int V, int k, unsigned long long* part_keys,
+                    float* part_ml, int* counters, int32_t* ids, float* vals, float* lse,
+                    int32_t* draft, cudaStream_t s) {
+  const int chunks = row_chunks(V);
+  dim3 grid(chunks, rows);
+  if (k <= 4)
+    topk_lse_kernel<4><<<grid, kTopkThreads, 0, s>>>(logits, V, k, chunks, part_keys, part_ml,
+                                                     counters, ids, vals, lse, draft);
+  else
+    topk_lse_kernel<16><<<grid, kTopkThreads, 0, s>>>(logits, V, k, chunks, part_keys, part_ml,
+                                                      counters, ids, vals, lse, draft);
+  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_LAUNCH;
+}
+
+int launch_add_lengths(int B, const int32_t* n_new, int64_t* ctx_len, cudaStream_t s) {
+  add_lengths_kernel<<<(B + 127) / 128, 128, 0, s>>>(B, n_new, ctx_len);
+  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_LAUNCH;
+}
+
+}  // namespace dfl

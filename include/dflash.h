@@ -208,6 +208,17 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
 int dflash_probs(int rows, int vocab, const float* logits, float temperature, float top_p,
                  float* probs, void* workspace, size_t ws_bytes, dflash_stream_t stream);
 
+/* The drafter's proposal y ~ q ("The problem: one expensive token at a time":
+ * the drafter proposes y from its distribution q): for request b and
+ * position i < G, y[b, i] is the fixed-point inverse-CDF draw from q[b, i]
+ * with Philox (seeds[b], step, position i, purpose 0).  draft_block makes the
+ * same draw when given sampling parameters.
+ *   q  float32 [B, G, V], rows normalised;  y  int32 [B, G] out */
+int dflash_sample_draft(int B, int G, int vocab, const float* q, const uint64_t* seeds,
+                        uint64_t step, int32_t* y, void* workspace, size_t ws_bytes,
+                        dflash_stream_t stream);
+size_t dflash_sample_workspace_bytes(int rows, int vocab);
+
 /* Verification ("The problem: one expensive token at a time").
  *   mode GREEDY:  target = target logits float32 [B, gamma, V]; q, seeds unused.
  *                 n = longest prefix with draft[b, i] == argmax target[b, i]
