@@ -91,8 +91,8 @@ def lib():
                                     ctypes.POINTER(dflash_sampling),
                                     ctypes.POINTER(dflash_draft_out), _P, _SZ, _P]),
         "dflash_probs": (_I, [_I, _I, _P, ctypes.c_float, ctypes.c_float, _P, _P, _SZ, _P]),
-        "dflash_verify": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, ctypes.c_uint64, _P, _P, _P, _SZ,
-                               _P]),
+        "dflash_verify": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, ctypes.c_uint64, _P, _P, _P, _P, _P,
+                               _SZ, _P]),
         "dflash_read_status": (_I, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
         "dflash_strerror": (ctypes.c_char_p, [_I]),
         "dflash_selftest_timeout": (_I, [_P, ctypes.c_longlong, _P]),
@@ -235,13 +235,13 @@ def dflash_probs(logits, temperature, top_p, probs, ws, stream=None):
 
 
 def dflash_verify(mode, target, draft, accept_len, tokens, ws, q=None, seeds=None, step=0,
-                  stream=None):
+                  next_anchor=None, n_append=None, stream=None):
     """target: greedy target logits or sampled p, float32 [B, gamma, V]."""
     B, gamma, V = target.shape
     _check(lib().dflash_verify(int(mode), B, gamma, V, _ptr(target), _ptr(q), _ptr(draft),
                                _ptr(seeds), ctypes.c_uint64(int(step) & (2 ** 64 - 1)),
-                               _ptr(accept_len), _ptr(tokens), _ptr(ws), ws.numel(),
-                               _stream(stream)), "dflash_verify")
+                               _ptr(accept_len), _ptr(tokens), _ptr(next_anchor), _ptr(n_append),
+                               _ptr(ws), ws.numel(), _stream(stream)), "dflash_verify")
 
 
 def dflash_read_status(ws, stream=None):

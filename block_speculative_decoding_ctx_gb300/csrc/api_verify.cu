@@ -49,25 +49,26 @@ size_t dflash_probs_workspace_bytes(int rows, int vocab) {
 
 int dflash_verify(int mode, int B, int gamma, int vocab, const float* target, const float* q,
                   const int32_t* draft, const uint64_t* seeds, uint64_t step,
-                  int32_t* accept_len, int32_t* tokens, void* workspace, size_t ws_bytes,
-                  dflash_stream_t stream) {
+                  int32_t* accept_len, int32_t* tokens, int32_t* next_anchor, int32_t* n_append,
+                  void* workspace, size_t ws_bytes, dflash_stream_t stream) {
   if (mode != DFLASH_VERIFY_GREEDY && mode != DFLASH_VERIFY_SAMPLED) return DFLASH_ERR_ARG;
   if (B < 1 || B > 65535 || gamma < 2 || gamma > 64 || vocab < 1 || vocab > kMaxVocab)
     return DFLASH_ERR_SHAPE;
   if (!target || !draft || !accept_len || !tokens) return DFLASH_ERR_ARG;
   if (mode == DFLASH_VERIFY_SAMPLED && (!q || !seeds)) return DFLASH_ERR_ARG;
   if (!aligned(target, 4) || !aligned(draft, 4) || !aligned(accept_len, 4) ||
-      !aligned(tokens, 4) || (q && !aligned(q, 4)) || (seeds && !aligned(seeds, 8)))
+      !aligned(tokens, 4) || (q && !aligned(q, 4)) || (seeds && !aligned(seeds, 8)) ||
+      (next_anchor && !aligned(next_anchor, 4)) || (n_append && !aligned(n_append, 4)))
     return DFLASH_ERR_ALIGN;
   if (!workspace || !aligned(workspace, 256)) return DFLASH_ERR_WORKSPACE;
   VerifyLayout L = verify_layout(workspace, B, gamma, vocab);
   if (ws_bytes < L.bytes) return DFLASH_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (mode == DFLASH_VERIFY_GREEDY)
-    return launch_verify_greedy(B, gamma, vocab, target, draft, accept_len, tokens, L.counters,
-                                L.keys, L.status, s);
+    return launch_verify_greedy(B, gamma, vocab, target, draft, accept_len, tokens, next_anchor,
+                                n_append, L.counters, L.keys, L.status, s);
   return launch_verify_sampled(B, gamma, vocab, target, q, draft, seeds, step, accept_len, tokens,
-                               L.counters, L.zsum, L.status, s);
+                               next_anchor, n_append, L.counters, L.zsum, L.status, s);
 }
 
 int dflash_probs(int rows, int vocab, const float* logits, float temperature, float top_p,

@@ -20,15 +20,17 @@ inline int row_chunks(int V) { return (V + kRowChunk - 1) / kRowChunk; }
 // Greedy verification.  counters [B] and keys [B * gamma] must be zero on
 // entry and are zero again on exit.
 int launch_verify_greedy(int B, int gamma, int V, const float* target, const int32_t* draft,
-                         int32_t* accept_len, int32_t* tokens, int* counters,
-                         unsigned long long* keys, int* status, cudaStream_t s);
+                         int32_t* accept_len, int32_t* tokens, int32_t* next_anchor,
+                         int32_t* n_append, int* counters, unsigned long long* keys, int* status,
+                         cudaStream_t s);
 
 // Sampled verification.  counters [B] zero on entry and exit;
 // zsum [B * row_chunks(V) * 2] scratch.
 int launch_verify_sampled(int B, int gamma, int V, const float* p, const float* q,
                           const int32_t* draft, const uint64_t* seeds, uint64_t step,
-                          int32_t* accept_len, int32_t* tokens, int* counters,
-                          unsigned long long* zsum, int* status, cudaStream_t s);
+                          int32_t* accept_len, int32_t* tokens, int32_t* next_anchor,
+                          int32_t* n_append, int* counters, unsigned long long* zsum, int* status,
+                          cudaStream_t s);
 
 // out[r] ~ w[r, :] for rows r = b * rows_per_req + i with Philox
 // (seeds[b], step, position = i, purpose).  counters [rows] zero on entry and

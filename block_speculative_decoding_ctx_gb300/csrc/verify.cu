@@ -77,7 +77,8 @@ __device__ int find_in_chunk(const WFn& wfn, int v0, int v1, unsigned long long 
 __global__ void __launch_bounds__(kThreads)
     verify_greedy_kernel(const float* __restrict__ target, const int32_t* __restrict__ draft,
                          int gamma, int V, int chunks, int32_t* __restrict__ accept_len,
-                         int32_t* __restrict__ tokens, int* counters, unsigned long long* keys) {
+                         int32_t* __restrict__ tokens, int32_t* __restrict__ next_anchor,
+                         int32_t* __restrict__ n_append, int* counters, unsigned long long* keys) {
   __shared__ unsigned long long red[33];
   __shared__ int s_last;
   const int c = blockIdx.x;
@@ -116,20 +117,25 @@ __global__ void __launch_bounds__(kThreads)
     const int G = gamma - 1;
     int n = 0;
     bool match = true;
+    int32_t last = -1;
     for (int i = 0; i < gamma; ++i) {
       const unsigned long long k = atomicExch(&keys[b * gamma + i], 0ull);
       const int a = (int)(~(uint32_t)(k & 0xFFFFFFFFull));
       int32_t t = -1;
       if (match) {
         t = a;
-        if (i < G && draft[b * G + i] == a)
+        if (i < G && draft[b * G + i] == a) {
           n = i + 1;
-        else
+        } else {
           match = false;
+          last = a;
+        }
       }
       tokens[b * gamma + i] = t;
     }
     accept_len[b] = n;
+    if (next_anchor) next_anchor[b] = last;
+    if (n_append) n_append[b] = n + 1;
     atomicExch(&counters[b], 0);
   }
 }
@@ -153,6 +159,7 @@ __global__ void __launch_bounds__(kThreads)
                           const int32_t* __restrict__ draft, const uint64_t* __restrict__ seeds,
                           uint64_t step, int gamma, int V, int chunks,
                           int32_t* __restrict__ accept_len, int32_t* __restrict__ tokens,
+                          int32_t* __restrict__ next_anchor, int32_t* __restrict__ n_append,
                           int* counters, unsigned long long* zsum, int* status) {
   __shared__ unsigned long long red[33];
   __shared__ int s_n, s_last, s_chunk, s_use_resid, s_found;
@@ -243,6 +250,8 @@ __global__ void __launch_bounds__(kThreads)
       tokens[b * gamma + i] = t;
     }
     accept_len[b] = n;
+    if (next_anchor) next_anchor[b] = tok;
+    if (n_append) n_append[b] = n + 1;
     atomicExch(&counters[b], 0);
   }
 }
@@ -455,23 +464,26 @@ __global__ void __launch_bounds__(kProbThreads)
 }  // namespace
 
 int launch_verify_greedy(int B, int gamma, int V, const float* target, const int32_t* draft,
-                         int32_t* accept_len, int32_t* tokens, int* counters,
-                         unsigned long long* keys, int* /*status*/, cudaStream_t s) {
+                         int32_t* accept_len, int32_t* tokens, int32_t* next_anchor,
+                         int32_t* n_append, int* counters, unsigned long long* keys,
+                         int* /*status*/, cudaStream_t s) {
   const int chunks = row_chunks(V);
   dim3 grid(chunks, B * gamma);
   verify_greedy_kernel<<<grid, kThreads, 0, s>>>(target, draft, gamma, V, chunks, accept_len,
-                                                 tokens, counters, keys);
+                                                 tokens, next_anchor, n_append, counters, keys);
   return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_LAUNCH;
 }
 
 int launch_verify_sampled(int B, int gamma, int V, const float* p, const float* q,
                           const int32_t* draft, const uint64_t* seeds, uint64_t step,
-                          int32_t* accept_len, int32_t* tokens, int* counters,
-                          unsigned long long* zsum, int* status, cudaStream_t s) {
+                          int32_t* accept_len, int32_t* tokens, int32_t* next_anchor,
+                          int32_t* n_append, int* counters, unsigned long long* zsum, int* status,
+                          cudaStream_t s) {
   const int chunks = row_chunks(V);
   dim3 grid(chunks, B);
   verify_sampled_kernel<<<grid, kThreads, 0, s>>>(p, q, draft, seeds, step, gamma, V, chunks,
-                                                  accept_len, tokens, counters, zsum, status);
+                                                  accept_len, tokens, next_anchor, n_append,
+                                                  counters, zsum, status);
   return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_LAUNCH;
 }
 

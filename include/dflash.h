@@ -233,10 +233,17 @@ size_t dflash_sample_workspace_bytes(int rows, int vocab);
  *   draft      int32 [B, gamma-1]
  *   accept_len int32 [B] out: n in [0, gamma-1]; tau = n + 1
  *   tokens     int32 [B, gamma] out: drafts 0..n-1, the correction or bonus
- *              at n, -1 after. */
+ *              at n, -1 after.
+ *   next_anchor, n_append  int32 [B] out, each may be NULL: the commit step
+ *              of the cycle ("Speculative decoding" product doc, section "How
+ *              it works": accepted tokens are emitted, then the next block) —
+ *              next_anchor = tokens[b, n] (the anchor of the next block) and
+ *              n_append = n + 1 (the positions the target has now scored: the
+ *              anchor and the n accepted drafts, whose features ctx_append
+ *              takes next). */
 int dflash_verify(int mode, int B, int gamma, int vocab, const float* target, const float* q,
                   const int32_t* draft, const uint64_t* seeds, uint64_t step,
-                  int32_t* accept_len, int32_t* tokens,
+                  int32_t* accept_len, int32_t* tokens, int32_t* next_anchor, int32_t* n_append,
                   void* workspace, size_t ws_bytes, dflash_stream_t stream);
 
 /* Copy the workspace status word to the host (synchronises the stream). */

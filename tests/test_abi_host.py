@@ -33,19 +33,19 @@ def test_verify_rejects_bad_arguments_on_the_host(L):
     P = ctypes.c_void_p
     fake = P(4096)  # never dereferenced: validation fails first
     # bad mode
-    assert L.dflash_verify(7, 1, 8, 100, fake, fake, fake, fake, 0, fake, fake, fake, 1 << 20, None) == -1
+    assert L.dflash_verify(7, 1, 8, 100, fake, fake, fake, fake, 0, fake, fake, None, None, fake, 1 << 20, None) == -1
     # gamma < 2, vocab too large
-    assert L.dflash_verify(0, 1, 1, 100, fake, None, fake, None, 0, fake, fake, fake, 1 << 20, None) == -2
-    assert L.dflash_verify(0, 1, 8, 1 << 19, fake, None, fake, None, 0, fake, fake, fake, 1 << 20, None) == -2
+    assert L.dflash_verify(0, 1, 1, 100, fake, None, fake, None, 0, fake, fake, None, None, fake, 1 << 20, None) == -2
+    assert L.dflash_verify(0, 1, 8, 1 << 19, fake, None, fake, None, 0, fake, fake, None, None, fake, 1 << 20, None) == -2
     # null target / sampled without q
-    assert L.dflash_verify(0, 1, 8, 100, None, None, fake, None, 0, fake, fake, fake, 1 << 20, None) == -1
-    assert L.dflash_verify(1, 1, 8, 100, fake, None, fake, fake, 0, fake, fake, fake, 1 << 20, None) == -1
+    assert L.dflash_verify(0, 1, 8, 100, None, None, fake, None, 0, fake, fake, None, None, fake, 1 << 20, None) == -1
+    assert L.dflash_verify(1, 1, 8, 100, fake, None, fake, fake, 0, fake, fake, None, None, fake, 1 << 20, None) == -1
     # misaligned pointer
-    assert L.dflash_verify(0, 1, 8, 100, P(4098), None, fake, None, 0, fake, fake, fake, 1 << 20, None) == -3
+    assert L.dflash_verify(0, 1, 8, 100, P(4098), None, fake, None, 0, fake, fake, None, None, fake, 1 << 20, None) == -3
     # workspace too small
     need = dfl.dflash_verify_workspace_bytes(4, 8, 151936)
     assert need > 256
-    assert L.dflash_verify(0, 4, 8, 151936, fake, None, fake, None, 0, fake, fake, fake, need - 1, None) == -7
+    assert L.dflash_verify(0, 4, 8, 151936, fake, None, fake, None, 0, fake, fake, None, None, fake, need - 1, None) == -7
 
 
 def test_probs_rejects_bad_arguments_on_the_host(L):
