@@ -1,0 +1,534 @@
+#!/usr/bin/env python3
+"""Benchmark of one speculative cycle: context injection, the single-pass
+block draft and verification, on the full drafter dimensions.
+
+A step is one cycle for every request of the batch:
+  dflash_ctx_append  (features of the tau positions the target scored last cycle)
+  dflash_draft_block (anchor + 7 MASK, 5 layers, LM head, top-4)
+  dflash_verify      (greedy; writes the next anchor and append count on device)
+The target model is not part of this path: its logits are stood in for by the
+draft logits plus N(0, sigma) noise, formed by two torch ops whose time is
+measured separately and excluded (latency per token L = (T_draft + T_verify)
+/ tau, blog "DFlash vs DFlash 2", section "The problem: one expensive token at
+a time").  The whole step is captured once in a CUDA graph and replayed.
+
+Prints one JSON line (rank 0).  --impl reference times the float64 CPU
+oracle on the host cores instead (bounded sample per step, scaled).
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "draft blocks/s and verified tokens/s (γ=8) at batch 1/16/32; % HBM/TC roofline"
+DIMS_FULL = dict(d=5120, n_q=40, n_kv=8, hd=128, ffn=17408, vocab=151936, n_layers=5,
+                 n_feat=5, feat_dim=5120, window=4096)
+WORKLOAD = ("full drafter dims (5 layers, hidden 5120, 40q/8kv x 128, SwiGLU 17408, vocab 151936), "
+            "batch {B}, gamma {G}, context {L} filling the 4096 window, top-4, greedy verify")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--gamma", type=int, default=8)
+    ap.add_argument("--context", type=int, default=4096)
+    ap.add_argument("--sigma", type=float, default=0.05,
+                    help="std of the noise that turns draft logits into stand-in target logits")
+    ap.add_argument("--no-extras", action="store_true", help="skip the batch 16/32 lines")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- helpers
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, ws
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during a timed region."""
+
+    def __init__(self):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        dev = os.environ.get("LOCAL_RANK", "0")
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", dev, f"--query-gpu={q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        self.p.wait()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[3:7]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p.get("hbm_gbs", 6800.0), p.get("bf16_tflops", 1900.0), \
+            p.get("bf16_tflops_sustained", 1700.0), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def gpu_weights(dims, seed, dev):
+    """Random-init weights of the drafter architecture, N(0, 0.02) bf16, made on the GPU."""
+    g = torch.Generator(device=dev).manual_seed(seed)
+    d, hd = dims["d"], dims["hd"]
+
+    def mat(r, c):
+        return (torch.randn((r, c), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+
+    ones = torch.ones(d, device=dev)
+    W = {"embed": mat(dims["vocab"], d), "lm_head": mat(dims["vocab"], d),
+         "w_c": mat(d, dims["n_feat"] * dims["feat_dim"]), "g_c": ones, "g_final": ones,
+         "layers": []}
+    for _ in range(dims["n_layers"]):
+        W["layers"].append({"g_attn": ones, "w_qkv": mat((dims["n_q"] + 2 * dims["n_kv"]) * hd, d),
+                            "w_o": mat(d, dims["n_q"] * hd), "g_mlp": ones,
+                            "w_gate": mat(dims["ffn"], d), "w_up": mat(dims["ffn"], d),
+                            "w_down": mat(d, dims["ffn"])})
+    return W
+
+
+def lib_cfg(dims, B, gamma, append_max):
+    return dict(hidden=dims["d"], n_q_heads=dims["n_q"], n_kv_heads=dims["n_kv"],
+                head_dim=dims["hd"], ffn=dims["ffn"], vocab=dims["vocab"],
+                n_layers=dims["n_layers"], n_feat=dims["n_feat"], feat_dim=dims["feat_dim"],
+                window=dims["window"], gamma_max=max(gamma, 8), topk_max=4, batch_max=B,
+                append_max=append_max, rope_theta=1.0e6, eps=1.0e-6, mask_id=-1)
+
+
+def time_graph(g, steps, stream):
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def capture(fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()                    # eager warm-up outside the capture
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+# ------------------------------------------------------------- GPU cycle
+
+class Cycle:
+    """State and launch sequence of one speculative cycle at (B, gamma)."""
+
+    def __init__(self, dfl, h, dims, B, gamma, context, sigma, dev, seed):
+        self.dfl, self.h, self.dims, self.B, self.gamma = dfl, h, dims, B, gamma
+        V, Wn = dims["vocab"], dims["window"]
+        gen = torch.Generator(device=dev).manual_seed(seed)
+        shape = (dims["n_layers"], B, dims["n_kv"], Wn, dims["hd"])
+        self.rk = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+        self.rv = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+        self.ws_a = dfl.workspace(dfl.dflash_append_workspace_bytes(h), dev)
+        self.ws_d = dfl.workspace(dfl.dflash_draft_workspace_bytes(h), dev)
+        self.ws_v = dfl.workspace(dfl.dflash_verify_workspace_bytes(B, gamma, V), dev)
+        # prefill: the last min(L, W) positions of a context of length L
+        n0 = min(context, Wn)
+        self.ctx = torch.full((B,), context - n0, dtype=torch.int64, device=dev)
+        feats0 = torch.randn((B, n0, dims["n_feat"], dims["feat_dim"]), generator=gen,
+                             device=dev).to(torch.bfloat16)
+        dfl.dflash_ctx_append(h, feats0, torch.full((B,), n0, dtype=torch.int32, device=dev),
+                              self.ctx, self.rk, self.rv, self.ws_a)
+        del feats0
+        self.feats = torch.randn((B, gamma, dims["n_feat"], dims["feat_dim"]), generator=gen,
+                                 device=dev).to(torch.bfloat16)
+        self.anchor = torch.randint(0, V - 1, (B,), generator=gen, device=dev, dtype=torch.int32)
+        self.n_app = torch.ones(B, dtype=torch.int32, device=dev)
+        self.noise = torch.randn((B, gamma, V), generator=gen, device=dev) * sigma
+        self.logits = torch.empty((B, gamma - 1, V), device=dev)
+        self.ids = torch.empty((B, gamma - 1, 4), dtype=torch.int32, device=dev)
+        self.vals = torch.empty((B, gamma - 1, 4), device=dev)
+        self.lse = torch.empty((B, gamma - 1), device=dev)
+        self.draft = torch.empty((B, gamma - 1), dtype=torch.int32, device=dev)
+        self.target = torch.empty((B, gamma, V), device=dev)
+        self.acc = torch.empty(B, dtype=torch.int32, device=dev)
+        self.tok = torch.empty((B, gamma), dtype=torch.int32, device=dev)
+        self.tau_sum = torch.zeros(B, dtype=torch.int64, device=dev)
+        self.out = dict(topk_ids=self.ids, topk_vals=self.vals, lse=self.lse, logits=self.logits,
+                        draft=self.draft)
+
+    def append(self):
+        self.dfl.dflash_ctx_append(self.h, self.feats, self.n_app, self.ctx, self.rk, self.rv, self.ws_a)
+
+    def draft_pass(self):
+        self.dfl.dflash_draft_block(self.h, self.anchor, self.ctx, self.rk, self.rv, self.gamma,
+                                    self.ws_d, topk=4, out=self.out)
+
+    def stand_in(self):
+        G = self.gamma - 1
+        torch.add(self.logits, self.noise[:, :G], out=self.target[:, :G])
+        torch.add(self.logits[:, G - 1], self.noise[:, G], out=self.target[:, G])
+
+    def verify(self):
+        self.dfl.dflash_verify(self.dfl.DFLASH_VERIFY_GREEDY, self.target, self.draft, self.acc,
+                               self.tok, self.ws_v, next_anchor=self.anchor, n_append=self.n_app)
+        self.tau_sum.add_(self.n_app)
+
+    def step(self):
+        self.append()
+        self.draft_pass()
+        self.stand_in()
+        self.verify()
+
+
+def gpu_launches_per_step(dims, with_append=True):
+    per_layer = 7       # QKV, attention, O, RMSNorm, gate|up, down, RMSNorm
+    n = 1 + per_layer * dims["n_layers"] + 2          # embed+norm, layers, LM head, top-k
+    n += 1                                            # verify
+    if with_append:
+        n += 4                                        # W_c GEMM, RMSNorm, K/V GEMM, lengths
+    return n
+
+
+def run_ours(args, rank, ws):
+    import block_speculative_decoding_ctx_gb300 as dfl
+    dfl.lib()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    dims = dict(DIMS_FULL)
+    B, G = args.batch, args.gamma
+    W = gpu_weights(dims, 1234, dev)
+    h = dfl.dflash_create(lib_cfg(dims, max(B, 1), G, dims["window"]), W)
+    cyc = Cycle(dfl, h, dims, B, G, args.context, args.sigma, dev, 99 + rank)
+    stream = torch.cuda.Stream(device=dev)
+
+    g_step = capture(cyc.step, stream)
+    g_stand = capture(cyc.stand_in, stream)
+    g_draft = capture(cyc.draft_pass, stream)
+    g_app = capture(cyc.append, stream)
+    g_ver = capture(cyc.verify, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            g_step.replay()
+    torch.cuda.synchronize()
+    cyc.tau_sum.zero_()
+
+    # ------------------------------------------------------ timed region
+    barrier(ws)
+    torch.cuda.synchronize()
+    clocks = ClockSampler()
+    t_step = time_graph(g_step, args.steps, stream)
+    tau_mean = cyc.tau_sum.sum().item() / (args.steps * B)
+    clk = clocks.stop()
+    barrier(ws)
+    t_stand = time_graph(g_stand, args.steps, stream)
+    t_draft = time_graph(g_draft, args.steps, stream)
+    t_app = time_graph(g_app, args.steps, stream)
+    t_ver = time_graph(g_ver, args.steps, stream)
+    t_path = max(t_step - t_stand, 1e-6)
+    t_path_max = max_over_ranks(t_path, ws)
+
+    # ------------------------------------ dominant kernel (GEMMs of the pass)
+    dfl.dflash_profile_enable(h, 64)
+    rows = []
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            cyc.draft_pass()
+            rows.append(dfl.dflash_profile_read(h))
+    dfl.dflash_profile_enable(h, 0)
+    ms = sum(r[0] for rr in rows for r in rr) / len(rows)
+    by = sum(r[1] for r in rows[0])
+    lm = [rr[-1] for rr in rows]
+    hbm, tf, tf_sus, src = measured_peaks()
+    achieved = by / (ms * 1e-3) / 1e9
+    roof = {"kernel": "gemm_bf16_tc_kernel (all 21 GEMM launches of the draft pass)",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved / hbm, 4), "peak_source": src, "traffic": None,
+            "gemm_ms_per_pass": round(ms, 4), "gemm_bytes_per_pass": by,
+            "lm_head_GBps": round(lm[0][1] / (statistics.median(r[0] for r in lm) * 1e-3) / 1e9, 1)}
+
+    # ------------------------------------------------- end to end (host buffers)
+    e2e = run_e2e(args, dfl, cyc, stream)
+
+    extras = {}
+    if not args.no_extras and ws == 1:
+        del cyc, g_step, g_stand, g_draft, g_app, g_ver
+        torch.cuda.empty_cache()
+        extras = run_extras(args, dfl, dims, W, dev, stream)
+
+    value = B * ws * 1000.0 / t_path_max
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "draft blocks/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": round(t_path_max, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init weights N(0,0.02), "
+        "features N(0,1), target logits = draft logits + N(0,sigma))",
+        "config": {"workload": WORKLOAD.format(B=B, G=G, L=args.context), "batch": B, "gamma": G,
+                   "context": args.context, "sigma": args.sigma,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": "inputs larger than L2: 4.9 GB of weights streamed per step"},
+        "verified_tokens_per_s": round(tau_mean * B * ws * 1000.0 / t_path_max, 2),
+        "tau_mean": round(tau_mean, 3),
+        "stage_ms": {"ctx_append": round(t_app, 4), "draft_block": round(t_draft, 4),
+                     "verify": round(t_ver, 4), "target_stand_in_excluded": round(t_stand, 4)},
+        "clocks": clk, "e2e": e2e,
+        "gpu_launches": gpu_launches_per_step(dims) * args.steps,
+        "roofline": roof,
+    }
+    if extras:
+        res["batches"] = extras
+    return res
+
+
+def run_e2e(args, dfl, cyc, stream):
+    """The same cycle through the public API with pinned host inputs and
+    outputs: features and stand-in target noise copied in, accept length and
+    tokens copied out, every step."""
+    B, G, V = cyc.B, cyc.gamma, cyc.dims["vocab"]
+    feats_h = cyc.feats.cpu().pin_memory()
+    noise_h = cyc.noise.cpu().pin_memory()
+    acc_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    tok_h = torch.empty((B, G), dtype=torch.int32).pin_memory()
+    steps = max(5, args.steps // 2)
+
+    def one():
+        cyc.feats.copy_(feats_h, non_blocking=True)
+        cyc.noise.copy_(noise_h, non_blocking=True)
+        cyc.step()
+        acc_h.copy_(cyc.acc, non_blocking=True)
+        tok_h.copy_(cyc.tok, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            one()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            one()
+            stream.synchronize()          # the caller reads the result every step
+        t = (time.perf_counter() - t0) / steps
+    h2d = feats_h.numel() * feats_h.element_size() + noise_h.numel() * noise_h.element_size()
+    d2h = acc_h.numel() * 4 + tok_h.numel() * 4
+    return {"value": round(B / t, 2), "unit": "draft blocks/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(t * 1e3, 4),
+            "note": "eager launches through the ctypes API; includes the target stand-in"}
+
+
+def run_extras(args, dfl, dims, W, dev, stream):
+    """Draft-pass throughput at batch 16 and 32 (gamma 8) and batch 32 gamma 16
+    over a random full ring (context 8192 -> window 4096)."""
+    out = {}
+    hbm, tf, tf_sus, src = measured_peaks()
+    for B, G in ((16, 8), (32, 8), (32, 16)):
+        h = dfl.dflash_create(lib_cfg(dims, B, G, 8), W)
+        shape = (dims["n_layers"], B, dims["n_kv"], dims["window"], dims["hd"])
+        gen = torch.Generator(device=dev).manual_seed(7 + B + G)
+        rk = torch.randn(shape, generator=gen, device=dev).to(torch.bfloat16)
+        rv = torch.randn(shape, generator=gen, device=dev).to(torch.bfloat16)
+        ctx = torch.full((B,), 8192, dtype=torch.int64, device=dev)
+        anchor = torch.randint(0, dims["vocab"] - 1, (B,), generator=gen, device=dev, dtype=torch.int32)
+        ws = dfl.workspace(dfl.dflash_draft_workspace_bytes(h), dev)
+        o = dict(topk_ids=torch.empty((B, G - 1, 4), dtype=torch.int32, device=dev),
+                 topk_vals=torch.empty((B, G - 1, 4), device=dev),
+                 lse=torch.empty((B, G - 1), device=dev),
+                 draft=torch.empty((B, G - 1), dtype=torch.int32, device=dev))
+
+        def fn():
+            dfl.dflash_draft_block(h, anchor, ctx, rk, rv, G, ws, topk=4, out=o)
+
+        g = capture(fn, stream)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+        t = time_graph(g, max(5, args.steps // 2), stream)
+        dfl.dflash_profile_enable(h, 64)
+        with torch.cuda.stream(stream):
+            fn()
+            prof = dfl.dflash_profile_read(h)
+        dfl.dflash_profile_enable(h, 0)
+        gemm_ms = sum(p[0] for p in prof)
+        M = B * G
+        flops = 0.0
+        d, F, V = dims["d"], dims["ffn"], dims["vocab"]
+        qkv = (dims["n_q"] + 2 * dims["n_kv"]) * dims["hd"]
+        flops += dims["n_layers"] * 2.0 * M * d * (qkv + dims["n_q"] * dims["hd"] + 3 * F)
+        flops += 2.0 * B * (G - 1) * d * V
+        gemm_tflops = flops / (gemm_ms * 1e-3) / 1e12
+        key = f"batch{B}_gamma{G}"
+        out[key] = {"draft_blocks_per_s": round(B * 1000.0 / t, 2), "ms_per_pass": round(t, 4),
+                    "gemm_ms": round(gemm_ms, 4), "gemm_tflops": round(gemm_tflops, 1),
+                    "gemm_frac_of_bf16_peak": round(gemm_tflops / tf_sus, 4),
+                    "peak_tflops_sustained": tf_sus, "peak_source": src}
+        del h, rk, rv, ws, g
+        torch.cuda.empty_cache()
+    return out
+
+
+# --------------------------------------------------------------- CPU oracle
+
+def oracle_cycle_sample(dims, frac_layers=1.0, vocab_frac=1.0, seed=5):
+    """Time the float64 oracle on one cycle's work for one request, with one
+    full-size layer (the cost of the 5 layers is 5x it), the LM head over a
+    fraction of the vocabulary and ctx_append of tau = 5 positions; returns
+    (seconds for a whole cycle, description)."""
+    import numpy as np
+
+    from block_speculative_decoding_ctx_gb300 import synth
+    from oracle import model as om
+    from oracle import verify as over
+
+    d = dims["d"]
+    cfg1 = om.Config(**dict(dims, n_layers=1))
+    g = synth.gen(seed)
+
+    def mat(r, c):
+        return (torch.randn((r, c), generator=g) * 0.02).to(torch.bfloat16)
+
+    Vs = max(1024, int(dims["vocab"] * vocab_frac))
+    head = mat(Vs, d)
+    layer = {"g_attn": torch.ones(d), "w_qkv": mat((dims["n_q"] + 2 * dims["n_kv"]) * dims["hd"], d),
+             "w_o": mat(d, dims["n_q"] * dims["hd"]), "g_mlp": torch.ones(d),
+             "w_gate": mat(dims["ffn"], d), "w_up": mat(dims["ffn"], d), "w_down": mat(d, dims["ffn"])}
+    Wd = {"embed": head, "lm_head": head, "g_final": torch.ones(d), "g_c": torch.ones(d),
+          "w_c": mat(d, dims["n_feat"] * dims["feat_dim"]), "layers": [layer]}
+    rk = torch.randn((1, 1, dims["n_kv"], dims["window"], dims["hd"]), generator=g).to(torch.bfloat16)
+    rv = torch.randn((1, 1, dims["n_kv"], dims["window"], dims["hd"]), generator=g).to(torch.bfloat16)
+    feats = torch.randn((5, dims["n_feat"], dims["feat_dim"]), generator=g).to(torch.bfloat16)
+    t0 = time.perf_counter()
+    om.draft_pass(cfg1, Wd, rk, rv, np.array([8192]),
+                  np.array([3]), 8)
+    t_layer_head = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    om.linear(np.zeros((7, d)), head)
+    t_head = time.perf_counter() - t0
+    t_layer = max(t_layer_head - t_head, 0.0)
+    t0 = time.perf_counter()
+    H = om.fuse_features(cfg1, Wd, feats)
+    om.context_kv(cfg1, Wd, H, np.arange(5))
+    t_append_1 = time.perf_counter() - t0
+    tgt = np.random.default_rng(0).normal(size=(1, 8, dims["vocab"])).astype(np.float32)
+    t0 = time.perf_counter()
+    over.greedy(tgt, tgt[:, :7].argmax(-1))
+    t_ver = time.perf_counter() - t0
+    # W_c is shared; the K/V projection of 5 layers costs ~5x the 1-layer one
+    t_cycle = (t_append_1 + 5 * t_layer + t_head / (Vs / dims["vocab"]) + t_ver)
+    desc = (f"one request: 1 full layer timed (x5), LM head over {Vs} of {dims['vocab']} rows "
+            f"(scaled), ctx_append of 5 positions, greedy verify; float64 numpy oracle")
+    return t_cycle, desc, t_layer_head + t_append_1 + t_ver
+
+
+def run_reference(args, rank, ws):
+    if rank != 0:
+        return None
+    dims = dict(DIMS_FULL)
+    steps, warm = args.steps, max(args.warmup, 3)
+    # each step: a fifth of a cycle (1 of 5 layers + 1/5 of the LM head rows), scaled x5
+    times = []
+    desc = None
+    for i in range(warm + steps):
+        t_cycle, desc, _ = oracle_cycle_sample(dims, vocab_frac=0.2, seed=11 + i % 2)
+        if i >= warm:
+            times.append(t_cycle)
+    t = statistics.mean(times)
+    cores = os.cpu_count()
+    value = 1.0 / t
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "draft blocks/s",
+            "n_gpus": ws, "steps": steps, "warmup": warm, "ms_per_step": round(t * 1e3, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD.format(B=1, G=8, L=4096) +
+                                            " (CPU oracle)", "batch": 1, "gamma": 8},
+            "cpu_baseline": {"value": round(value, 5), "unit": "draft blocks/s", "cores": cores,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(value, 5), "unit": "draft blocks/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, ws = dist_setup()
+    if args.impl == "reference":
+        res = run_reference(args, rank, ws)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    res = run_ours(args, rank, ws)
+    if rank == 0:
+        if not args.no_cpu and ws == 1:
+            t_cycle, desc, wall = oracle_cycle_sample(dict(DIMS_FULL))
+            res["cpu_baseline"] = {"value": round(1.0 / t_cycle, 5), "unit": "draft blocks/s",
+                                   "cores": os.cpu_count(), "kind": "oracle",
+                                   "sample": desc + f" ({wall:.1f} s of CPU work)"}
+        print(json.dumps(res), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -98,6 +98,9 @@ def lib():
         "dflash_selftest_timeout": (_I, [_P, ctypes.c_longlong, _P]),
         "dflash_sample_draft": (_I, [_I, _I, _I, _P, _P, ctypes.c_uint64, _P, _P, _SZ, _P]),
         "dflash_sample_workspace_bytes": (_SZ, [_I, _I]),
+        "dflash_profile_enable": (_I, [_P, _I]),
+        "dflash_profile_read": (_I, [_P, ctypes.POINTER(ctypes.c_float),
+                                     ctypes.POINTER(ctypes.c_double), _I, ctypes.POINTER(_I)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -266,3 +269,16 @@ def dflash_sample_draft(q, seeds, step, y, ws, stream=None):
     _check(lib().dflash_sample_draft(B, G, V, _ptr(q), _ptr(seeds), ctypes.c_uint64(int(step) & (2 ** 64 - 1)),
                                      _ptr(y), _ptr(ws), ws.numel(), _stream(stream)),
            "dflash_sample_draft")
+
+
+def dflash_profile_enable(handle, n_pairs):
+    _check(lib().dflash_profile_enable(handle.ptr, int(n_pairs)), "dflash_profile_enable")
+
+
+def dflash_profile_read(handle, cap=64):
+    """Per-GEMM (ms, algorithmic bytes) of the last draft_block call."""
+    ms = (ctypes.c_float * cap)()
+    by = (ctypes.c_double * cap)()
+    n = ctypes.c_int(0)
+    _check(lib().dflash_profile_read(handle.ptr, ms, by, cap, ctypes.byref(n)), "dflash_profile_read")
+    return [(ms[i], by[i]) for i in range(n.value)]

@@ -38,6 +38,10 @@ struct dflash_handle {
   CUtensorMap lm_head, w_c;
   int num_sms;
   int mask_id;
+  // benchmark hook: event pairs around the GEMM launches of draft_block
+  std::vector<cudaEvent_t> prof_events;
+  std::vector<double> prof_bytes;
+  int prof_used = 0;
 };
 
 namespace {
@@ -186,9 +190,54 @@ int splits_for(const dflash_handle* h, int n_tiles, int M, int K) {
   return gemm_plan_splits(n_tiles * m_tiles, K, h->num_sms * per_sm);
 }
 
+// Launch one draft GEMM, bracketed by the handle's profiling events when
+// enabled.  bytes = algorithmic bytes of the launch.
+int draft_gemm(dflash_handle* h, const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void* x,
+               int M, int K, const GemmEpi& e, const GemmScratch& sc, cudaStream_t s, double bytes) {
+  const int i = h->prof_used;
+  const bool prof = 2 * (i + 1) <= (int)h->prof_events.size();
+  if (prof && cudaEventRecord(h->prof_events[2 * i], s) != cudaSuccess) return DFLASH_ERR_CUDA;
+  const int rc = launch_gemm(A, ao, n_tiles, x, M, K, e, sc, splits_for(h, n_tiles, M, K), s, true);
+  if (rc) return rc;
+  if (prof) {
+    if (cudaEventRecord(h->prof_events[2 * i + 1], s) != cudaSuccess) return DFLASH_ERR_CUDA;
+    h->prof_bytes[i] = bytes;
+    h->prof_used = i + 1;
+  }
+  return DFLASH_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+int dflash_profile_enable(dflash_handle* h, int n_pairs) {
+  if (!h || n_pairs < 0 || n_pairs > 4096) return DFLASH_ERR_ARG;
+  for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
+  h->prof_events.clear();
+  h->prof_bytes.assign(n_pairs, 0.0);
+  h->prof_used = 0;
+  for (int i = 0; i < 2 * n_pairs; ++i) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return DFLASH_ERR_CUDA;
+    h->prof_events.push_back(e);
+  }
+  return DFLASH_OK;
+}
+
+int dflash_profile_read(dflash_handle* h, float* ms, double* bytes, int cap, int* count) {
+  if (!h || !count || cap < 0 || (cap > 0 && (!ms || !bytes))) return DFLASH_ERR_ARG;
+  const int n = h->prof_used < cap ? h->prof_used : cap;
+  if (n > 0 && cudaEventSynchronize(h->prof_events[2 * h->prof_used - 1]) != cudaSuccess)
+    return DFLASH_ERR_CUDA;
+  for (int i = 0; i < n; ++i) {
+    if (cudaEventElapsedTime(&ms[i], h->prof_events[2 * i], h->prof_events[2 * i + 1]) != cudaSuccess)
+      return DFLASH_ERR_CUDA;
+    bytes[i] = h->prof_bytes[i];
+  }
+  *count = n;
+  return DFLASH_OK;
+}
 
 int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_handle** out) {
   if (!out) return DFLASH_ERR_ARG;
@@ -242,6 +291,8 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
 }
 
 int dflash_destroy(dflash_handle* h) {
+  if (h)
+    for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
   delete h;
   return DFLASH_OK;
 }
@@ -352,6 +403,7 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   GemmScratch scratch{ws.gemm_partial, kGemmPartialFloats, ws.gemm_counters, kGemmCounters, ws.status};
+  h->prof_used = 0;
   const int M = B * gamma;
   const int R = B * (gamma - 1);
   const int d = c.hidden, hd = c.head_dim;
@@ -397,7 +449,8 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
       e.rope_rows = (c.n_q_heads + c.n_kv_heads) * hd;
       e.hd = hd;
       const int nt = (qkv_dim + 127) / 128;
-      rc = launch_gemm(A, single_map(), nt, ws.h, M, d, e, scratch, splits_for(h, nt, M, d), s, true);
+      rc = draft_gemm(h, A, single_map(), nt, ws.h, M, d, e, scratch, s,
+                      2.0 * qkv_dim * d + 2.0 * M * d + 2.0 * M * qkv_dim);
       if (rc) return rc;
     }
     rc = launch_attention(static_cast<const char*>(ring_k) + l * ring_layer * 2,
@@ -408,7 +461,8 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
       A.map[0] = lm.o;
       GemmEpi e = epi_base(EPI_RESID, M, d, ws.x, d);
       const int nt = (d + 127) / 128;
-      rc = launch_gemm(A, single_map(), nt, ws.attn, M, qd, e, scratch, splits_for(h, nt, M, qd), s, true);
+      rc = draft_gemm(h, A, single_map(), nt, ws.attn, M, qd, e, scratch, s,
+                      2.0 * d * qd + 2.0 * M * qd + 8.0 * M * d);
       if (rc) return rc;
     }
     rc = launch_rmsnorm(ws.x, M, d, static_cast<const float*>(L.g_mlp), c.eps, 0, ws.h, s);
@@ -422,7 +476,8 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
       ao.dual = 1;
       GemmEpi e = epi_base(EPI_SWIGLU, M, c.ffn, ws.mlp, c.ffn);
       const int nt = c.ffn / 64;
-      rc = launch_gemm(A, ao, nt, ws.h, M, d, e, scratch, splits_for(h, nt, M, d), s, true);
+      rc = draft_gemm(h, A, ao, nt, ws.h, M, d, e, scratch, s,
+                      4.0 * c.ffn * d + 2.0 * M * d + 2.0 * M * c.ffn);
       if (rc) return rc;
     }
     {  // down + residual
@@ -430,8 +485,8 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
       A.map[0] = lm.down;
       GemmEpi e = epi_base(EPI_RESID, M, d, ws.x, d);
       const int nt = (d + 127) / 128;
-      rc = launch_gemm(A, single_map(), nt, ws.mlp, M, c.ffn, e, scratch,
-                       splits_for(h, nt, M, c.ffn), s, true);
+      rc = draft_gemm(h, A, single_map(), nt, ws.mlp, M, c.ffn, e, scratch, s,
+                      2.0 * d * c.ffn + 2.0 * M * c.ffn + 8.0 * M * d);
       if (rc) return rc;
     }
     if (l + 1 < c.n_layers)
@@ -447,7 +502,8 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
     A.map[0] = h->lm_head;
     GemmEpi e = epi_base(EPI_F32, R, c.vocab, logits, c.vocab);
     const int nt = (c.vocab + 127) / 128;
-    rc = launch_gemm(A, single_map(), nt, ws.hf, R, d, e, scratch, splits_for(h, nt, R, d), s, true);
+    rc = draft_gemm(h, A, single_map(), nt, ws.hf, R, d, e, scratch, s,
+                    2.0 * c.vocab * d + 2.0 * R * d + 4.0 * R * c.vocab);
     if (rc) return rc;
   }
   const int k_eff = topk > 0 ? topk : 1;
