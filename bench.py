@@ -51,6 +51,9 @@ def parse():
                     help="std of the noise that turns draft logits into stand-in target logits")
     ap.add_argument("--no-extras", action="store_true", help="skip the batch 16/32 lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--profile-cycles", type=int, default=0,
+                    help="profiling case: run this many eager cycles and exit (for ncu)")
+    ap.add_argument("--layers", type=int, default=5, help="drafter layers (profiling cases only)")
     return ap.parse_args()
 
 
@@ -261,12 +264,19 @@ def run_ours(args, rank, ws):
     dfl.lib()
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
-    dims = dict(DIMS_FULL)
+    dims = dict(DIMS_FULL, n_layers=args.layers)
     B, G = args.batch, args.gamma
     W = gpu_weights(dims, 1234, dev)
     h = dfl.dflash_create(lib_cfg(dims, max(B, 1), G, dims["window"]), W)
     cyc = Cycle(dfl, h, dims, B, G, args.context, args.sigma, dev, 99 + rank)
     stream = torch.cuda.Stream(device=dev)
+    if args.profile_cycles:
+        with torch.cuda.stream(stream):
+            for _ in range(args.profile_cycles):
+                cyc.step()
+        torch.cuda.synchronize()
+        return {"profile_cycles": args.profile_cycles, "layers": args.layers,
+                "tau_sum": int(cyc.tau_sum.sum().item())}
 
     g_step = capture(cyc.step, stream)
     g_stand = capture(cyc.stand_in, stream)
@@ -519,7 +529,7 @@ def main():
         return
     res = run_ours(args, rank, ws)
     if rank == 0:
-        if not args.no_cpu and ws == 1:
+        if not args.no_cpu and ws == 1 and not args.profile_cycles:
             t_cycle, desc, wall = oracle_cycle_sample(dict(DIMS_FULL))
             res["cpu_baseline"] = {"value": round(1.0 / t_cycle, 5), "unit": "draft blocks/s",
                                    "cores": os.cpu_count(), "kind": "oracle",

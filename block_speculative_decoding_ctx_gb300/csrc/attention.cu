@@ -368,20 +368,38 @@ __global__ void __launch_bounds__((MT + 1) * 32)
   __threadfence();
   const float* part = a.part + (size_t)bg * S * kMq * HD;
   const float* ml = a.part_ml + (size_t)bg * S * kMq * 2;
-  for (int idx = threadIdx.x; idx < rows * HD; idx += blockDim.x) {
-    const int ri = idx / HD, d = idx % HD;
+  // normalised weight of every (split, row) in shared memory (the K/V stage
+  // buffers are free now): w[s][ri] = exp2(m_s - M) / sum_s' exp2(m_s' - M) l_s'
+  float* wsm = reinterpret_cast<float*>(smem);
+  for (int ri = threadIdx.x; ri < rows; ri += blockDim.x) {
     float M = -INFINITY;
     for (int s = 0; s < S; ++s) M = fmaxf(M, __ldcg(ml + ((size_t)s * kMq + ri) * 2));
-    float num = 0.0f, den = 0.0f;
+    float den = 0.0f;
     for (int s = 0; s < S; ++s) {
       const float ms = __ldcg(ml + ((size_t)s * kMq + ri) * 2);
       const float w = ms == -INFINITY ? 0.0f : exp2f(ms - M);
-      num += w * __ldcg(part + ((size_t)s * kMq + ri) * HD + d);
+      wsm[s * kMq + ri] = w;
       den += w * __ldcg(ml + ((size_t)s * kMq + ri) * 2 + 1);
     }
+    const float inv = 1.0f / den;
+    for (int s = 0; s < S; ++s) wsm[s * kMq + ri] *= inv;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < rows * (HD / 4); idx += blockDim.x) {
+    const int ri = idx / (HD / 4), d = (idx % (HD / 4)) * 4;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < S; ++s) {
+      const float w = wsm[s * kMq + ri];
+      const float4 p = __ldcg(reinterpret_cast<const float4*>(part + ((size_t)s * kMq + ri) * HD + d));
+      o.x += w * p.x;
+      o.y += w * p.y;
+      o.z += w * p.z;
+      o.w += w * p.w;
+    }
     const int hh = ri / a.gamma, i = ri % a.gamma;
-    a.out[(size_t)(b * a.gamma + i) * a.ld_out + (size_t)(g * group + hh) * HD + d] =
-        __float2bfloat16_rn(num / den);
+    __nv_bfloat16* dst = a.out + (size_t)(b * a.gamma + i) * a.ld_out + (size_t)(g * group + hh) * HD + d;
+    *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(o.x, o.y);
+    *reinterpret_cast<__nv_bfloat162*>(dst + 2) = __floats2bfloat162_rn(o.z, o.w);
   }
   if (threadIdx.x == 0) atomicExch(&a.counters[bg], 0);
 }

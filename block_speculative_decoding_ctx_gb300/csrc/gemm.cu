@@ -417,7 +417,9 @@ int gemm_token_tile(int M) {
 
 int gemm_plan_splits(int tiles, int K, int target_ctas) {
   const int kb = (K + kBK - 1) / kBK;
-  int s = (target_ctas + tiles - 1) / tiles;
+  // as many splits as fit in one wave of CTA slots: a second, mostly empty
+  // wave would cost a whole extra CTA lifetime
+  int s = target_ctas / tiles;
   const int max_s = kb / 4 > 0 ? kb / 4 : 1;  // at least 4 k-blocks per split
   if (s > max_s) s = max_s;
   if (s < 1) s = 1;

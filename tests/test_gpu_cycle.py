@@ -1,0 +1,162 @@
+"""GPU checks of the cycle as a whole: graph capture, device-side commit
+outputs, and device-side argument checks reported through the status word."""
+
+import numpy as np
+import pytest
+import torch
+
+import block_speculative_decoding_ctx_gb300 as dfl
+import dflash_testutil as tu
+from block_speculative_decoding_ctx_gb300 import synth
+from oracle import verify as over
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    dfl.lib()
+
+
+def _setup(name="small", B=2, gamma=8):
+    dims = synth.DIMS[name]
+    W = synth.weights(dims, 91, random_gains=True)
+    h = dfl.dflash_create(tu.lib_cfg(dims, batch_max=B, gamma_max=gamma, append_max=gamma), tu.to_dev(W))
+    rk, rv = synth.ring(dims, B, 92)
+    return dims, h, rk.cuda(), rv.cuda()
+
+
+def test_captured_cycle_replays_like_eager_calls():
+    dims, h, rk, rv = _setup()
+    B, gamma, V = 2, 8, dims["vocab"]
+    dev = torch.device("cuda")
+    feats = synth.features(dims, B * gamma, 93).reshape(B, gamma, dims["n_feat"], dims["feat_dim"]).cuda()
+    noise = synth.normal((B, gamma, V), 0.05, 94).cuda()
+
+    def state():
+        return dict(ctx=torch.tensor([300, 40], dtype=torch.int64, device=dev),
+                    anchor=torch.tensor([5, 7], dtype=torch.int32, device=dev),
+                    n_app=torch.tensor([3, 1], dtype=torch.int32, device=dev),
+                    rk=rk.clone(), rv=rv.clone(),
+                    logits=torch.empty((B, gamma - 1, V), device=dev),
+                    draft=torch.empty((B, gamma - 1), dtype=torch.int32, device=dev),
+                    target=torch.empty((B, gamma, V), device=dev),
+                    acc=torch.empty(B, dtype=torch.int32, device=dev),
+                    tok=torch.empty((B, gamma), dtype=torch.int32, device=dev),
+                    ws_a=dfl.workspace(dfl.dflash_append_workspace_bytes(h)),
+                    ws_d=dfl.workspace(dfl.dflash_draft_workspace_bytes(h)),
+                    ws_v=dfl.workspace(dfl.dflash_verify_workspace_bytes(B, gamma, V)))
+
+    def cycle(st):
+        dfl.dflash_ctx_append(h, feats, st["n_app"], st["ctx"], st["rk"], st["rv"], st["ws_a"])
+        dfl.dflash_draft_block(h, st["anchor"], st["ctx"], st["rk"], st["rv"], gamma, st["ws_d"],
+                               out=dict(logits=st["logits"], draft=st["draft"]))
+        torch.add(st["logits"], noise[:, :gamma - 1], out=st["target"][:, :gamma - 1])
+        torch.add(st["logits"][:, gamma - 2], noise[:, gamma - 1], out=st["target"][:, gamma - 1])
+        dfl.dflash_verify(dfl.DFLASH_VERIFY_GREEDY, st["target"], st["draft"], st["acc"], st["tok"],
+                          st["ws_v"], next_anchor=st["anchor"], n_append=st["n_app"])
+
+    eager = state()
+    hist_e = []
+    for _ in range(3):
+        cycle(eager)
+        hist_e.append((eager["acc"].cpu().clone(), eager["tok"].cpu().clone(), eager["ctx"].cpu().clone()))
+
+    graphed = state()
+    s = torch.cuda.Stream()
+    warm = state()
+    with torch.cuda.stream(s):
+        cycle(warm)                      # first calls outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        cycle(graphed)
+    # capture records work without running it: reset the state, then replay
+    fresh = state()
+    for k in ("ctx", "anchor", "n_app", "rk", "rv"):
+        graphed[k].copy_(fresh[k])
+    for ws in ("ws_a", "ws_d", "ws_v"):
+        graphed[ws].zero_()
+    torch.cuda.synchronize()
+    for i in range(3):
+        with torch.cuda.stream(s):
+            g.replay()
+        torch.cuda.synchronize()
+        a, t, c = hist_e[i]
+        assert torch.equal(graphed["acc"].cpu(), a)
+        assert torch.equal(graphed["tok"].cpu(), t)
+        assert torch.equal(graphed["ctx"].cpu(), c)
+    # commit outputs follow the committed tokens
+    n = graphed["acc"].cpu().numpy()
+    tok = graphed["tok"].cpu().numpy()
+    assert (graphed["n_app"].cpu().numpy() == n + 1).all()
+    assert (graphed["anchor"].cpu().numpy() == tok[np.arange(B), n]).all()
+
+
+def test_verify_commit_outputs_sampled():
+    B, gamma, V = 5, 6, 300
+    rng = np.random.default_rng(3)
+    p = rng.dirichlet(np.ones(V), size=(B, gamma)).astype(np.float32)
+    q = rng.dirichlet(np.ones(V), size=(B, gamma - 1)).astype(np.float32)
+    seeds = np.arange(B, dtype=np.uint64) + np.uint64(17)
+    from oracle import sampling as osamp
+    y = osamp.draft_draw(q, seeds, 4).astype(np.int32)
+    n_ref, tok_ref = over.sampled(p, q, y, seeds, 4)
+    dev = torch.device("cuda")
+    n = torch.empty(B, dtype=torch.int32, device=dev)
+    tok = torch.empty((B, gamma), dtype=torch.int32, device=dev)
+    anc = torch.empty(B, dtype=torch.int32, device=dev)
+    app = torch.empty(B, dtype=torch.int32, device=dev)
+    ws = dfl.workspace(dfl.dflash_verify_workspace_bytes(B, gamma, V))
+    dfl.dflash_verify(dfl.DFLASH_VERIFY_SAMPLED, torch.from_numpy(p).to(dev), torch.from_numpy(y).to(dev),
+                      n, tok, ws, q=torch.from_numpy(q).to(dev),
+                      seeds=torch.from_numpy(seeds.view(np.int64)).to(dev), step=4,
+                      next_anchor=anc, n_append=app)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(n.cpu().numpy(), n_ref)
+    np.testing.assert_array_equal(anc.cpu().numpy(), tok_ref[np.arange(B), n_ref])
+    np.testing.assert_array_equal(app.cpu().numpy(), n_ref + 1)
+
+
+def test_out_of_range_slot_and_anchor_are_reported_not_faulted():
+    dims, h, rk, rv = _setup(B=2)
+    B, gamma = 2, 8
+    dev = torch.device("cuda")
+    ws = dfl.workspace(dfl.dflash_draft_workspace_bytes(h))
+    bad_slot = torch.tensor([0, 9], dtype=torch.int32, device=dev)      # ring has 2 rows
+    dfl.dflash_draft_block(h, torch.tensor([1, 2], dtype=torch.int32, device=dev),
+                           torch.tensor([100, 100], dtype=torch.int64, device=dev), rk, rv, gamma, ws,
+                           out=dict(draft=torch.empty((B, gamma - 1), dtype=torch.int32, device=dev)),
+                           req_slot=bad_slot)
+    torch.cuda.synchronize()
+    assert dfl.dflash_read_status(ws) == -1
+    ws2 = dfl.workspace(dfl.dflash_draft_workspace_bytes(h))
+    dfl.dflash_draft_block(h, torch.tensor([1, 10 ** 6], dtype=torch.int32, device=dev),
+                           torch.tensor([100, 100], dtype=torch.int64, device=dev), rk, rv, gamma, ws2,
+                           out=dict(draft=torch.empty((B, gamma - 1), dtype=torch.int32, device=dev)))
+    torch.cuda.synchronize()
+    assert dfl.dflash_read_status(ws2) == -1
+    # a good call afterwards still works
+    ws3 = dfl.workspace(dfl.dflash_draft_workspace_bytes(h))
+    dfl.dflash_draft_block(h, torch.tensor([1, 2], dtype=torch.int32, device=dev),
+                           torch.tensor([100, 100], dtype=torch.int64, device=dev), rk, rv, gamma, ws3,
+                           out=dict(draft=torch.empty((B, gamma - 1), dtype=torch.int32, device=dev)))
+    torch.cuda.synchronize()
+    assert dfl.dflash_read_status(ws3) == 0
+
+
+def test_host_validation_rejects_bad_draft_calls():
+    dims, h, rk, rv = _setup(B=2)
+    dev = torch.device("cuda")
+    ws = dfl.workspace(dfl.dflash_draft_workspace_bytes(h))
+    a = torch.tensor([1, 2], dtype=torch.int32, device=dev)
+    L = torch.tensor([10, 10], dtype=torch.int64, device=dev)
+    with pytest.raises(dfl.DflashError) as e:
+        dfl.dflash_draft_block(h, a, L, rk, rv, 17, ws)                 # gamma > gamma_max
+    assert e.value.code == -2
+    with pytest.raises(dfl.DflashError) as e:
+        dfl.dflash_draft_block(h, a, L, rk, rv, 8, ws[:1024])           # workspace too small
+    assert e.value.code == -7
+    with pytest.raises(dfl.DflashError) as e:
+        dfl.dflash_draft_block(h, a, L, rk, rv, 8, ws, topk=17)
+    assert e.value.code == -2
