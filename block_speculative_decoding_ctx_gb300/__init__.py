@@ -100,7 +100,8 @@ def lib():
         "dflash_sample_workspace_bytes": (_SZ, [_I, _I]),
         "dflash_profile_enable": (_I, [_P, _I]),
         "dflash_profile_read": (_I, [_P, ctypes.POINTER(ctypes.c_float),
-                                     ctypes.POINTER(ctypes.c_double), _I, ctypes.POINTER(_I)]),
+                                     ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I), _I,
+                                     ctypes.POINTER(_I)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -275,10 +276,15 @@ def dflash_profile_enable(handle, n_pairs):
     _check(lib().dflash_profile_enable(handle.ptr, int(n_pairs)), "dflash_profile_enable")
 
 
-def dflash_profile_read(handle, cap=64):
-    """Per-GEMM (ms, algorithmic bytes) of the last draft_block call."""
+PROFILE_KINDS = {0: "gemm", 1: "attention", 2: "norm", 3: "topk", 4: "sampling"}
+
+
+def dflash_profile_read(handle, cap=128):
+    """Per-launch (ms, algorithmic bytes, kind) of the last draft_block call."""
     ms = (ctypes.c_float * cap)()
     by = (ctypes.c_double * cap)()
+    kd = (ctypes.c_int * cap)()
     n = ctypes.c_int(0)
-    _check(lib().dflash_profile_read(handle.ptr, ms, by, cap, ctypes.byref(n)), "dflash_profile_read")
-    return [(ms[i], by[i]) for i in range(n.value)]
+    _check(lib().dflash_profile_read(handle.ptr, ms, by, kd, cap, ctypes.byref(n)),
+           "dflash_profile_read")
+    return [(ms[i], by[i], PROFILE_KINDS.get(kd[i], str(kd[i]))) for i in range(n.value)]

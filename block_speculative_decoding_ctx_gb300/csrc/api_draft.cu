@@ -41,6 +41,7 @@ struct dflash_handle {
   // benchmark hook: event pairs around the GEMM launches of draft_block
   std::vector<cudaEvent_t> prof_events;
   std::vector<double> prof_bytes;
+  std::vector<int> prof_kinds;
   int prof_used = 0;
 };
 
@@ -72,19 +73,20 @@ int validate_config(const dflash_config& c) {
   return DFLASH_OK;
 }
 
+// Key splits per (request, KV head): a power of two up to the portable
+// cluster size, enough to give every SM a CTA when there are few heads.
 int attn_splits(const dflash_handle* h, int B) {
   const int bh = B * h->cfg.n_kv_heads;
   const int tiles = (h->cfg.window + 63) / 64;
-  int s = (h->num_sms + bh - 1) / bh;
-  if (s > tiles) s = tiles;
-  if (s > 64) s = 64;
-  return s < 1 ? 1 : s;
+  const int want = (h->num_sms + bh - 1) / bh;
+  int s = 1;
+  while (s * 2 <= want && s * 2 <= tiles && s * 2 <= 8) s *= 2;
+  return s;
 }
 
 struct DraftWs {
   int* status;
   int* gemm_counters;
-  int* attn_counters;
   int* topk_counters;
   int* samp_counters;
   float* x;
@@ -93,10 +95,9 @@ struct DraftWs {
   void* attn;
   void* mlp;
   void* hf;
+  void* q_lo;
   float* logits;
   float* gemm_partial;
-  float* attn_part;
-  float* attn_ml;
   unsigned long long* topk_keys;
   float* topk_ml;
   unsigned long long* samp_zsum;
@@ -110,29 +111,22 @@ DraftWs draft_layout(const dflash_handle* h, void* base) {
   const int qkv_dim = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
   const int q_dim = c.n_q_heads * c.head_dim;
   const int chunks = row_chunks(c.vocab);
-  const int mq = 16 * attn_row_tiles(c.n_q_heads, c.n_kv_heads, c.gamma_max);
-  size_t attn_rows = 0;  // (request, KV head, split) triples that write partials
-  for (int B = 1; B <= c.batch_max; ++B) {
-    const int S = attn_splits(h, B);
-    if (S > 1 && (size_t)B * c.n_kv_heads * S > attn_rows) attn_rows = (size_t)B * c.n_kv_heads * S;
-  }
   Carve cv(base, kWsHeader);
   DraftWs w;
   w.status = static_cast<int*>(base);
   w.gemm_counters = cv.take<int>(kGemmCounters);
-  w.attn_counters = cv.take<int>((size_t)c.batch_max * c.n_kv_heads);
   w.topk_counters = cv.take<int>(R);
   w.samp_counters = cv.take<int>(R);
+  // bf16 GEMM operands are [2, rows, K]: bf16 values, then their bf16 remainders
   w.x = cv.take<float>(M * c.hidden);
-  w.h = cv.take<uint16_t>(M * c.hidden);
+  w.h = cv.take<uint16_t>(2 * M * c.hidden);
   w.qkv = cv.take<uint16_t>(M * qkv_dim);
-  w.attn = cv.take<uint16_t>(M * q_dim);
-  w.mlp = cv.take<uint16_t>(M * c.ffn);
-  w.hf = cv.take<uint16_t>(R * c.hidden);
+  w.attn = cv.take<uint16_t>(2 * M * q_dim);
+  w.mlp = cv.take<uint16_t>(2 * M * c.ffn);
+  w.hf = cv.take<uint16_t>(2 * R * c.hidden);
+  w.q_lo = cv.take<uint16_t>(M * q_dim);
   w.logits = cv.take<float>(R * c.vocab);
   w.gemm_partial = cv.take<float>(kGemmPartialFloats);
-  w.attn_part = cv.take<float>(attn_rows * mq * c.head_dim);
-  w.attn_ml = cv.take<float>(attn_rows * mq * 2);
   w.topk_keys = cv.take<unsigned long long>(R * chunks * 16);
   w.topk_ml = cv.take<float>(R * chunks * 2);
   w.samp_zsum = cv.take<unsigned long long>(R * chunks);
@@ -157,19 +151,32 @@ AppendWs append_layout(const dflash_handle* h, void* base) {
   w.status = static_cast<int*>(base);
   w.gemm_counters = cv.take<int>(kGemmCounters);
   w.fused = cv.take<float>(M * c.hidden);
-  w.ht = cv.take<uint16_t>(M * c.hidden);
+  w.ht = cv.take<uint16_t>(2 * M * c.hidden);
   w.gemm_partial = cv.take<float>(kGemmPartialFloats);
   w.bytes = cv.off;
   return w;
 }
 
-GemmAOpts single_map() {
+GemmAOpts single_map(int split = 0) {
   GemmAOpts o;
   o.n_maps = 1;
   o.tiles_per_map = 1 << 30;
   o.row_offset = 0;
   o.dual = 0;
+  o.split = split;
   return o;
+}
+
+// Token operands are fed as a bf16 (value, remainder) pair — twice the MMA
+// columns, about 16 significant bits — always for the RMSNorm outputs that
+// feed QKV, gate|up and the context K/V, and for the other inputs while the
+// doubled token count still fits the tile the plain operand would use
+// (then the extra MMA work is free: the GEMM streams weights).
+constexpr int kFreeSplitTokens = 64;
+
+template <typename T>
+T* lo_half(void* base, size_t rows, size_t cols) {
+  return static_cast<T*>(base) + rows * cols;
 }
 
 GemmEpi epi_base(int kind, int M, int N, void* out, long long ld) {
@@ -183,27 +190,36 @@ GemmEpi epi_base(int kind, int M, int N, void* out, long long ld) {
   return e;
 }
 
-int splits_for(const dflash_handle* h, int n_tiles, int M, int K) {
-  const int BN = gemm_token_tile(M);
-  const int m_tiles = (M + BN - 1) / BN;
+int splits_for(const dflash_handle* h, int n_tiles, int M, int K, int split) {
+  const int BN = gemm_token_tile(split ? 2 * M : M);
+  const int T = split ? BN / 2 : BN;
+  const int m_tiles = (M + T - 1) / T;
   const int per_sm = BN <= 64 ? 2 : 1;
   return gemm_plan_splits(n_tiles * m_tiles, K, h->num_sms * per_sm);
 }
 
-// Launch one draft GEMM, bracketed by the handle's profiling events when
-// enabled.  bytes = algorithmic bytes of the launch.
+// Profiling brackets around one launch of the pass (no-ops unless enabled).
+int prof_begin(dflash_handle* h, cudaStream_t s) {
+  const int i = h->prof_used;
+  if (2 * (i + 1) > (int)h->prof_events.size()) return -1;
+  return cudaEventRecord(h->prof_events[2 * i], s) == cudaSuccess ? i : -1;
+}
+void prof_end(dflash_handle* h, cudaStream_t s, int slot, double bytes, int kind) {
+  if (slot < 0) return;
+  if (cudaEventRecord(h->prof_events[2 * slot + 1], s) != cudaSuccess) return;
+  h->prof_bytes[slot] = bytes;
+  h->prof_kinds[slot] = kind;
+  h->prof_used = slot + 1;
+}
+
+// Launch one draft GEMM.  bytes = algorithmic bytes of the launch.
 int draft_gemm(dflash_handle* h, const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void* x,
                int M, int K, const GemmEpi& e, const GemmScratch& sc, cudaStream_t s, double bytes) {
-  const int i = h->prof_used;
-  const bool prof = 2 * (i + 1) <= (int)h->prof_events.size();
-  if (prof && cudaEventRecord(h->prof_events[2 * i], s) != cudaSuccess) return DFLASH_ERR_CUDA;
-  const int rc = launch_gemm(A, ao, n_tiles, x, M, K, e, sc, splits_for(h, n_tiles, M, K), s, true);
+  const int slot = prof_begin(h, s);
+  const int rc = launch_gemm(A, ao, n_tiles, x, M, K, e, sc, splits_for(h, n_tiles, M, K, ao.split),
+                             s, true);
   if (rc) return rc;
-  if (prof) {
-    if (cudaEventRecord(h->prof_events[2 * i + 1], s) != cudaSuccess) return DFLASH_ERR_CUDA;
-    h->prof_bytes[i] = bytes;
-    h->prof_used = i + 1;
-  }
+  prof_end(h, s, slot, bytes, DFLASH_KIND_GEMM);
   return DFLASH_OK;
 }
 
@@ -216,6 +232,7 @@ int dflash_profile_enable(dflash_handle* h, int n_pairs) {
   for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
   h->prof_events.clear();
   h->prof_bytes.assign(n_pairs, 0.0);
+  h->prof_kinds.assign(n_pairs, 0);
   h->prof_used = 0;
   for (int i = 0; i < 2 * n_pairs; ++i) {
     cudaEvent_t e;
@@ -225,8 +242,8 @@ int dflash_profile_enable(dflash_handle* h, int n_pairs) {
   return DFLASH_OK;
 }
 
-int dflash_profile_read(dflash_handle* h, float* ms, double* bytes, int cap, int* count) {
-  if (!h || !count || cap < 0 || (cap > 0 && (!ms || !bytes))) return DFLASH_ERR_ARG;
+int dflash_profile_read(dflash_handle* h, float* ms, double* bytes, int* kinds, int cap, int* count) {
+  if (!h || !count || cap < 0 || (cap > 0 && (!ms || !bytes || !kinds))) return DFLASH_ERR_ARG;
   const int n = h->prof_used < cap ? h->prof_used : cap;
   if (n > 0 && cudaEventSynchronize(h->prof_events[2 * h->prof_used - 1]) != cudaSuccess)
     return DFLASH_ERR_CUDA;
@@ -234,6 +251,7 @@ int dflash_profile_read(dflash_handle* h, float* ms, double* bytes, int cap, int
     if (cudaEventElapsedTime(&ms[i], h->prof_events[2 * i], h->prof_events[2 * i + 1]) != cudaSuccess)
       return DFLASH_ERR_CUDA;
     bytes[i] = h->prof_bytes[i];
+    kinds[i] = h->prof_kinds[i];
   }
   *count = n;
   return DFLASH_OK;
@@ -332,10 +350,11 @@ int dflash_ctx_append(dflash_handle* h, int B, int n_max, const void* feats, con
     A.map[0] = h->w_c;
     GemmEpi e = epi_base(EPI_F32, M, d, ws.fused, d);
     const int nt = (d + 127) / 128;
-    rc = launch_gemm(A, single_map(), nt, feats, M, Kc, e, scratch, splits_for(h, nt, M, Kc), s, true);
+    rc = launch_gemm(A, single_map(), nt, feats, M, Kc, e, scratch, splits_for(h, nt, M, Kc, 0), s, true);
     if (rc) return rc;
   }
-  rc = launch_rmsnorm(ws.fused, M, d, static_cast<const float*>(h->w.g_c), c.eps, 0, ws.ht, s);
+  rc = launch_rmsnorm(ws.fused, M, d, static_cast<const float*>(h->w.g_c), c.eps, 0, ws.ht,
+                      lo_half<uint16_t>(ws.ht, M, d), s);
   if (rc) return rc;
   // K/V of every layer into the ring, up to kMaxAMaps layers per launch
   const int kvd = c.n_kv_heads * c.head_dim;
@@ -349,6 +368,7 @@ int dflash_ctx_append(dflash_handle* h, int B, int n_max, const void* feats, con
     ao.tiles_per_map = tiles_per_layer;
     ao.row_offset = c.n_q_heads * c.head_dim;
     ao.dual = 0;
+    ao.split = 1;
     GemmEpi e = epi_base(EPI_KV_RING, M, nl * 2 * kvd, nullptr, 0);
     e.ctx_len = ctx_len;
     e.rope_theta = c.rope_theta;
@@ -365,7 +385,7 @@ int dflash_ctx_append(dflash_handle* h, int B, int n_max, const void* feats, con
     e.layer0 = l0;
     e.status = ws.status;
     const int nt = nl * tiles_per_layer;
-    rc = launch_gemm(A, ao, nt, ws.ht, M, d, e, scratch, splits_for(h, nt, M, d), s, true);
+    rc = launch_gemm(A, ao, nt, ws.ht, M, d, e, scratch, splits_for(h, nt, M, d, 1), s, true);
     if (rc) return rc;
   }
   return launch_add_lengths(B, n_new, ctx_len, s);
@@ -412,15 +432,22 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
   const size_t ring_layer = (size_t)ring_batch * c.n_kv_heads * c.window * hd;
   int rc;
 
+  const bool split_o = M <= kFreeSplitTokens;   // O and down inputs
+  const bool split_head = R <= kFreeSplitTokens;
+  int slot = prof_begin(h, s);
   rc = launch_embed_norm(h->w.embed, anchor, B, gamma, h->mask_id, c.vocab, d,
                          static_cast<const float*>(h->layers[0].g_attn), c.eps, ws.x, ws.h,
-                         ws.status, s);
+                         lo_half<uint16_t>(ws.h, M, d), ws.status, s);
   if (rc) return rc;
+  prof_end(h, s, slot, (double)M * d * (2 + 4 + 4), DFLASH_KIND_NORM);
   AttnArgs aa;
   aa.qkv = static_cast<const __nv_bfloat16*>(ws.qkv);
   aa.ld_qkv = qkv_dim;
   aa.out = static_cast<__nv_bfloat16*>(ws.attn);
+  aa.out_lo = split_o ? lo_half<__nv_bfloat16>(ws.attn, M, qd) : nullptr;
   aa.ld_out = qd;
+  aa.q_lo = static_cast<const __nv_bfloat16*>(ws.q_lo);
+  aa.ld_q_lo = qd;
   aa.ctx_len = ctx_len;
   aa.req_slot = req_slot;
   aa.gamma = gamma;
@@ -431,10 +458,13 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
   aa.ring_batch = ring_batch;
   aa.splits = attn_splits(h, B);
   aa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)hd));
-  aa.part = ws.attn_part;
-  aa.part_ml = ws.attn_ml;
-  aa.counters = ws.attn_counters;
   aa.status = ws.status;
+  // ring K/V of the visible window + block q, k, v read, output written
+  double attn_bytes = 0.0;
+  {
+    const double win = c.window;  // upper bound; the visible part is min(L, W) per request
+    attn_bytes = (double)B * c.n_kv_heads * win * hd * 2 * 2 + (double)M * (qkv_dim + qd) * 2;
+  }
 
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerMaps& lm = h->maps[l];
@@ -448,33 +478,43 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
       e.rope_theta = c.rope_theta;
       e.rope_rows = (c.n_q_heads + c.n_kv_heads) * hd;
       e.hd = hd;
+      e.out_lo = ws.q_lo;
+      e.ld_lo = qd;
+      e.lo_cols = qd;
       const int nt = (qkv_dim + 127) / 128;
-      rc = draft_gemm(h, A, single_map(), nt, ws.h, M, d, e, scratch, s,
+      rc = draft_gemm(h, A, single_map(1), nt, ws.h, M, d, e, scratch, s,
                       2.0 * qkv_dim * d + 2.0 * M * d + 2.0 * M * qkv_dim);
       if (rc) return rc;
     }
+    slot = prof_begin(h, s);
     rc = launch_attention(static_cast<const char*>(ring_k) + l * ring_layer * 2,
                           static_cast<const char*>(ring_v) + l * ring_layer * 2, aa, B, s);
     if (rc) return rc;
+    prof_end(h, s, slot, attn_bytes, DFLASH_KIND_ATTENTION);
     {  // O projection + residual
       GemmAMaps A;
       A.map[0] = lm.o;
       GemmEpi e = epi_base(EPI_RESID, M, d, ws.x, d);
       const int nt = (d + 127) / 128;
-      rc = draft_gemm(h, A, single_map(), nt, ws.attn, M, qd, e, scratch, s,
+      rc = draft_gemm(h, A, single_map(split_o), nt, ws.attn, M, qd, e, scratch, s,
                       2.0 * d * qd + 2.0 * M * qd + 8.0 * M * d);
       if (rc) return rc;
     }
-    rc = launch_rmsnorm(ws.x, M, d, static_cast<const float*>(L.g_mlp), c.eps, 0, ws.h, s);
+    slot = prof_begin(h, s);
+    rc = launch_rmsnorm(ws.x, M, d, static_cast<const float*>(L.g_mlp), c.eps, 0, ws.h,
+                        lo_half<uint16_t>(ws.h, M, d), s);
     if (rc) return rc;
+    prof_end(h, s, slot, (double)M * d * 8, DFLASH_KIND_NORM);
     {  // gate | up + SwiGLU
       GemmAMaps A;
       A.map[0] = lm.gate;
       A.map[1] = lm.up;
-      GemmAOpts ao = single_map();
+      GemmAOpts ao = single_map(1);
       ao.n_maps = 2;
       ao.dual = 1;
       GemmEpi e = epi_base(EPI_SWIGLU, M, c.ffn, ws.mlp, c.ffn);
+      e.out_lo = split_o ? lo_half<uint16_t>(ws.mlp, M, c.ffn) : nullptr;
+      e.ld_lo = c.ffn;
       const int nt = c.ffn / 64;
       rc = draft_gemm(h, A, ao, nt, ws.h, M, d, e, scratch, s,
                       4.0 * c.ffn * d + 2.0 * M * d + 2.0 * M * c.ffn);
@@ -485,16 +525,19 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
       A.map[0] = lm.down;
       GemmEpi e = epi_base(EPI_RESID, M, d, ws.x, d);
       const int nt = (d + 127) / 128;
-      rc = draft_gemm(h, A, single_map(), nt, ws.mlp, M, c.ffn, e, scratch, s,
+      rc = draft_gemm(h, A, single_map(split_o), nt, ws.mlp, M, c.ffn, e, scratch, s,
                       2.0 * d * c.ffn + 2.0 * M * c.ffn + 8.0 * M * d);
       if (rc) return rc;
     }
+    slot = prof_begin(h, s);
     if (l + 1 < c.n_layers)
       rc = launch_rmsnorm(ws.x, M, d, static_cast<const float*>(h->layers[l + 1].g_attn), c.eps, 0,
-                          ws.h, s);
+                          ws.h, lo_half<uint16_t>(ws.h, M, d), s);
     else
-      rc = launch_rmsnorm(ws.x, R, d, static_cast<const float*>(h->w.g_final), c.eps, gamma, ws.hf, s);
+      rc = launch_rmsnorm(ws.x, R, d, static_cast<const float*>(h->w.g_final), c.eps, gamma, ws.hf,
+                          split_head ? lo_half<uint16_t>(ws.hf, R, d) : nullptr, s);
     if (rc) return rc;
+    prof_end(h, s, slot, (double)(l + 1 < c.n_layers ? M : R) * d * 8, DFLASH_KIND_NORM);
   }
   float* logits = out->logits ? out->logits : ws.logits;
   {  // shared LM head on the gamma - 1 MASK rows
@@ -502,18 +545,22 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
     A.map[0] = h->lm_head;
     GemmEpi e = epi_base(EPI_F32, R, c.vocab, logits, c.vocab);
     const int nt = (c.vocab + 127) / 128;
-    rc = draft_gemm(h, A, single_map(), nt, ws.hf, R, d, e, scratch, s,
+    rc = draft_gemm(h, A, single_map(split_head), nt, ws.hf, R, d, e, scratch, s,
                     2.0 * c.vocab * d + 2.0 * R * d + 4.0 * R * c.vocab);
     if (rc) return rc;
   }
   const int k_eff = topk > 0 ? topk : 1;
+  slot = prof_begin(h, s);
   rc = launch_topk_lse(logits, R, c.vocab, k_eff, ws.topk_keys, ws.topk_ml, ws.topk_counters,
                        topk > 0 ? out->topk_ids : nullptr, topk > 0 ? out->topk_vals : nullptr,
                        out->lse, sampling ? nullptr : out->draft, s);
   if (rc) return rc;
+  prof_end(h, s, slot, 4.0 * R * c.vocab, DFLASH_KIND_TOPK);
   if (sampling) {
+    slot = prof_begin(h, s);
     rc = launch_probs(R, c.vocab, logits, sampling->temperature, sampling->top_p, out->q, s);
     if (rc) return rc;
+    prof_end(h, s, slot, 8.0 * R * c.vocab, DFLASH_KIND_SAMPLING);
     if (out->draft) {
       rc = launch_sample_rows(R, c.vocab, out->q, c.vocab, gamma - 1, sampling->seeds, sampling->step,
                               0u, out->draft, gamma - 1, ws.samp_counters, ws.samp_zsum, ws.status, s);

@@ -18,6 +18,8 @@
 // every block key is visible).  Splits of the key range write unnormalised
 // partials, and the last CTA of a (request, KV head) merges them in split
 // order — deterministic.
+#include <cooperative_groups.h>
+
 #include <cmath>
 
 #include "attention.h"
@@ -26,6 +28,8 @@
 
 namespace dfl {
 namespace {
+
+namespace cg = cooperative_groups;
 
 constexpr int kKeys = 64;      // keys per context tile
 constexpr int kStages = 3;
@@ -61,6 +65,16 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Two adjacent outputs as bf16 hi parts, and their bf16 remainders when lo != null.
+__device__ __forceinline__ void store_pair2(__nv_bfloat16* hi, __nv_bfloat16* lo, size_t o, float y0,
+                                            float y1) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
+  *reinterpret_cast<__nv_bfloat162*>(hi + o) = h;
+  if (lo)
+    *reinterpret_cast<__nv_bfloat162*>(lo + o) =
+        __floats2bfloat162_rn(y0 - __low2float(h), y1 - __high2float(h));
+}
+
 __device__ __forceinline__ void named_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -71,11 +85,12 @@ struct WarpState {
   float o[NT][4];
   float m[2], l[2];
   uint32_t qa[HD / 16][4];           // Q fragments (A operand), k-steps of 16 dims
+  uint32_t ql[HD / 16][4];           // fragments of the bf16 remainder of Q
 };
 
 // Scores, online softmax and P.V of one key tile held in shared memory as
 // HD/64 swizzled halves [NK keys][64 dims] for K and for V.
-template <int HD, int NK>
+template <int HD, int NK, bool QLO>
 __device__ __forceinline__ void process_tile(WarpState<HD>& st, uint32_t k_base, uint32_t v_base,
                                              int n_valid, float scale_log2) {
   constexpr int NT_S = NK / 8;
@@ -97,6 +112,10 @@ __device__ __forceinline__ void process_tile(WarpState<HD>& st, uint32_t k_base,
       ldsm_x4(addr, b0, b1, b2, b3);
       mma_bf16(s[2 * kp], st.qa[kk][0], st.qa[kk][1], st.qa[kk][2], st.qa[kk][3], b0, b1);
       mma_bf16(s[2 * kp + 1], st.qa[kk][0], st.qa[kk][1], st.qa[kk][2], st.qa[kk][3], b2, b3);
+      if (QLO) {
+        mma_bf16(s[2 * kp], st.ql[kk][0], st.ql[kk][1], st.ql[kk][2], st.ql[kk][3], b0, b1);
+        mma_bf16(s[2 * kp + 1], st.ql[kk][0], st.ql[kk][1], st.ql[kk][2], st.ql[kk][3], b2, b3);
+      }
     }
   }
   // mask and scale; rows r0 = lane/4 (regs 0,1) and r1 = lane/4 + 8 (regs 2,3)
@@ -138,13 +157,19 @@ __device__ __forceinline__ void process_tile(WarpState<HD>& st, uint32_t k_base,
       st.l[e >> 1] += s[j][e];
     }
   }
-  // O += P V: k-steps of 16 keys; V^T fragments through ldmatrix.trans
+  // O += P V: k-steps of 16 keys; V^T fragments through ldmatrix.trans.  Keys
+  // past n_valid have P = 0, and their V halves are zeroed in registers so
+  // that whatever those slots hold cannot turn 0 * V into NaN.
+  const int kq = (lane & 3) << 1;
 #pragma unroll
   for (int ks = 0; ks < NK / 16; ++ks) {
     const uint32_t a0 = pack_bf16(s[2 * ks][0], s[2 * ks][1]);
     const uint32_t a1 = pack_bf16(s[2 * ks][2], s[2 * ks][3]);
     const uint32_t a2 = pack_bf16(s[2 * ks + 1][0], s[2 * ks + 1][1]);
     const uint32_t a3 = pack_bf16(s[2 * ks + 1][2], s[2 * ks + 1][3]);
+    const int k0 = ks * 16 + kq;  // keys of the low (k0, k0+1) and high (k0+8, k0+9) halves
+    const uint32_t m_lo = (k0 < n_valid ? 0x0000FFFFu : 0u) | (k0 + 1 < n_valid ? 0xFFFF0000u : 0u);
+    const uint32_t m_hi = (k0 + 8 < n_valid ? 0x0000FFFFu : 0u) | (k0 + 9 < n_valid ? 0xFFFF0000u : 0u);
 #pragma unroll
     for (int dp = 0; dp < HD / 16; ++dp) {
       const int key = ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
@@ -152,12 +177,19 @@ __device__ __forceinline__ void process_tile(WarpState<HD>& st, uint32_t k_base,
       const uint32_t addr = v_base + (dim >> 6) * kHalf + swz(key, dim & 63);
       uint32_t b0, b1, b2, b3;
       ldsm_x4_t(addr, b0, b1, b2, b3);
+      b0 &= m_lo;
+      b2 &= m_lo;
+      b1 &= m_hi;
+      b3 &= m_hi;
       mma_bf16(st.o[2 * dp], a0, a1, a2, a3, b0, b1);
       mma_bf16(st.o[2 * dp + 1], a0, a1, a2, a3, b2, b3);
     }
   }
 }
 
+// One CTA per (key split, KV head, request); the S splits of a (request, KV
+// head) form one thread-block cluster and merge their partial softmax states
+// through distributed shared memory.
 template <int HD, int MT>
 __global__ void __launch_bounds__((MT + 1) * 32)
     attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -167,14 +199,19 @@ __global__ void __launch_bounds__((MT + 1) * 32)
   constexpr int kMq = MT * 16;
   constexpr int kBlkKeys = 16;
   constexpr int kConsumers = MT * 32;
+  static_assert(kMq * (HD + 2 + 16) * 4 <= kStages * kStageBytes, "partials must fit the stage buffers");
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages];
-  __shared__ int abort_sh, last_sh;
+  __shared__ int abort_sh;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_s = smem + kStages * kStageBytes;            // [kMq][HD] swizzled halves
-  uint8_t* bk_s = q_s + kMq * HD * 2;                     // block K [16][HD]
+  uint8_t* ql_s = q_s + kMq * HD * 2;                     // remainder of Q, same layout
+  uint8_t* bk_s = ql_s + kMq * HD * 2;                    // block K [16][HD]
   uint8_t* bv_s = bk_s + kBlkKeys * HD * 2;               // block V [16][HD]
+  float* part_s = reinterpret_cast<float*>(smem);         // after the loop: [kMq][HD] partial O
+  float* ml_s = part_s + kMq * HD;                        // [kMq][2] running max (log2) and sum
+  float* w_s = ml_s + kMq * 2;                            // [rows of this CTA][16] merge weights
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -228,27 +265,34 @@ __global__ void __launch_bounds__((MT + 1) * 32)
         issued = i + 1;
       }
       if (abort_sh) {
-        // a wait gave up: let the copies in flight land before exiting
+        // a wait gave up: let the copies in flight land before reusing the buffers
         int dummy = 0;
         for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
           (void)mbar_wait_bounded(&full_bar[i % kStages], (uint32_t)(i / kStages) & 1u, &dummy,
                                   nullptr, 100000000ull);
       }
     }
-  } else {
+  }
+
+  WarpState<HD> st;
+  if (warp > 0) {
     // ----------------------------------------------------------- consumers
     const int ctid = threadIdx.x - 32;
     // Q rows ri = hh * gamma + i  <-  qkv row b*gamma + i, column (g*group + hh) * hd
     for (int idx = ctid; idx < kMq * (HD / 8); idx += kConsumers) {
       const int ri = idx / (HD / 8), ch = idx % (HD / 8);
-      uint4 v = make_uint4(0, 0, 0, 0);
+      uint4 v = make_uint4(0, 0, 0, 0), vl = make_uint4(0, 0, 0, 0);
       if (ri < rows) {
         const int hh = ri / a.gamma, i = ri % a.gamma;
         v = *reinterpret_cast<const uint4*>(a.qkv + (size_t)(b * a.gamma + i) * a.ld_qkv +
                                             (size_t)(g * group + hh) * HD + ch * 8);
+        if (a.q_lo)
+          vl = *reinterpret_cast<const uint4*>(a.q_lo + (size_t)(b * a.gamma + i) * a.ld_q_lo +
+                                               (size_t)(g * group + hh) * HD + ch * 8);
       }
       const int col = ch * 8;
       *reinterpret_cast<uint4*>(q_s + (col >> 6) * (kMq * 128) + swz(ri, col & 63)) = v;
+      *reinterpret_cast<uint4*>(ql_s + (col >> 6) * (kMq * 128) + swz(ri, col & 63)) = vl;
     }
     if (do_block) {
       const size_t kcol = (size_t)a.n_q * HD + (size_t)g * HD;
@@ -269,7 +313,6 @@ __global__ void __launch_bounds__((MT + 1) * 32)
     }
     named_sync(1, kConsumers);
 
-    WarpState<HD> st;
     const int mt = warp - 1;
     {
       const uint32_t qb = smem_u32(q_s);
@@ -279,6 +322,8 @@ __global__ void __launch_bounds__((MT + 1) * 32)
         const int col = kk * 16 + ((lane >> 4) << 3);
         ldsm_x4(qb + (col >> 6) * (kMq * 128) + swz(row, col & 63), st.qa[kk][0], st.qa[kk][1],
                 st.qa[kk][2], st.qa[kk][3]);
+        ldsm_x4(qb + kMq * HD * 2 + (col >> 6) * (kMq * 128) + swz(row, col & 63), st.ql[kk][0],
+                st.ql[kk][1], st.ql[kk][2], st.ql[kk][3]);
       }
     }
 #pragma unroll
@@ -286,9 +331,13 @@ __global__ void __launch_bounds__((MT + 1) * 32)
     st.m[0] = st.m[1] = -INFINITY;
     st.l[0] = st.l[1] = 0.0f;
 
-    if (do_block)
-      process_tile<HD, kBlkKeys>(st, smem_u32(bk_s), smem_u32(bv_s), a.gamma, a.scale_log2);
-
+    const bool qlo = a.q_lo != nullptr;
+    if (do_block) {
+      if (qlo)
+        process_tile<HD, kBlkKeys, true>(st, smem_u32(bk_s), smem_u32(bv_s), a.gamma, a.scale_log2);
+      else
+        process_tile<HD, kBlkKeys, false>(st, smem_u32(bk_s), smem_u32(bv_s), a.gamma, a.scale_log2);
+    }
     for (int i = 0; i < nt; ++i) {
       const int s = i % kStages;
       const uint32_t ph = (uint32_t)(i / kStages) & 1u;
@@ -297,127 +346,124 @@ __global__ void __launch_bounds__((MT + 1) * 32)
       uint8_t* vs = ks + kTileBytes;
       const int slot0 = (t0 + i) * kKeys;
       const int valid = n_valid - slot0 < kKeys ? n_valid - slot0 : kKeys;
-      if (valid < kKeys) {
-        // slots past the visible window may hold anything: clear their V rows
-        named_sync(2, kConsumers);
-        for (int idx = ctid; idx < (kKeys - valid) * (HD / 8); idx += kConsumers) {
-          const int r = valid + idx / (HD / 8), col = (idx % (HD / 8)) * 8;
-          *reinterpret_cast<uint4*>(vs + (col >> 6) * (kKeys * 128) + swz(r, col & 63)) =
-              make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-        named_sync(2, kConsumers);
-      }
-      process_tile<HD, kKeys>(st, smem_u32(ks), smem_u32(vs), valid, a.scale_log2);
+      if (qlo)
+        process_tile<HD, kKeys, true>(st, smem_u32(ks), smem_u32(vs), valid, a.scale_log2);
+      else
+        process_tile<HD, kKeys, false>(st, smem_u32(ks), smem_u32(vs), valid, a.scale_log2);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[s]);
     }
-
     // full row sums
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       st.l[h] += __shfl_xor_sync(0xffffffffu, st.l[h], 1);
       st.l[h] += __shfl_xor_sync(0xffffffffu, st.l[h], 2);
     }
-    const int r0 = mt * 16 + (lane >> 2), r1 = r0 + 8;
-    const int bg = b * a.n_kv + g;
-    if (S == 1) {
-      // final output directly
+  }
+
+  const int r0 = (warp - 1) * 16 + (lane >> 2), r1 = r0 + 8;
+  if (S == 1) {
+    if (warp > 0) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int ri = h ? r1 : r0;
         if (ri < rows) {
           const float inv = 1.0f / st.l[h];
           const int hh = ri / a.gamma, i = ri % a.gamma;
-          __nv_bfloat16* dst = a.out + (size_t)(b * a.gamma + i) * a.ld_out + (size_t)(g * group + hh) * HD;
+          const size_t off = (size_t)(b * a.gamma + i) * a.ld_out + (size_t)(g * group + hh) * HD;
 #pragma unroll
           for (int t = 0; t < WarpState<HD>::NT; ++t) {
             const int d = t * 8 + ((lane & 3) << 1);
-            *reinterpret_cast<__nv_bfloat162*>(dst + d) =
-                __floats2bfloat162_rn(st.o[t][2 * h] * inv, st.o[t][2 * h + 1] * inv);
+            store_pair2(a.out, a.out_lo, off + d, st.o[t][2 * h] * inv, st.o[t][2 * h + 1] * inv);
           }
         }
       }
-    } else {
-      float* part = a.part + ((size_t)bg * S + split) * kMq * HD;
-      float* ml = a.part_ml + ((size_t)bg * S + split) * kMq * 2;
+    }
+    return;
+  }
+
+  // ------------------------------------------------ merge across the cluster
+  // every stage buffer has been consumed (or the CTA gave up): reuse them
+  __syncthreads();
+  if (warp > 0) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int ri = h ? r1 : r0;
+    for (int h = 0; h < 2; ++h) {
+      const int ri = h ? r1 : r0;
 #pragma unroll
-        for (int t = 0; t < WarpState<HD>::NT; ++t) {
-          const int d = t * 8 + ((lane & 3) << 1);
-          *reinterpret_cast<float2*>(part + (size_t)ri * HD + d) = make_float2(st.o[t][2 * h], st.o[t][2 * h + 1]);
-        }
-        if ((lane & 3) == 0) {
-          ml[ri * 2 + 0] = st.m[h];
-          ml[ri * 2 + 1] = st.l[h];
-        }
+      for (int t = 0; t < WarpState<HD>::NT; ++t) {
+        const int d = t * 8 + ((lane & 3) << 1);
+        *reinterpret_cast<float2*>(part_s + ri * HD + d) = make_float2(st.o[t][2 * h], st.o[t][2 * h + 1]);
+      }
+      if ((lane & 3) == 0) {
+        ml_s[ri * 2 + 0] = st.m[h];
+        ml_s[ri * 2 + 1] = st.l[h];
       }
     }
   }
-  if (S == 1) return;
-
-  // ------------------------------------------------ merge the key splits
-  __threadfence();
-  __syncthreads();
-  const int bg = b * a.n_kv + g;
-  if (threadIdx.x == 0) last_sh = (atomicAdd(&a.counters[bg], 1) == S - 1);
-  __syncthreads();
-  if (!last_sh) return;
-  __threadfence();
-  const float* part = a.part + (size_t)bg * S * kMq * HD;
-  const float* ml = a.part_ml + (size_t)bg * S * kMq * 2;
-  // normalised weight of every (split, row) in shared memory (the K/V stage
-  // buffers are free now): w[s][ri] = exp2(m_s - M) / sum_s' exp2(m_s' - M) l_s'
-  float* wsm = reinterpret_cast<float*>(smem);
-  for (int ri = threadIdx.x; ri < rows; ri += blockDim.x) {
+  cg::cluster_group cluster = cg::this_cluster();
+  cluster.sync();
+  const int rank = (int)cluster.block_rank();
+  const int my_rows = (rows - rank + S - 1) / S;           // rows rank, rank + S, ...
+  if ((int)threadIdx.x < my_rows) {
+    const int ri = rank + (int)threadIdx.x * S;
     float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, __ldcg(ml + ((size_t)s * kMq + ri) * 2));
+    for (int s = 0; s < S; ++s) M = fmaxf(M, cluster.map_shared_rank(ml_s, s)[ri * 2]);
     float den = 0.0f;
     for (int s = 0; s < S; ++s) {
-      const float ms = __ldcg(ml + ((size_t)s * kMq + ri) * 2);
+      const float* ml = cluster.map_shared_rank(ml_s, s);
+      const float ms = ml[ri * 2];
       const float w = ms == -INFINITY ? 0.0f : exp2f(ms - M);
-      wsm[s * kMq + ri] = w;
-      den += w * __ldcg(ml + ((size_t)s * kMq + ri) * 2 + 1);
+      w_s[threadIdx.x * 16 + s] = w;
+      den += w * ml[ri * 2 + 1];
     }
     const float inv = 1.0f / den;
-    for (int s = 0; s < S; ++s) wsm[s * kMq + ri] *= inv;
+    for (int s = 0; s < S; ++s) w_s[threadIdx.x * 16 + s] *= inv;
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < rows * (HD / 4); idx += blockDim.x) {
-    const int ri = idx / (HD / 4), d = (idx % (HD / 4)) * 4;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int idx = threadIdx.x; idx < my_rows * (HD / 2); idx += blockDim.x) {
+    const int k = idx / (HD / 2), d = (idx % (HD / 2)) * 2;
+    const int ri = rank + k * S;
+    float o0 = 0.0f, o1 = 0.0f;
     for (int s = 0; s < S; ++s) {
-      const float w = wsm[s * kMq + ri];
-      const float4 p = __ldcg(reinterpret_cast<const float4*>(part + ((size_t)s * kMq + ri) * HD + d));
-      o.x += w * p.x;
-      o.y += w * p.y;
-      o.z += w * p.z;
-      o.w += w * p.w;
+      const float2 p = *reinterpret_cast<const float2*>(cluster.map_shared_rank(part_s, s) + ri * HD + d);
+      o0 += w_s[k * 16 + s] * p.x;
+      o1 += w_s[k * 16 + s] * p.y;
     }
     const int hh = ri / a.gamma, i = ri % a.gamma;
-    __nv_bfloat16* dst = a.out + (size_t)(b * a.gamma + i) * a.ld_out + (size_t)(g * group + hh) * HD + d;
-    *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(o.x, o.y);
-    *reinterpret_cast<__nv_bfloat162*>(dst + 2) = __floats2bfloat162_rn(o.z, o.w);
+    store_pair2(a.out, a.out_lo,
+                (size_t)(b * a.gamma + i) * a.ld_out + (size_t)(g * group + hh) * HD + d, o0, o1);
   }
-  if (threadIdx.x == 0) atomicExch(&a.counters[bg], 0);
+  // no CTA may leave while another still reads its shared memory
+  cluster.sync();
 }
 
 template <int HD, int MT>
 int launch_t(const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a, int B, cudaStream_t s) {
-  constexpr size_t smem = 1024 + (size_t)kStages * 2 * kKeys * HD * 2 + (size_t)MT * 16 * HD * 2 +
+  constexpr size_t smem = 1024 + (size_t)kStages * 2 * kKeys * HD * 2 + 2 * (size_t)MT * 16 * HD * 2 +
                           2 * 16 * HD * 2;
   auto kern = attn_kernel<HD, MT>;
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return DFLASH_ERR_LAUNCH;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+      return DFLASH_ERR_LAUNCH;
     attr = true;
   }
-  dim3 grid(a.splits, a.n_kv, B);
-  kern<<<grid, (MT + 1) * 32, smem, s>>>(tk, tv, a);
-  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_LAUNCH;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.splits, a.n_kv, B);
+  cfg.blockDim = dim3((MT + 1) * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr_c[1];
+  attr_c[0].id = cudaLaunchAttributeClusterDimension;
+  attr_c[0].val.clusterDim.x = a.splits;
+  attr_c[0].val.clusterDim.y = 1;
+  attr_c[0].val.clusterDim.z = 1;
+  cfg.attrs = attr_c;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, tk, tv, a) != cudaSuccess) return DFLASH_ERR_LAUNCH;
+  return DFLASH_OK;
 }
 
 }  // namespace

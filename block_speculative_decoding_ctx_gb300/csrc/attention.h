@@ -10,16 +10,17 @@ namespace dfl {
 struct AttnArgs {
   const __nv_bfloat16* qkv;  // [B*gamma, (Hq + 2 Hkv) hd]: rotated q, rotated k, v
   long long ld_qkv;
+  const __nv_bfloat16* q_lo; // [B*gamma, Hq hd] bf16 remainders of the rotated queries (or null)
+  long long ld_q_lo;
   __nv_bfloat16* out;        // [B*gamma, Hq hd]
+  __nv_bfloat16* out_lo;     // bf16 remainders of the output (or null)
   long long ld_out;
   const int64_t* ctx_len;    // [B] context lengths L
   const int32_t* req_slot;   // [B] ring rows or nullptr
   int gamma, n_q, n_kv, hd, window, ring_batch;
-  int splits;                // key-range splits per (request, KV head)
+  int splits;                // key-range splits per (request, KV head): 1, 2, 4 or 8; the
+                             // splits of one head run as a thread-block cluster
   float scale_log2;          // log2(e) / sqrt(hd)
-  float* part;               // [B*Hkv][splits][16*row_tiles][hd]
-  float* part_ml;            // [B*Hkv][splits][16*row_tiles][2]
-  int* counters;             // [B*Hkv], zero between launches
   int* status;
 };
 

@@ -72,11 +72,19 @@ __device__ __forceinline__ float rope_apply(float x, float partner, const RopeRo
   return rr.first_half ? fmaf(x, c, -partner * s) : fmaf(x, c, partner * s);
 }
 
-// Epilogue of 16 consecutive tokens of this thread's row.  `xchg` holds the
-// chunk as [16][128] floats so that partner rows can be read.  Every thread
-// of the CTA calls it (it synchronises).
+__device__ __forceinline__ void store_bf16_pair(const GemmEpi& e, size_t o_hi, size_t o_lo, float y) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(y);
+  static_cast<__nv_bfloat16*>(e.out)[o_hi] = hi;
+  if (e.out_lo)
+    static_cast<__nv_bfloat16*>(e.out_lo)[o_lo] = __float2bfloat16_rn(y - __bfloat162float(hi));
+}
+
+// Epilogue of up to 16 consecutive tokens (the first `ntok` of v are real)
+// of this thread's row.  `xchg` holds the chunk as [16][128] floats so that
+// partner rows can be read.  Every thread of the CTA calls it (it
+// synchronises).
 __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const float (&v)[16],
-                               int tok_base, int tile_n, int r, float* xchg) {
+                               int tok_base, int ntok, int tile_n, int r, float* xchg) {
   const int kind = e.kind;
   const bool needs_xchg = (kind == EPI_QKV || kind == EPI_SWIGLU || kind == EPI_KV_RING);
   if (needs_xchg) {
@@ -90,12 +98,12 @@ __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const floa
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int tok = tok_base + j;
-        if (tok < e.M) {
+        if (j < ntok && tok < e.M) {
           const size_t o = (size_t)tok * e.ld + n;
           if (kind == EPI_F32)
             static_cast<float*>(e.out)[o] = v[j];
           else if (kind == EPI_BF16)
-            static_cast<__nv_bfloat16*>(e.out)[o] = __float2bfloat16_rn(v[j]);
+            store_bf16_pair(e, o, (size_t)tok * e.ld_lo + n, v[j]);
           else
             static_cast<float*>(e.out)[o] += v[j];
         }
@@ -111,13 +119,17 @@ __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const floa
 #pragma unroll 4
       for (int j = 0; j < 16; ++j) {
         const int tok = tok_base + j;
-        if (tok < e.M) {
+        if (j < ntok && tok < e.M) {
           float y = v[j];
           if (rot) {
             const float pos = (float)(e.ctx_len[tok / e.gamma] + tok % e.gamma);
             y = rope_apply(v[j], xchg[j * 128 + pr], rr, pos);
           }
-          static_cast<__nv_bfloat16*>(e.out)[(size_t)tok * e.ld + n] = __float2bfloat16_rn(y);
+          const __nv_bfloat16 hi = __float2bfloat16_rn(y);
+          static_cast<__nv_bfloat16*>(e.out)[(size_t)tok * e.ld + n] = hi;
+          if (e.out_lo && n < e.lo_cols)
+            static_cast<__nv_bfloat16*>(e.out_lo)[(size_t)tok * e.ld_lo + n] =
+                __float2bfloat16_rn(y - __bfloat162float(hi));
         }
       }
     }
@@ -127,10 +139,9 @@ __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const floa
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int tok = tok_base + j;
-        if (tok < e.M) {
+        if (j < ntok && tok < e.M) {
           const float g = v[j], u = xchg[j * 128 + r + 64];
-          static_cast<__nv_bfloat16*>(e.out)[(size_t)tok * e.ld + f] =
-              __float2bfloat16_rn(silu(g) * u);
+          store_bf16_pair(e, (size_t)tok * e.ld + f, (size_t)tok * e.ld_lo + f, silu(g) * u);
         }
       }
     }
@@ -146,7 +157,7 @@ __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const floa
 #pragma unroll 4
     for (int j = 0; j < 16; ++j) {
       const int tok = tok_base + j;
-      if (tok < e.M) {
+      if (j < ntok && tok < e.M) {
         const int b = tok / e.n_max, jr = tok % e.n_max;
         if (jr < e.n_new[b]) {
           const long long pos = e.ctx_len[b] + jr;
@@ -228,7 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       map_i = tile_n / ao.tiles_per_map;
       row0 = ao.row_offset + (tile_n % ao.tiles_per_map) * 128;
     }
-    const int tok0 = tile_m * BN;
+    const int T = ao.split ? BN / 2 : BN;  // tokens per tile
+    const int tok0 = tile_m * T;
     // weights do not depend on the previous kernel: start streaming them
     // before waiting for it (programmatic dependent launch)
     const int pre = nkb < STAGES ? nkb : STAGES;
@@ -244,8 +256,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     grid_dependency_wait();
-    for (int i = 0; i < pre; ++i)
-      tma_load_2d(smem + i * kStage + kABytes, &tmB, &full_bar[i], (kb0 + i) * kBK, tok0, pol_x);
+    for (int i = 0; i < pre; ++i) {
+      uint8_t* sb = smem + i * kStage + kABytes;
+      tma_load_2d(sb, &tmB, &full_bar[i], (kb0 + i) * kBK, tok0, pol_x);
+      if (ao.split) tma_load_2d(sb + T * 128, &tmB, &full_bar[i], (kb0 + i) * kBK, epi.M + tok0, pol_x);
+    }
     issued = pre;
     for (int i = pre; i < nkb; ++i) {
       const int s = i % STAGES;
@@ -261,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sa, &A.map[map_i], &full_bar[s], kc, row0, pol_w);
       }
       tma_load_2d(sa + kABytes, &tmB, &full_bar[s], kc, tok0, pol_x);
+      if (ao.split) tma_load_2d(sa + kABytes + T * 128, &tmB, &full_bar[s], kc, epi.M + tok0, pol_x);
       issued = i + 1;
     }
   } else if (warp == 1 && lane == 0) {
@@ -299,27 +315,51 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* xchg = reinterpret_cast<float*>(smem);
   const bool aborted = abort_sh != 0 || !acc_ok;
 
+  // tokens per tile; with split operands column j (hi) pairs with column T + j (lo)
+  const int T = ao.split ? BN / 2 : BN;
+  const int ntok = T < 16 ? T : 16;
+  const int n_chunks = (T + 15) / 16;
+  auto load_chunk = [&](int c, float (&v)[16]) {
+    uint32_t raw[16];
+    if (!ao.split) {
+      tmem_ld_x16(t_row + c * 16, raw);
+      tc_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]);
+    } else if (T >= 16) {
+      uint32_t lo[16];
+      tmem_ld_x16(t_row + c * 16, raw);
+      tmem_ld_x16(t_row + T + c * 16, lo);
+      tc_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]) + __uint_as_float(lo[j]);
+    } else {
+      tmem_ld_x16(t_row, raw);
+      tc_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(raw[j]) + __uint_as_float(raw[j + 8]);
+#pragma unroll
+      for (int j = 8; j < 16; ++j) v[j] = 0.0f;
+    }
+  };
+
   if (!aborted) {
     if (args.splits == 1) {
-      for (int c = 0; c < BN / 16; ++c) {
-        uint32_t raw[16];
-        tmem_ld_x16(t_row + c * 16, raw);
-        tc_wait_ld();
+      for (int c = 0; c < n_chunks; ++c) {
         float v[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]);
-        epilogue_chunk(epi, ao, v, tile_m * BN + c * 16, tile_n, r, xchg);
+        load_chunk(c, v);
+        epilogue_chunk(epi, ao, v, tile_m * T + c * 16, ntok, tile_n, r, xchg);
       }
     } else {
       const int tile_lin = tile_m * gridDim.x + tile_n;
-      float* part = args.partial + (size_t)tile_lin * args.splits * (BN * 128);
-      float* mine = part + (size_t)split * (BN * 128);
-      for (int c = 0; c < BN / 16; ++c) {
-        uint32_t raw[16];
-        tmem_ld_x16(t_row + c * 16, raw);
-        tc_wait_ld();
+      const size_t per_split = (size_t)n_chunks * 16 * 128;
+      float* part = args.partial + (size_t)tile_lin * args.splits * per_split;
+      float* mine = part + (size_t)split * per_split;
+      for (int c = 0; c < n_chunks; ++c) {
+        float v[16];
+        load_chunk(c, v);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) mine[(c * 16 + j) * 128 + r] = __uint_as_float(raw[j]);
+        for (int j = 0; j < 16; ++j) mine[(c * 16 + j) * 128 + r] = v[j];
       }
       __threadfence();
       __syncthreads();
@@ -327,16 +367,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();
       if (last_sh) {
         __threadfence();
-        for (int c = 0; c < BN / 16; ++c) {
+        for (int c = 0; c < n_chunks; ++c) {
           float v[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = 0.0f;
           for (int s = 0; s < args.splits; ++s) {
-            const float* ps = part + (size_t)s * (BN * 128);
+            const float* ps = part + (size_t)s * per_split;
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] += __ldcg(ps + (c * 16 + j) * 128 + r);
           }
-          epilogue_chunk(epi, ao, v, tile_m * BN + c * 16, tile_n, r, xchg);
+          epilogue_chunk(epi, ao, v, tile_m * T + c * 16, ntok, tile_n, r, xchg);
         }
         if (threadIdx.x == 0) atomicExch(&args.counters[tile_lin], 0);
       }
@@ -412,7 +452,8 @@ int encode_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t o
 int gemm_token_tile(int M) {
   if (M <= 16) return 16;
   if (M <= 64) return 64;
-  return 128;
+  if (M <= 128) return 128;
+  return 256;
 }
 
 int gemm_plan_splits(int tiles, int K, int target_ctas) {
@@ -429,18 +470,20 @@ int gemm_plan_splits(int tiles, int K, int target_ctas) {
 int launch_gemm(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void* x, int M, int K,
                 const GemmEpi& epi, const GemmScratch& scratch, int splits, cudaStream_t s,
                 bool pdl) {
-  const int BN = gemm_token_tile(M);
+  const int BN = gemm_token_tile(ao.split ? 2 * M : M);
+  const int T = ao.split ? BN / 2 : BN;
   CUtensorMap tmB;
-  int rc = encode_bf16_2d(&tmB, x, (uint64_t)K, (uint64_t)M, kBK, (uint32_t)BN);
+  int rc = encode_bf16_2d(&tmB, x, (uint64_t)K, (uint64_t)(ao.split ? 2 * M : M), kBK, (uint32_t)T);
   if (rc) return rc;
-  const int m_tiles = (M + BN - 1) / BN;
+  const int m_tiles = (M + T - 1) / T;
   const int kb = (K + kBK - 1) / kBK;
   if (splits < 1) splits = 1;
   if (splits > kb) splits = kb;
   const size_t tiles = (size_t)n_tiles * m_tiles;
+  const size_t per_split = (size_t)((T + 15) / 16) * 16 * 128;
   if (splits > 1) {
     if (tiles > (size_t)scratch.counters_cap) splits = 1;
-    while (splits > 1 && tiles * splits * BN * 128 > scratch.partial_cap_floats) --splits;
+    while (splits > 1 && tiles * splits * per_split > scratch.partial_cap_floats) --splits;
   }
   GemmArgs args;
   args.K = K;
@@ -452,7 +495,8 @@ int launch_gemm(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void
   switch (BN) {
     case 16: return launch_one<16, 6>(A, tmB, ao, args, epi, grid, s, pdl);
     case 64: return launch_one<64, 4>(A, tmB, ao, args, epi, grid, s, pdl);
-    default: return launch_one<128, 6>(A, tmB, ao, args, epi, grid, s, pdl);
+    case 128: return launch_one<128, 6>(A, tmB, ao, args, epi, grid, s, pdl);
+    default: return launch_one<256, 4>(A, tmB, ao, args, epi, grid, s, pdl);
   }
 }
 

@@ -30,6 +30,9 @@ struct GemmAOpts {
   int tiles_per_map;  // 128-row tiles served by each descriptor (multi-map mode)
   int row_offset;     // first weight row inside each descriptor
   int dual;           // SwiGLU: map[0] gate rows, map[1] up rows, 64-row boxes
+  int split;          // token operand is [2M, K]: rows [0, M) bf16 hi parts, rows [M, 2M) the
+                      // bf16 remainders (x - hi); a tile of BN columns holds BN/2 tokens as
+                      // (hi, lo) column pairs and the epilogue adds them
 };
 
 struct GemmArgs {
@@ -46,6 +49,10 @@ struct GemmEpi {
   int N;            // valid output features (SwiGLU: F)
   void* out;
   long long ld;
+  void* out_lo;     // EPI_BF16 / EPI_QKV / EPI_SWIGLU: bf16 remainder x - bf16(x) is written
+                    // here too ([M, ld_lo]; EPI_QKV: only the rope_rows_lo first columns)
+  long long ld_lo;
+  int lo_cols;      // EPI_QKV: columns [0, lo_cols) get a remainder
   // rotary positions
   const int64_t* ctx_len;
   int gamma;
@@ -83,7 +90,8 @@ int gemm_token_tile(int M);
 int gemm_plan_splits(int tiles, int K, int target_ctas);
 
 // Y = X W^T through the epilogue.  n_tiles = number of 128-row weight tiles
-// (SwiGLU: F / 64).  x: bf16 [M, K] row-major.
+// (SwiGLU: F / 64).  x: bf16 [M, K] row-major, or [2M, K] (hi rows then
+// remainder rows) when ao.split.
 int launch_gemm(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void* x, int M, int K,
                 const GemmEpi& epi, const GemmScratch& scratch, int splits, cudaStream_t s,
                 bool pdl);

@@ -15,12 +15,22 @@ namespace {
 
 constexpr int kNormThreads = 256;
 
+// y as a bf16 pair: hi = bf16(y) and lo = bf16(y - hi), so that hi + lo
+// carries y to about 16 bits for the split-operand GEMMs.
+__device__ __forceinline__ void store_pair(__nv_bfloat16* hi, __nv_bfloat16* lo, size_t o, float y) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(y);
+  hi[o] = h;
+  if (lo) lo[o] = __float2bfloat16_rn(y - __bfloat162float(h));
+}
+
 // One CTA per block row m = b * gamma + i: x[m] = embed[id] (fp32 residual
-// stream), h[m] = bf16(RMSNorm(x[m]) * g), id = anchor[b] for i = 0, MASK after.
+// stream), h[m] = RMSNorm(x[m]) * g as a bf16 pair (h_lo may be null),
+// id = anchor[b] for i = 0, MASK after.
 __global__ void __launch_bounds__(kNormThreads)
     embed_norm_kernel(const __nv_bfloat16* __restrict__ embed, const int32_t* __restrict__ anchor,
                       int gamma, int mask_id, int vocab, int d, const float* __restrict__ g, float eps,
-                      float* __restrict__ x, __nv_bfloat16* __restrict__ h, int* status) {
+                      float* __restrict__ x, __nv_bfloat16* __restrict__ h,
+                      __nv_bfloat16* __restrict__ h_lo, int* status) {
   __shared__ float red[33];
   const int m = blockIdx.x;
   const int b = m / gamma, i = m % gamma;
@@ -39,14 +49,16 @@ __global__ void __launch_bounds__(kNormThreads)
   ss = block_sum(ss, red);
   const float rs = rsqrtf(ss / (float)d + eps);
   for (int c = threadIdx.x; c < d; c += kNormThreads)
-    h[(size_t)m * d + c] = __float2bfloat16_rn(__bfloat162float(e[c]) * rs * g[c]);
+    store_pair(h, h_lo, (size_t)m * d + c, __bfloat162float(e[c]) * rs * g[c]);
 }
 
-// out row r = bf16(RMSNorm(x[src(r)]) * g).  gather_gamma = 0: src(r) = r;
-// otherwise the MASK rows: src(r) = (r / (G - 1)) * G + r % (G - 1) + 1.
+// out row r = RMSNorm(x[src(r)]) * g as a bf16 pair (out_lo may be null).
+// gather_gamma = 0: src(r) = r; otherwise the MASK rows:
+// src(r) = (r / (G - 1)) * G + r % (G - 1) + 1.
 __global__ void __launch_bounds__(kNormThreads)
     rmsnorm_kernel(const float* __restrict__ x, int d, const float* __restrict__ g, float eps,
-                   int gather_gamma, __nv_bfloat16* __restrict__ out) {
+                   int gather_gamma, __nv_bfloat16* __restrict__ out,
+                   __nv_bfloat16* __restrict__ out_lo) {
   __shared__ float red[33];
   const int r = blockIdx.x;
   int src = r;
@@ -60,7 +72,7 @@ __global__ void __launch_bounds__(kNormThreads)
   ss = block_sum(ss, red);
   const float rs = rsqrtf(ss / (float)d + eps);
   for (int c = threadIdx.x; c < d; c += kNormThreads)
-    out[(size_t)r * d + c] = __float2bfloat16_rn(xr[c] * rs * g[c]);
+    store_pair(out, out_lo, (size_t)r * d + c, xr[c] * rs * g[c]);
 }
 
 // ------------------------------------------------------ top-k and LSE
@@ -216,18 +228,19 @@ __global__ void add_lengths_kernel(int B, const int32_t* __restrict__ n_new, int
 }  // namespace
 
 int launch_embed_norm(const void* embed, const int32_t* anchor, int B, int gamma, int mask_id,
-                      int vocab, int d, const float* g, float eps, float* x, void* h, int* status,
-                      cudaStream_t s) {
+                      int vocab, int d, const float* g, float eps, float* x, void* h, void* h_lo,
+                      int* status, cudaStream_t s) {
   embed_norm_kernel<<<B * gamma, kNormThreads, 0, s>>>(
       static_cast<const __nv_bfloat16*>(embed), anchor, gamma, mask_id, vocab, d, g, eps, x,
-      static_cast<__nv_bfloat16*>(h), status);
+      static_cast<__nv_bfloat16*>(h), static_cast<__nv_bfloat16*>(h_lo), status);
   return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_LAUNCH;
 }
 
 int launch_rmsnorm(const float* x, int rows, int d, const float* g, float eps, int gather_gamma,
-                   void* out, cudaStream_t s) {
+                   void* out, void* out_lo, cudaStream_t s) {
   rmsnorm_kernel<<<rows, kNormThreads, 0, s>>>(x, d, g, eps, gather_gamma,
-                                               static_cast<__nv_bfloat16*>(out));
+                                               static_cast<__nv_bfloat16*>(out),
+                                               static_cast<__nv_bfloat16*>(out_lo));
   return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_LAUNCH;
 }
 

@@ -248,14 +248,16 @@ int dflash_verify(int mode, int B, int gamma, int vocab, const float* target, co
 
 /* Benchmark hook.  dflash_profile_enable(h, n) creates n pairs of CUDA
  * events (n = 0 destroys them); afterwards every draft_block call on h
- * records a pair around each of its first n GEMM launches, on the call's
+ * records a pair around each of its first n kernel launches, on the call's
  * stream.  dflash_profile_read synchronises on the last recorded event and
- * returns, for each GEMM launch of the last call, its duration in ms and its
- * algorithmic bytes (weights + activations read + outputs written, each
- * counted once); *count receives the number of launches (<= cap).
+ * returns, for each launch of the last call, its duration in ms, its
+ * algorithmic bytes (operands read + results written, each counted once) and
+ * its kind (DFLASH_KIND_*); *count receives the number of launches (<= cap).
  * Not for use while a graph is being captured. */
+enum { DFLASH_KIND_GEMM = 0, DFLASH_KIND_ATTENTION = 1, DFLASH_KIND_NORM = 2,
+       DFLASH_KIND_TOPK = 3, DFLASH_KIND_SAMPLING = 4 };
 int dflash_profile_enable(dflash_handle* h, int n_pairs);
-int dflash_profile_read(dflash_handle* h, float* ms, double* bytes, int cap, int* count);
+int dflash_profile_read(dflash_handle* h, float* ms, double* bytes, int* kinds, int cap, int* count);
 
 /* Copy the workspace status word to the host (synchronises the stream). */
 int dflash_read_status(const void* workspace, int32_t* status_host, dflash_stream_t stream);
