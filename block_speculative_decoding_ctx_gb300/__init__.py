@@ -99,6 +99,8 @@ def lib():
         "dflash_sample_draft": (_I, [_I, _I, _I, _P, _P, ctypes.c_uint64, _P, _P, _SZ, _P]),
         "dflash_sample_workspace_bytes": (_SZ, [_I, _I]),
         "dflash_profile_enable": (_I, [_P, _I]),
+        "dflash_verify_noalloc": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, ctypes.c_uint64, _P, _P, _P,
+                                       _P, _P]),
         "dflash_profile_read": (_I, [_P, ctypes.POINTER(ctypes.c_float),
                                      ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I), _I,
                                      ctypes.POINTER(_I)]),
@@ -288,3 +290,15 @@ def dflash_profile_read(handle, cap=128):
     _check(lib().dflash_profile_read(handle.ptr, ms, by, kd, cap, ctypes.byref(n)),
            "dflash_profile_read")
     return [(ms[i], by[i], PROFILE_KINDS.get(kd[i], str(kd[i]))) for i in range(n.value)]
+
+
+def dflash_verify_noalloc(mode, target, draft, accept_len, tokens, q=None, seeds=None, step=0,
+                          next_anchor=None, n_append=None, stream=None):
+    """dflash_verify without a workspace, for callers that cannot provide
+    device memory: the scratch is a fixed array inside the library (see
+    include/dflash.h for its size limit and for why overlapping calls race)."""
+    B, gamma, V = target.shape
+    _check(lib().dflash_verify_noalloc(int(mode), B, gamma, V, _ptr(target), _ptr(q), _ptr(draft),
+                                       _ptr(seeds), ctypes.c_uint64(int(step) & (2 ** 64 - 1)),
+                                       _ptr(accept_len), _ptr(tokens), _ptr(next_anchor),
+                                       _ptr(n_append), _stream(stream)), "dflash_verify_noalloc")

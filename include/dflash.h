@@ -259,6 +259,38 @@ enum { DFLASH_KIND_GEMM = 0, DFLASH_KIND_ATTENTION = 1, DFLASH_KIND_NORM = 2,
 int dflash_profile_enable(dflash_handle* h, int n_pairs);
 int dflash_profile_read(dflash_handle* h, float* ms, double* bytes, int* kinds, int cap, int* count);
 
+/* Verification for callers that cannot provide device memory.  The pages have
+ * no counterpart to this entry point: it exists for callers that cannot
+ * allocate or lend device memory at the point where they verify — for example
+ * a serving process whose device memory is reserved up front by another
+ * allocator, where a further cudaMalloc would fail or fragment the
+ * reservation, or a host framework that forbids plug-ins from allocating
+ * device memory (cudaMalloc also synchronises the device).
+ *
+ * Same arguments and results as dflash_verify, without the workspace: the
+ * kernels' scratch (status word, per-request tickets, argmax keys, chunk
+ * masses) lives in one fixed 256 KiB __device__ array inside this library,
+ * which every GPU that loads the library holds until the process exits.  The
+ * call allocates nothing (no cudaMalloc, no cudaFree, no allocating library
+ * routine); it clears the part of the array that must start at zero with an
+ * asynchronous memset on the given stream.
+ *   Limit: 256 + 256*ceil(4B/256) + 256*ceil(8*B*gamma/256)
+ *          + 16*B*ceil(vocab/8192) bytes (rounded up to 256) must not exceed
+ *          256 KiB — e.g. B <= 256 at gamma 16 and vocabulary 151,936;
+ *          larger calls return DFLASH_ERR_SHAPE and launch nothing.
+ *   The first call on a device looks up the array's device address with that
+ *   device current (cudaGetSymbolAddress) and caches it; make that first call
+ *   before any stream capture.
+ *   Every call on a device shares the one array and the array keeps the last
+ *   call's contents: calls whose work overlaps on the GPU (two streams, or
+ *   graphs replayed concurrently) race on it and must be serialised by the
+ *   caller.  Device-side errors go to the array's status word, which callers
+ *   of this entry point cannot read back; use dflash_verify for that. */
+int dflash_verify_noalloc(int mode, int B, int gamma, int vocab, const float* target,
+                          const float* q, const int32_t* draft, const uint64_t* seeds,
+                          uint64_t step, int32_t* accept_len, int32_t* tokens,
+                          int32_t* next_anchor, int32_t* n_append, dflash_stream_t stream);
+
 /* Copy the workspace status word to the host (synchronises the stream). */
 int dflash_read_status(const void* workspace, int32_t* status_host, dflash_stream_t stream);
 
