@@ -53,7 +53,7 @@ constexpr int kGemmCounters = 8192;
 bool aligned(const void* p, size_t a) { return p && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int validate_config(const dflash_config& c) {
-  if (c.hidden < 64 || c.hidden % 64) return DFLASH_ERR_UNSUPPORTED;
+  if (c.hidden < 64 || c.hidden % 64 || c.hidden > 12288) return DFLASH_ERR_UNSUPPORTED;
   if (c.head_dim != 64 && c.head_dim != 128) return DFLASH_ERR_UNSUPPORTED;
   if (c.n_q_heads < 1 || c.n_kv_heads < 1 || c.n_q_heads % c.n_kv_heads) return DFLASH_ERR_SHAPE;
   if ((c.n_q_heads * c.head_dim) % 64) return DFLASH_ERR_UNSUPPORTED;
@@ -202,11 +202,15 @@ int splits_for(const dflash_handle* h, int n_tiles, int M, int K, int split) {
 int prof_begin(dflash_handle* h, cudaStream_t s) {
   const int i = h->prof_used;
   if (2 * (i + 1) > (int)h->prof_events.size()) return -1;
-  return cudaEventRecord(h->prof_events[2 * i], s) == cudaSuccess ? i : -1;
+  // external records become event nodes (with timestamps) when the stream is captured
+  return cudaEventRecordWithFlags(h->prof_events[2 * i], s, cudaEventRecordExternal) == cudaSuccess
+             ? i
+             : -1;
 }
 void prof_end(dflash_handle* h, cudaStream_t s, int slot, double bytes, int kind) {
   if (slot < 0) return;
-  if (cudaEventRecord(h->prof_events[2 * slot + 1], s) != cudaSuccess) return;
+  if (cudaEventRecordWithFlags(h->prof_events[2 * slot + 1], s, cudaEventRecordExternal) != cudaSuccess)
+    return;
   h->prof_bytes[slot] = bytes;
   h->prof_kinds[slot] = kind;
   h->prof_used = slot + 1;

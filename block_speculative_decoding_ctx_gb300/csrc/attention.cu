@@ -194,6 +194,7 @@ template <int HD, int MT>
 __global__ void __launch_bounds__((MT + 1) * 32)
     attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 const AttnArgs a) {
+  pdl_enter();
   constexpr int kTileBytes = kKeys * HD * 2;     // one of K or V, all halves
   constexpr int kStageBytes = 2 * kTileBytes;
   constexpr int kMq = MT * 16;
@@ -455,13 +456,15 @@ int launch_t(const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a, in
   cfg.blockDim = dim3((MT + 1) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr_c[1];
+  cudaLaunchAttribute attr_c[2];
   attr_c[0].id = cudaLaunchAttributeClusterDimension;
   attr_c[0].val.clusterDim.x = a.splits;
   attr_c[0].val.clusterDim.y = 1;
   attr_c[0].val.clusterDim.z = 1;
+  attr_c[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr_c[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr_c;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, kern, tk, tv, a) != cudaSuccess) return DFLASH_ERR_LAUNCH;
   return DFLASH_OK;
 }

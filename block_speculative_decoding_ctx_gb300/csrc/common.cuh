@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "dflash.h"
 
 namespace dfl {
@@ -362,6 +364,33 @@ __device__ __forceinline__ void grid_dependency_wait() {
 }
 __device__ __forceinline__ void grid_dependents_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// First statement of every kernel launched with launch_pdl: let the next
+// kernel of the stream be scheduled now (it waits for our completion before
+// it reads our results), then wait for the previous kernel's results.
+__device__ __forceinline__ void pdl_enter() {
+  grid_dependents_launch();
+  grid_dependency_wait();
+}
+
+// Launch with programmatic stream serialization, so the kernel's CTAs can be
+// scheduled while the previous kernel of the stream is still finishing.
+template <typename... KArgs, typename... Args>
+inline int launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                      Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...) == cudaSuccess ? DFLASH_OK
+                                                                                     : DFLASH_ERR_LAUNCH;
 }
 
 }  // namespace dfl

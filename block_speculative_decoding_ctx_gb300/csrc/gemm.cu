@@ -226,6 +226,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+  // the next kernel may be scheduled now; it waits for our completion before
+  // reading what we write
+  grid_dependents_launch();
 
   int issued = 0;
   if (warp == 0 && lane == 0) {
@@ -382,7 +385,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  grid_dependents_launch();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);

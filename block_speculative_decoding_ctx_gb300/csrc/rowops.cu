@@ -25,12 +25,15 @@ __device__ __forceinline__ void store_pair(__nv_bfloat16* hi, __nv_bfloat16* lo,
 
 // One CTA per block row m = b * gamma + i: x[m] = embed[id] (fp32 residual
 // stream), h[m] = RMSNorm(x[m]) * g as a bf16 pair (h_lo may be null),
-// id = anchor[b] for i = 0, MASK after.
+// id = anchor[b] for i = 0, MASK after.  The row is staged in shared memory
+// (dynamic, 4 d bytes) with 16-byte loads issued together.
 __global__ void __launch_bounds__(kNormThreads)
     embed_norm_kernel(const __nv_bfloat16* __restrict__ embed, const int32_t* __restrict__ anchor,
                       int gamma, int mask_id, int vocab, int d, const float* __restrict__ g, float eps,
                       float* __restrict__ x, __nv_bfloat16* __restrict__ h,
                       __nv_bfloat16* __restrict__ h_lo, int* status) {
+  pdl_enter();
+  extern __shared__ float row_s[];
   __shared__ float red[33];
   const int m = blockIdx.x;
   const int b = m / gamma, i = m % gamma;
@@ -39,40 +42,54 @@ __global__ void __launch_bounds__(kNormThreads)
     if (threadIdx.x == 0) report_status(status, DFLASH_ERR_ARG);
     id = 0;
   }
-  const __nv_bfloat16* e = embed + (size_t)id * d;
+  const uint4* e8 = reinterpret_cast<const uint4*>(embed + (size_t)id * d);
   float ss = 0.0f;
-  for (int c = threadIdx.x; c < d; c += kNormThreads) {
-    const float v = __bfloat162float(e[c]);
-    x[(size_t)m * d + c] = v;
-    ss += v * v;
+#pragma unroll 4
+  for (int c = threadIdx.x; c < d / 8; c += kNormThreads) {
+    const uint4 u = __ldg(e8 + c);
+    const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&u);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float v = __bfloat162float(hv[k]);
+      row_s[c * 8 + k] = v;
+      ss += v * v;
+    }
   }
   ss = block_sum(ss, red);
   const float rs = rsqrtf(ss / (float)d + eps);
-  for (int c = threadIdx.x; c < d; c += kNormThreads)
-    store_pair(h, h_lo, (size_t)m * d + c, __bfloat162float(e[c]) * rs * g[c]);
+  for (int c = threadIdx.x; c < d; c += kNormThreads) {
+    const float v = row_s[c];
+    x[(size_t)m * d + c] = v;
+    store_pair(h, h_lo, (size_t)m * d + c, v * rs * g[c]);
+  }
 }
 
 // out row r = RMSNorm(x[src(r)]) * g as a bf16 pair (out_lo may be null).
 // gather_gamma = 0: src(r) = r; otherwise the MASK rows:
-// src(r) = (r / (G - 1)) * G + r % (G - 1) + 1.
+// src(r) = (r / (G - 1)) * G + r % (G - 1) + 1.  The row is staged in
+// shared memory (dynamic, 4 d bytes) with 16-byte loads issued together.
 __global__ void __launch_bounds__(kNormThreads)
     rmsnorm_kernel(const float* __restrict__ x, int d, const float* __restrict__ g, float eps,
                    int gather_gamma, __nv_bfloat16* __restrict__ out,
                    __nv_bfloat16* __restrict__ out_lo) {
+  pdl_enter();
+  extern __shared__ float row_s[];
   __shared__ float red[33];
   const int r = blockIdx.x;
   int src = r;
   if (gather_gamma > 0) src = (r / (gather_gamma - 1)) * gather_gamma + r % (gather_gamma - 1) + 1;
-  const float* xr = x + (size_t)src * d;
+  const float4* x4 = reinterpret_cast<const float4*>(x + (size_t)src * d);
   float ss = 0.0f;
-  for (int c = threadIdx.x; c < d; c += kNormThreads) {
-    const float v = xr[c];
-    ss += v * v;
+#pragma unroll 4
+  for (int c = threadIdx.x; c < d / 4; c += kNormThreads) {
+    const float4 v = __ldcg(x4 + c);
+    reinterpret_cast<float4*>(row_s)[c] = v;
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
   }
   ss = block_sum(ss, red);
   const float rs = rsqrtf(ss / (float)d + eps);
   for (int c = threadIdx.x; c < d; c += kNormThreads)
-    store_pair(out, out_lo, (size_t)r * d + c, xr[c] * rs * g[c]);
+    store_pair(out, out_lo, (size_t)r * d + c, row_s[c] * rs * g[c]);
 }
 
 // ------------------------------------------------------ top-k and LSE
@@ -140,6 +157,7 @@ __global__ void __launch_bounds__(kTopkThreads)
                     unsigned long long* __restrict__ part_keys, float* __restrict__ part_ml,
                     int* counters, int32_t* __restrict__ ids, float* __restrict__ vals,
                     float* __restrict__ lse, int32_t* __restrict__ draft) {
+  pdl_enter();
   __shared__ unsigned long long cand[kTopkThreads * KT];
   __shared__ unsigned long long sel[KT];
   __shared__ float redm[32], reds[32];
@@ -151,15 +169,24 @@ __global__ void __launch_bounds__(kTopkThreads)
   unsigned long long top[KT];
 #pragma unroll
   for (int j = 0; j < KT; ++j) top[j] = 0;
-  float m = -INFINITY, s = 0.0f;
-  for (int v = v0 + threadIdx.x; v < v1; v += kTopkThreads) {
-    const float x = __ldg(row + v);
-    insert_key<KT>(top, vkey(x, v));
-    if (x > m) {
-      s = (m == -INFINITY ? 0.0f : s * expf(m - x)) + 1.0f;
-      m = x;
-    } else {
-      s += expf(x - m);
+  // the thread's 32 elements of the chunk, loaded together
+  constexpr int kPer = kRowChunk / kTopkThreads;
+  float xv[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int v = v0 + threadIdx.x + j * kTopkThreads;
+    xv[j] = v < v1 ? __ldg(row + v) : -INFINITY;
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) m = fmaxf(m, xv[j]);
+  float s = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int v = v0 + threadIdx.x + j * kTopkThreads;
+    if (v < v1) {
+      s += expf(xv[j] - m);
+      insert_key<KT>(top, vkey(xv[j], v));
     }
   }
 #pragma unroll
@@ -221,6 +248,7 @@ __global__ void __launch_bounds__(kTopkThreads)
 }
 
 __global__ void add_lengths_kernel(int B, const int32_t* __restrict__ n_new, int64_t* ctx_len) {
+  pdl_enter();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b < B) ctx_len[b] += n_new[b];
 }
@@ -230,18 +258,16 @@ __global__ void add_lengths_kernel(int B, const int32_t* __restrict__ n_new, int
 int launch_embed_norm(const void* embed, const int32_t* anchor, int B, int gamma, int mask_id,
                       int vocab, int d, const float* g, float eps, float* x, void* h, void* h_lo,
                       int* status, cudaStream_t s) {
-  embed_norm_kernel<<<B * gamma, kNormThreads, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(embed), anchor, gamma, mask_id, vocab, d, g, eps, x,
-      static_cast<__nv_bfloat16*>(h), static_cast<__nv_bfloat16*>(h_lo), status);
-  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_LAUNCH;
+  return launch_pdl(embed_norm_kernel, dim3(B * gamma), dim3(kNormThreads), (size_t)d * 4, s,
+                    static_cast<const __nv_bfloat16*>(embed), anchor, gamma, mask_id, vocab, d, g, eps,
+                    x, static_cast<__nv_bfloat16*>(h), static_cast<__nv_bfloat16*>(h_lo), status);
 }
 
 int launch_rmsnorm(const float* x, int rows, int d, const float* g, float eps, int gather_gamma,
                    void* out, void* out_lo, cudaStream_t s) {
-  rmsnorm_kernel<<<rows, kNormThreads, 0, s>>>(x, d, g, eps, gather_gamma,
-                                               static_cast<__nv_bfloat16*>(out),
-                                               static_cast<__nv_bfloat16*>(out_lo));
-  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_LAUNCH;
+  return launch_pdl(rmsnorm_kernel, dim3(rows), dim3(kNormThreads), (size_t)d * 4, s, x, d, g, eps,
+                    gather_gamma,
+                    static_cast<__nv_bfloat16*>(out), static_cast<__nv_bfloat16*>(out_lo));
 }
 
 int topk_slots(int k) { return k <= 4 ? 4 : 16; }
@@ -252,17 +278,14 @@ int launch_topk_lse(const float* logits, int rows, int V, int k, unsigned long l
   const int chunks = row_chunks(V);
   dim3 grid(chunks, rows);
   if (k <= 4)
-    topk_lse_kernel<4><<<grid, kTopkThreads, 0, s>>>(logits, V, k, chunks, part_keys, part_ml,
-                                                     counters, ids, vals, lse, draft);
-  else
-    topk_lse_kernel<16><<<grid, kTopkThreads, 0, s>>>(logits, V, k, chunks, part_keys, part_ml,
-                                                      counters, ids, vals, lse, draft);
-  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_LAUNCH;
+    return launch_pdl(topk_lse_kernel<4>, grid, dim3(kTopkThreads), 0, s, logits, V, k, chunks,
+                      part_keys, part_ml, counters, ids, vals, lse, draft);
+  return launch_pdl(topk_lse_kernel<16>, grid, dim3(kTopkThreads), 0, s, logits, V, k, chunks,
+                    part_keys, part_ml, counters, ids, vals, lse, draft);
 }
 
 int launch_add_lengths(int B, const int32_t* n_new, int64_t* ctx_len, cudaStream_t s) {
-  add_lengths_kernel<<<(B + 127) / 128, 128, 0, s>>>(B, n_new, ctx_len);
-  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_LAUNCH;
+  return launch_pdl(add_lengths_kernel, dim3((B + 127) / 128), dim3(128), 0, s, B, n_new, ctx_len);
 }
 
 }  // namespace dfl

@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(kThreads)
                          int gamma, int V, int chunks, int32_t* __restrict__ accept_len,
                          int32_t* __restrict__ tokens, int32_t* __restrict__ next_anchor,
                          int32_t* __restrict__ n_append, int* counters, unsigned long long* keys) {
+  pdl_enter();
   __shared__ unsigned long long red[33];
   __shared__ int s_last;
   const int c = blockIdx.x;
@@ -88,21 +89,22 @@ __global__ void __launch_bounds__(kThreads)
   const int v0 = c * kRowChunk;
   const int v1 = min(V, v0 + kRowChunk);
 
-  unsigned long long best = 0ull;
-  int v = v0 + threadIdx.x;
-  for (; v + 3 * kThreads < v1; v += 4 * kThreads) {
-    const float a = __ldg(row + v), bb = __ldg(row + v + kThreads),
-                cc = __ldg(row + v + 2 * kThreads), d = __ldg(row + v + 3 * kThreads);
-    unsigned long long k0 = argmax_key(a, v), k1 = argmax_key(bb, v + kThreads),
-                       k2 = argmax_key(cc, v + 2 * kThreads), k3 = argmax_key(d, v + 3 * kThreads);
-    k0 = k1 > k0 ? k1 : k0;
-    k2 = k3 > k2 ? k3 : k2;
-    k0 = k2 > k0 ? k2 : k0;
-    best = k0 > best ? k0 : best;
+  // the thread's 32 elements of the chunk, loaded together
+  constexpr int kPer = kRowChunk / kThreads;
+  float xv[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int v = v0 + threadIdx.x + j * kThreads;
+    xv[j] = v < v1 ? __ldg(row + v) : -INFINITY;
   }
-  for (; v < v1; v += kThreads) {
-    const unsigned long long k = argmax_key(__ldg(row + v), v);
-    best = k > best ? k : best;
+  unsigned long long best = 0ull;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int v = v0 + threadIdx.x + j * kThreads;
+    if (v < v1) {
+      const unsigned long long k = argmax_key(xv[j], v);
+      best = k > best ? k : best;
+    }
   }
   best = block_max_u64(best, red);
   if (threadIdx.x == 0) {
@@ -161,6 +163,7 @@ __global__ void __launch_bounds__(kThreads)
                           int32_t* __restrict__ accept_len, int32_t* __restrict__ tokens,
                           int32_t* __restrict__ next_anchor, int32_t* __restrict__ n_append,
                           int* counters, unsigned long long* zsum, int* status) {
+  pdl_enter();
   __shared__ unsigned long long red[33];
   __shared__ int s_n, s_last, s_chunk, s_use_resid, s_found;
   __shared__ unsigned long long s_T;
@@ -263,6 +266,7 @@ __global__ void __launch_bounds__(kThreads)
                        int rows_per_req, const uint64_t* __restrict__ seeds, uint64_t step,
                        uint32_t purpose, int32_t* __restrict__ out, long long out_stride,
                        int* counters, unsigned long long* zsum, int* status) {
+  pdl_enter();
   __shared__ unsigned long long red[33];
   __shared__ int s_last, s_chunk, s_found;
   __shared__ unsigned long long s_T;
@@ -343,6 +347,7 @@ __device__ __forceinline__ void hist_add(unsigned long long* hist, unsigned* his
 __global__ void __launch_bounds__(kProbThreads)
     probs_kernel(const float* __restrict__ logits, int V, float invT, float top_p,
                  float* __restrict__ probs) {
+  pdl_enter();
   __shared__ float redf[33];
   __shared__ unsigned long long redu[33];
   __shared__ unsigned long long hist[256];
@@ -469,9 +474,8 @@ int launch_verify_greedy(int B, int gamma, int V, const float* target, const int
                          int* /*status*/, cudaStream_t s) {
   const int chunks = row_chunks(V);
   dim3 grid(chunks, B * gamma);
-  verify_greedy_kernel<<<grid, kThreads, 0, s>>>(target, draft, gamma, V, chunks, accept_len,
-                                                 tokens, next_anchor, n_append, counters, keys);
-  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_LAUNCH;
+  return launch_pdl(verify_greedy_kernel, grid, dim3(kThreads), 0, s, target, draft, gamma, V, chunks,
+                    accept_len, tokens, next_anchor, n_append, counters, keys);
 }
 
 int launch_verify_sampled(int B, int gamma, int V, const float* p, const float* q,
@@ -481,10 +485,8 @@ int launch_verify_sampled(int B, int gamma, int V, const float* p, const float* 
                           cudaStream_t s) {
   const int chunks = row_chunks(V);
   dim3 grid(chunks, B);
-  verify_sampled_kernel<<<grid, kThreads, 0, s>>>(p, q, draft, seeds, step, gamma, V, chunks,
-                                                  accept_len, tokens, next_anchor, n_append,
-                                                  counters, zsum, status);
-  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_LAUNCH;
+  return launch_pdl(verify_sampled_kernel, grid, dim3(kThreads), 0, s, p, q, draft, seeds, step, gamma,
+                    V, chunks, accept_len, tokens, next_anchor, n_append, counters, zsum, status);
 }
 
 int launch_sample_rows(int rows, int V, const float* w, long long row_stride, int rows_per_req,
@@ -493,15 +495,14 @@ int launch_sample_rows(int rows, int V, const float* w, long long row_stride, in
                        cudaStream_t s) {
   const int chunks = row_chunks(V);
   dim3 grid(chunks, rows);
-  sample_rows_kernel<<<grid, kThreads, 0, s>>>(w, row_stride, V, chunks, rows_per_req, seeds, step,
-                                               purpose, out, out_stride, counters, zsum, status);
-  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_LAUNCH;
+  return launch_pdl(sample_rows_kernel, grid, dim3(kThreads), 0, s, w, row_stride, V, chunks,
+                    rows_per_req, seeds, step, purpose, out, out_stride, counters, zsum, status);
 }
 
 int launch_probs(int rows, int V, const float* logits, float temperature, float top_p,
                  float* probs, cudaStream_t s) {
-  probs_kernel<<<rows, kProbThreads, 0, s>>>(logits, V, 1.0f / temperature, top_p, probs);
-  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_LAUNCH;
+  return launch_pdl(probs_kernel, dim3(rows), dim3(kProbThreads), 0, s, logits, V, 1.0f / temperature,
+                    top_p, probs);
 }
 
 }  // namespace dfl

@@ -85,7 +85,7 @@ enum { DFLASH_VERIFY_GREEDY = 0, DFLASH_VERIFY_SAMPLED = 1 };
 
 /* Drafter dimensions.  Constraints checked by dflash_create: head_dim is 64
  * or 128; hidden, ffn, n_q_heads*head_dim and n_feat*feat_dim are multiples
- * of 64; n_q_heads is a multiple of n_kv_heads; 1 <= gamma_max <= 16;
+ * of 64; hidden <= 12288; n_q_heads is a multiple of n_kv_heads; 1 <= gamma_max <= 16;
  * 1 <= topk_max <= 16; window >= 1. */
 typedef struct dflash_config {
   int hidden;      /* d */
@@ -253,7 +253,8 @@ int dflash_verify(int mode, int B, int gamma, int vocab, const float* target, co
  * returns, for each launch of the last call, its duration in ms, its
  * algorithmic bytes (operands read + results written, each counted once) and
  * its kind (DFLASH_KIND_*); *count receives the number of launches (<= cap).
- * Not for use while a graph is being captured. */
+ * A draft_block call captured into a CUDA graph records the events as event
+ * nodes, so a replayed graph can be profiled too (read after the replay). */
 enum { DFLASH_KIND_GEMM = 0, DFLASH_KIND_ATTENTION = 1, DFLASH_KIND_NORM = 2,
        DFLASH_KIND_TOPK = 3, DFLASH_KIND_SAMPLING = 4 };
 int dflash_profile_enable(dflash_handle* h, int n_pairs);
