@@ -47,8 +47,6 @@ struct dflash_handle {
 
 namespace {
 
-constexpr size_t kGemmPartialFloats = 4u << 20;  // split-K partial tiles (16 MiB)
-constexpr int kGemmCounters = 8192;
 
 bool aligned(const void* p, size_t a) { return p && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -73,20 +71,20 @@ int validate_config(const dflash_config& c) {
   return DFLASH_OK;
 }
 
-// Key splits per (request, KV head): a power of two up to the portable
-// cluster size, enough to give every SM a CTA when there are few heads.
+// Key splits per (request, KV head): a power of two up to 16 (the attention
+// launcher caps it to the largest cluster the GPU can co-schedule), enough to
+// give every SM a CTA when there are few heads.
 int attn_splits(const dflash_handle* h, int B) {
   const int bh = B * h->cfg.n_kv_heads;
   const int tiles = (h->cfg.window + 63) / 64;
   const int want = (h->num_sms + bh - 1) / bh;
   int s = 1;
-  while (s * 2 <= want && s * 2 <= tiles && s * 2 <= 8) s *= 2;
+  while (s * 2 <= want && s * 2 <= tiles && s * 2 <= 16) s *= 2;
   return s;
 }
 
 struct DraftWs {
   int* status;
-  int* gemm_counters;
   int* topk_counters;
   int* samp_counters;
   float* x;
@@ -97,7 +95,6 @@ struct DraftWs {
   void* hf;
   void* q_lo;
   float* logits;
-  float* gemm_partial;
   unsigned long long* topk_keys;
   float* topk_ml;
   unsigned long long* samp_zsum;
@@ -114,7 +111,6 @@ DraftWs draft_layout(const dflash_handle* h, void* base) {
   Carve cv(base, kWsHeader);
   DraftWs w;
   w.status = static_cast<int*>(base);
-  w.gemm_counters = cv.take<int>(kGemmCounters);
   w.topk_counters = cv.take<int>(R);
   w.samp_counters = cv.take<int>(R);
   // bf16 GEMM operands are [2, rows, K]: bf16 values, then their bf16 remainders
@@ -126,7 +122,6 @@ DraftWs draft_layout(const dflash_handle* h, void* base) {
   w.hf = cv.take<uint16_t>(2 * R * c.hidden);
   w.q_lo = cv.take<uint16_t>(M * q_dim);
   w.logits = cv.take<float>(R * c.vocab);
-  w.gemm_partial = cv.take<float>(kGemmPartialFloats);
   w.topk_keys = cv.take<unsigned long long>(R * chunks * 16);
   w.topk_ml = cv.take<float>(R * chunks * 2);
   w.samp_zsum = cv.take<unsigned long long>(R * chunks);
@@ -136,10 +131,8 @@ DraftWs draft_layout(const dflash_handle* h, void* base) {
 
 struct AppendWs {
   int* status;
-  int* gemm_counters;
   float* fused;
   void* ht;
-  float* gemm_partial;
   size_t bytes;
 };
 
@@ -149,10 +142,8 @@ AppendWs append_layout(const dflash_handle* h, void* base) {
   Carve cv(base, kWsHeader);
   AppendWs w;
   w.status = static_cast<int*>(base);
-  w.gemm_counters = cv.take<int>(kGemmCounters);
   w.fused = cv.take<float>(M * c.hidden);
   w.ht = cv.take<uint16_t>(2 * M * c.hidden);
-  w.gemm_partial = cv.take<float>(kGemmPartialFloats);
   w.bytes = cv.off;
   return w;
 }
@@ -342,7 +333,7 @@ int dflash_ctx_append(dflash_handle* h, int B, int n_max, const void* feats, con
   AppendWs ws = append_layout(h, workspace);
   if (ws_bytes < ws.bytes) return DFLASH_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  GemmScratch scratch{ws.gemm_partial, kGemmPartialFloats, ws.gemm_counters, kGemmCounters, ws.status};
+  GemmScratch scratch{ws.status};
   const int M = B * n_max;
   const int d = c.hidden;
   const int Kc = c.n_feat * c.feat_dim;
@@ -426,7 +417,7 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
   if (ws_bytes < ws.bytes) return DFLASH_ERR_WORKSPACE;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  GemmScratch scratch{ws.gemm_partial, kGemmPartialFloats, ws.gemm_counters, kGemmCounters, ws.status};
+  GemmScratch scratch{ws.status};
   h->prof_used = 0;
   const int M = B * gamma;
   const int R = B * (gamma - 1);

@@ -100,21 +100,32 @@ __device__ __forceinline__ void process_tile(WarpState<HD>& st, uint32_t k_base,
 #pragma unroll
   for (int j = 0; j < NT_S; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.0f;
 
-  // S = Q K^T: pairs of 8-key n-tiles per ldmatrix.x4
+  // S = Q K^T.  For each 16-dim k-step the K fragments of all key n-tiles are
+  // loaded first, then every accumulator receives its hi-part MMA and only
+  // then its remainder MMA, so consecutive MMAs on one accumulator are NT_S
+  // instructions apart instead of back to back.
 #pragma unroll
-  for (int kp = 0; kp < NT_S / 2; ++kp) {
+  for (int kk = 0; kk < HD / 16; ++kk) {
+    uint32_t bk[NT_S / 2][4];
 #pragma unroll
-    for (int kk = 0; kk < HD / 16; ++kk) {
+    for (int kp = 0; kp < NT_S / 2; ++kp) {
       const int key = kp * 16 + (lane & 7) + ((lane >> 4) << 3);
       const int dim = kk * 16 + (((lane >> 3) & 1) << 3);
-      const uint32_t addr = k_base + (dim >> 6) * kHalf + swz(key, dim & 63);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(addr, b0, b1, b2, b3);
-      mma_bf16(s[2 * kp], st.qa[kk][0], st.qa[kk][1], st.qa[kk][2], st.qa[kk][3], b0, b1);
-      mma_bf16(s[2 * kp + 1], st.qa[kk][0], st.qa[kk][1], st.qa[kk][2], st.qa[kk][3], b2, b3);
-      if (QLO) {
-        mma_bf16(s[2 * kp], st.ql[kk][0], st.ql[kk][1], st.ql[kk][2], st.ql[kk][3], b0, b1);
-        mma_bf16(s[2 * kp + 1], st.ql[kk][0], st.ql[kk][1], st.ql[kk][2], st.ql[kk][3], b2, b3);
+      ldsm_x4(k_base + (dim >> 6) * kHalf + swz(key, dim & 63), bk[kp][0], bk[kp][1], bk[kp][2],
+              bk[kp][3]);
+    }
+#pragma unroll
+    for (int kp = 0; kp < NT_S / 2; ++kp) {
+      mma_bf16(s[2 * kp], st.qa[kk][0], st.qa[kk][1], st.qa[kk][2], st.qa[kk][3], bk[kp][0], bk[kp][1]);
+      mma_bf16(s[2 * kp + 1], st.qa[kk][0], st.qa[kk][1], st.qa[kk][2], st.qa[kk][3], bk[kp][2],
+               bk[kp][3]);
+    }
+    if (QLO) {
+#pragma unroll
+      for (int kp = 0; kp < NT_S / 2; ++kp) {
+        mma_bf16(s[2 * kp], st.ql[kk][0], st.ql[kk][1], st.ql[kk][2], st.ql[kk][3], bk[kp][0], bk[kp][1]);
+        mma_bf16(s[2 * kp + 1], st.ql[kk][0], st.ql[kk][1], st.ql[kk][2], st.ql[kk][3], bk[kp][2],
+                 bk[kp][3]);
       }
     }
   }
@@ -451,21 +462,48 @@ int launch_t(const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a, in
       return DFLASH_ERR_LAUNCH;
     attr = true;
   }
+  // Largest power-of-two cluster (<= 16, the non-portable maximum) that the GPU
+  // can co-schedule for this kernel; the key splits are capped to it.
+  static int max_cluster = 0;
+  if (max_cluster == 0) {
+    max_cluster = 1;
+    for (int c = 16; c >= 2; c >>= 1) {
+      cudaLaunchConfig_t q = {};
+      q.gridDim = dim3(c, 1, 1);
+      q.blockDim = dim3((MT + 1) * 32);
+      q.dynamicSmemBytes = smem;
+      cudaLaunchAttribute qa[1];
+      qa[0].id = cudaLaunchAttributeClusterDimension;
+      qa[0].val.clusterDim.x = c;
+      qa[0].val.clusterDim.y = 1;
+      qa[0].val.clusterDim.z = 1;
+      q.attrs = qa;
+      q.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &q) == cudaSuccess && n > 0) {
+        max_cluster = c;
+        break;
+      }
+      (void)cudaGetLastError();
+    }
+  }
+  AttnArgs aa = a;
+  while (aa.splits > max_cluster) aa.splits >>= 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.splits, a.n_kv, B);
+  cfg.gridDim = dim3(aa.splits, aa.n_kv, B);
   cfg.blockDim = dim3((MT + 1) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr_c[2];
   attr_c[0].id = cudaLaunchAttributeClusterDimension;
-  attr_c[0].val.clusterDim.x = a.splits;
+  attr_c[0].val.clusterDim.x = aa.splits;
   attr_c[0].val.clusterDim.y = 1;
   attr_c[0].val.clusterDim.z = 1;
   attr_c[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr_c[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr_c;
   cfg.numAttrs = 2;
-  if (cudaLaunchKernelEx(&cfg, kern, tk, tv, a) != cudaSuccess) return DFLASH_ERR_LAUNCH;
+  if (cudaLaunchKernelEx(&cfg, kern, tk, tv, aa) != cudaSuccess) return DFLASH_ERR_LAUNCH;
   return DFLASH_OK;
 }
 

@@ -18,8 +18,8 @@ struct AttnArgs {
   const int64_t* ctx_len;    // [B] context lengths L
   const int32_t* req_slot;   // [B] ring rows or nullptr
   int gamma, n_q, n_kv, hd, window, ring_batch;
-  int splits;                // key-range splits per (request, KV head): 1, 2, 4 or 8; the
-                             // splits of one head run as a thread-block cluster
+  int splits;                // key-range splits per (request, KV head): a power of two <= 16;
+                             // the splits of one head run as a thread-block cluster
   float scale_log2;          // log2(e) / sqrt(hd)
   int* status;
 };

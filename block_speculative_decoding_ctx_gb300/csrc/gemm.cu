@@ -16,10 +16,13 @@
 //   all 4 warps     epilogue: tcgen05.ld of their 32-lane quarter, then the
 //                   fused epilogue of the layer (RoPE, residual add, SwiGLU,
 //                   fp32 logits, or scatter into the context ring).
-// Split-K: the grid's z dimension partitions K; each split stores its fp32
-// partial tile, and the last split to arrive (atomic ticket after a fence)
-// sums the partials in split order — deterministic — and runs the epilogue.
+// Split-K: the grid's z dimension partitions K and the splits of one tile run
+// as a thread-block cluster; each split keeps its fp32 partial tile in shared
+// memory and, after a cluster barrier, every CTA of the cluster sums a
+// disjoint subset of the tile's tokens over distributed shared memory (in
+// split order — deterministic) and runs the epilogue on it.
 // All waits are bounded (see mbar_wait_bounded).
+#include <cooperative_groups.h>
 #include <cudaTypedefs.h>
 
 #include <cmath>
@@ -31,9 +34,12 @@
 namespace dfl {
 namespace {
 
+namespace cg = cooperative_groups;
+
 constexpr int kThreads = 128;
 constexpr int kBK = 64;                   // K elements per stage (128 bytes of bf16)
 constexpr int kABytes = 128 * kBK * 2;    // weight box per stage
+constexpr int kMaxClusterSplits = 8;      // K splits of a tile = one portable cluster
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
 
@@ -79,12 +85,13 @@ __device__ __forceinline__ void store_bf16_pair(const GemmEpi& e, size_t o_hi, s
     static_cast<__nv_bfloat16*>(e.out_lo)[o_lo] = __float2bfloat16_rn(y - __bfloat162float(hi));
 }
 
-// Epilogue of up to 16 consecutive tokens (the first `ntok` of v are real)
-// of this thread's row.  `xchg` holds the chunk as [16][128] floats so that
-// partner rows can be read.  Every thread of the CTA calls it (it
-// synchronises).
+// Epilogue of up to 16 tokens of this thread's row: v[j] is token
+// tok_base + j * tok_step, the first `ntok` are real.  `xchg` holds the
+// chunk as [16][128] floats so that partner rows can be read.  Every thread
+// of the CTA calls it (it synchronises).
 __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const float (&v)[16],
-                               int tok_base, int ntok, int tile_n, int r, float* xchg) {
+                               int tok_base, int tok_step, int ntok, int tile_n, int r,
+                               float* xchg) {
   const int kind = e.kind;
   const bool needs_xchg = (kind == EPI_QKV || kind == EPI_SWIGLU || kind == EPI_KV_RING);
   if (needs_xchg) {
@@ -97,7 +104,7 @@ __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const floa
     if (n < e.N) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        const int tok = tok_base + j;
+        const int tok = tok_base + j * tok_step;
         if (j < ntok && tok < e.M) {
           const size_t o = (size_t)tok * e.ld + n;
           if (kind == EPI_F32)
@@ -118,7 +125,7 @@ __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const floa
       const int pr = r ^ (e.hd >> 1);
 #pragma unroll 4
       for (int j = 0; j < 16; ++j) {
-        const int tok = tok_base + j;
+        const int tok = tok_base + j * tok_step;
         if (j < ntok && tok < e.M) {
           float y = v[j];
           if (rot) {
@@ -138,7 +145,7 @@ __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const floa
     if (r < 64 && f < e.N) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        const int tok = tok_base + j;
+        const int tok = tok_base + j * tok_step;
         if (j < ntok && tok < e.M) {
           const float g = v[j], u = xchg[j * 128 + r + 64];
           store_bf16_pair(e, (size_t)tok * e.ld + f, (size_t)tok * e.ld_lo + f, silu(g) * u);
@@ -156,7 +163,7 @@ __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const floa
     __nv_bfloat16* ring = static_cast<__nv_bfloat16*>(kv ? e.ring_v : e.ring_k);
 #pragma unroll 4
     for (int j = 0; j < 16; ++j) {
-      const int tok = tok_base + j;
+      const int tok = tok_base + j * tok_step;
       if (j < ntok && tok < e.M) {
         const int b = tok / e.n_max, jr = tok % e.n_max;
         if (jr < e.n_new[b]) {
@@ -187,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kStage = kABytes + kBBytes;
   constexpr uint32_t kTmemCols = BN < 32 ? 32 : BN;
   static_assert(kStage % 1024 == 0, "stage buffers must keep 1024-byte alignment");
+  static_assert((BN + 16) * 128 * 4 <= STAGES * kStage, "split partials must fit the stage buffers");
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
@@ -346,44 +354,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
 
-  if (!aborted) {
-    if (args.splits == 1) {
+  if (args.splits == 1) {
+    if (!aborted) {
       for (int c = 0; c < n_chunks; ++c) {
         float v[16];
         load_chunk(c, v);
-        epilogue_chunk(epi, ao, v, tile_m * T + c * 16, ntok, tile_n, r, xchg);
-      }
-    } else {
-      const int tile_lin = tile_m * gridDim.x + tile_n;
-      const size_t per_split = (size_t)n_chunks * 16 * 128;
-      float* part = args.partial + (size_t)tile_lin * args.splits * per_split;
-      float* mine = part + (size_t)split * per_split;
-      for (int c = 0; c < n_chunks; ++c) {
-        float v[16];
-        load_chunk(c, v);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) mine[(c * 16 + j) * 128 + r] = v[j];
-      }
-      __threadfence();
-      __syncthreads();
-      if (threadIdx.x == 0) last_sh = (atomicAdd(&args.counters[tile_lin], 1) == args.splits - 1);
-      __syncthreads();
-      if (last_sh) {
-        __threadfence();
-        for (int c = 0; c < n_chunks; ++c) {
-          float v[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = 0.0f;
-          for (int s = 0; s < args.splits; ++s) {
-            const float* ps = part + (size_t)s * per_split;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] += __ldcg(ps + (c * 16 + j) * 128 + r);
-          }
-          epilogue_chunk(epi, ao, v, tile_m * T + c * 16, ntok, tile_n, r, xchg);
-        }
-        if (threadIdx.x == 0) atomicExch(&args.counters[tile_lin], 0);
+        epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg);
       }
     }
+  } else {
+    // The K splits of this tile form a thread-block cluster.  Each leaves its
+    // fp32 partial [T tokens][128 rows] in its own shared memory (the stage
+    // buffers are free: every stage has been consumed); after a cluster
+    // barrier CTA `rank` sums, over distributed shared memory and in split
+    // order, the tokens rank, rank + S, ... of the tile and runs the epilogue
+    // on them.  A CTA whose wait gave up still takes part in both cluster
+    // barriers (its siblings would otherwise wait for it) but writes nothing.
+    float* part_s = reinterpret_cast<float*>(smem);
+    float* xchg_s = part_s + (size_t)n_chunks * 16 * 128;
+    for (int c = 0; c < n_chunks; ++c) {
+      float v[16];
+      if (!aborted) {
+        load_chunk(c, v);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) part_s[(c * 16 + j) * 128 + r] = v[j];
+    }
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    if (!aborted) {
+      const int S = args.splits;
+      const int rank = split;  // cluster dims (1, 1, S): rank = blockIdx.z
+      const int mine = (T - rank + S - 1) / S;
+      for (int g0 = 0; g0 < mine; g0 += 16) {
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+        for (int s = 0; s < S; ++s) {
+          const float* ps = cluster.map_shared_rank(part_s, s);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int t = rank + (g0 + j) * S;
+            if (g0 + j < mine) v[j] += ps[t * 128 + r];
+          }
+        }
+        const int cnt = mine - g0 < 16 ? mine - g0 : 16;
+        epilogue_chunk(epi, ao, v, tile_m * T + rank + g0 * S, S, cnt, tile_n, r, xchg_s);
+      }
+    }
+    // no CTA may leave while another still reads its shared memory
+    cluster.sync();
   }
   tc_fence_before();
   __syncthreads();
@@ -417,11 +440,22 @@ int launch_one(const GemmAMaps& A, const CUtensorMap& tmB, const GemmAOpts& ao, 
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (args.splits > 1) {  // the K splits of a tile run as one cluster
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = args.splits;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = na;
   if (cudaLaunchKernelEx(&cfg, kern, A, tmB, ao, args, epi) != cudaSuccess) return DFLASH_ERR_LAUNCH;
   return DFLASH_OK;
 }
@@ -481,17 +515,10 @@ int launch_gemm(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void
   const int kb = (K + kBK - 1) / kBK;
   if (splits < 1) splits = 1;
   if (splits > kb) splits = kb;
-  const size_t tiles = (size_t)n_tiles * m_tiles;
-  const size_t per_split = (size_t)((T + 15) / 16) * 16 * 128;
-  if (splits > 1) {
-    if (tiles > (size_t)scratch.counters_cap) splits = 1;
-    while (splits > 1 && tiles * splits * per_split > scratch.partial_cap_floats) --splits;
-  }
+  if (splits > kMaxClusterSplits) splits = kMaxClusterSplits;
   GemmArgs args;
   args.K = K;
   args.splits = splits;
-  args.partial = scratch.partial;
-  args.counters = scratch.counters;
   args.status = scratch.status;
   dim3 grid(n_tiles, m_tiles, splits);
   switch (BN) {

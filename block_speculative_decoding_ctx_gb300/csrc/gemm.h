@@ -37,9 +37,7 @@ struct GemmAOpts {
 
 struct GemmArgs {
   int K;
-  int splits;
-  float* partial;   // [tiles][splits][BN][128]
-  int* counters;    // [tiles], zero between launches
+  int splits;       // K splits per tile (<= 8); the splits of a tile form a cluster
   int* status;
 };
 
@@ -74,11 +72,7 @@ struct GemmEpi {
 };
 
 struct GemmScratch {
-  float* partial;
-  size_t partial_cap_floats;
-  int* counters;
-  int counters_cap;
-  int* status;
+  int* status;      // device status word
 };
 
 // TMA descriptor of a row-major bf16 matrix [outer, inner] with a
