@@ -44,6 +44,9 @@ def _stale(src, obj, hdr_mtime):
 
 
 def build(verbose=False, extra_flags=()):
+    """Compile what is stale and link.  DFLASH_NVCC_FLAGS (environment) adds
+    compile flags, e.g. -D defaults of the launch heuristics."""
+    extra_flags = tuple(extra_flags) + tuple(os.environ.get("DFLASH_NVCC_FLAGS", "").split())
     os.makedirs(BUILD, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     hdr_mtime = max([os.path.getmtime(h) for h in _headers()] + [0.0])

@@ -31,6 +31,11 @@ namespace {
 
 namespace cg = cooperative_groups;
 
+// Largest thread-block cluster (key splits of one head) attention will use.
+#ifndef DFLASH_ATTN_MAX_CLUSTER
+#define DFLASH_ATTN_MAX_CLUSTER 16
+#endif
+
 constexpr int kKeys = 64;      // keys per context tile
 constexpr int kStages = 3;
 
@@ -467,7 +472,7 @@ int launch_t(const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a, in
   static int max_cluster = 0;
   if (max_cluster == 0) {
     max_cluster = 1;
-    for (int c = 16; c >= 2; c >>= 1) {
+    for (int c = DFLASH_ATTN_MAX_CLUSTER; c >= 2; c >>= 1) {
       cudaLaunchConfig_t q = {};
       q.gridDim = dim3(c, 1, 1);
       q.blockDim = dim3((MT + 1) * 32);

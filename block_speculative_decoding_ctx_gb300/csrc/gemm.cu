@@ -39,7 +39,6 @@ namespace cg = cooperative_groups;
 constexpr int kThreads = 128;
 constexpr int kBK = 64;                   // K elements per stage (128 bytes of bf16)
 constexpr int kABytes = 128 * kBK * 2;    // weight box per stage
-constexpr int kMaxClusterSplits = 8;      // K splits of a tile = one portable cluster
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
 
@@ -362,6 +361,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg);
       }
     }
+  } else if (!args.cluster) {
+    // Ticketed reduction: every split stores its fp32 partial [T][128] in
+    // global memory; the last split of the tile to arrive (atomic ticket after
+    // a fence) sums them in split order and runs the epilogue.
+    const int tile_lin = tile_m * gridDim.x + tile_n;
+    const size_t per_split = (size_t)n_chunks * 16 * 128;
+    float* part = args.partial + (size_t)tile_lin * args.splits * per_split;
+    float* mine = part + (size_t)split * per_split;
+    if (!aborted) {
+      for (int c = 0; c < n_chunks; ++c) {
+        float v[16];
+        load_chunk(c, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) mine[(c * 16 + j) * 128 + r] = v[j];
+      }
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last_sh = (atomicAdd(&args.counters[tile_lin], 1) == args.splits - 1);
+    __syncthreads();
+    if (last_sh) {
+      __threadfence();
+      if (!aborted) {
+        for (int c = 0; c < n_chunks; ++c) {
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+          for (int s = 0; s < args.splits; ++s) {
+            const float* ps = part + (size_t)s * per_split;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] += __ldcg(ps + (c * 16 + j) * 128 + r);
+          }
+          epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg);
+        }
+      }
+      if (threadIdx.x == 0) atomicExch(&args.counters[tile_lin], 0);
+    }
   } else {
     // The K splits of this tile form a thread-block cluster.  Each leaves its
     // fp32 partial [T tokens][128 rows] in its own shared memory (the stage
@@ -447,7 +483,7 @@ int launch_one(const GemmAMaps& A, const CUtensorMap& tmB, const GemmAOpts& ao, 
     attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
   }
-  if (args.splits > 1) {  // the K splits of a tile run as one cluster
+  if (args.splits > 1 && args.cluster) {  // the K splits of a tile run as one cluster
     attr[na].id = cudaLaunchAttributeClusterDimension;
     attr[na].val.clusterDim.x = 1;
     attr[na].val.clusterDim.y = 1;
@@ -515,10 +551,19 @@ int launch_gemm(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void
   const int kb = (K + kBK - 1) / kBK;
   if (splits < 1) splits = 1;
   if (splits > kb) splits = kb;
-  if (splits > kMaxClusterSplits) splits = kMaxClusterSplits;
+  const size_t tiles = (size_t)n_tiles * m_tiles;
+  const size_t per_split = (size_t)((T + 15) / 16) * 16 * 128;
+  const bool cluster = splits > 1 && splits <= DFLASH_SPLITK_CLUSTER_MAX;
+  if (splits > 1 && !cluster) {
+    if (tiles > (size_t)scratch.counters_cap || !scratch.partial) splits = 1;
+    while (splits > 1 && tiles * splits * per_split > scratch.partial_cap_floats) --splits;
+  }
   GemmArgs args;
   args.K = K;
   args.splits = splits;
+  args.cluster = cluster ? 1 : 0;
+  args.partial = scratch.partial;
+  args.counters = scratch.counters;
   args.status = scratch.status;
   dim3 grid(n_tiles, m_tiles, splits);
   switch (BN) {

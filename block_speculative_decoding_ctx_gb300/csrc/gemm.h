@@ -37,7 +37,13 @@ struct GemmAOpts {
 
 struct GemmArgs {
   int K;
-  int splits;       // K splits per tile (<= 8); the splits of a tile form a cluster
+  int splits;       // K splits per tile
+  int cluster;      // 1: the splits of a tile form a cluster and reduce through
+                    //    distributed shared memory (splits <= 8)
+                    // 0: each split stores an fp32 partial in global memory and the
+                    //    last split of the tile (atomic ticket) reduces them
+  float* partial;   // [tiles][splits][T][128] when cluster == 0
+  int* counters;    // [tiles] when cluster == 0, zero between launches
   int* status;
 };
 
@@ -72,8 +78,18 @@ struct GemmEpi {
 };
 
 struct GemmScratch {
+  float* partial;   // split-K partial tiles of the ticketed reduction
+  size_t partial_cap_floats;
+  int* counters;    // tickets, zero between launches
+  int counters_cap;
   int* status;      // device status word
 };
+
+// Largest K-split count reduced through a cluster; above it the ticketed
+// reduction through global memory is used.
+#ifndef DFLASH_SPLITK_CLUSTER_MAX
+#define DFLASH_SPLITK_CLUSTER_MAX 8
+#endif
 
 // TMA descriptor of a row-major bf16 matrix [outer, inner] with a
 // (box_outer x box_inner) box and the 128-byte swizzle.
