@@ -347,7 +347,8 @@ int dflash_ctx_append(dflash_handle* h, int B, int n_max, const void* feats, con
   AppendWs ws = append_layout(h, workspace);
   if (ws_bytes < ws.bytes) return DFLASH_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  GemmScratch scratch{ws.gemm_partial, kGemmPartialFloats, ws.gemm_counters, kGemmCounters, ws.status};
+  GemmScratch scratch{ws.gemm_partial, kGemmPartialFloats, ws.gemm_counters, kGemmCounters, ws.status,
+                      h->num_sms};
   const int M = B * n_max;
   const int d = c.hidden;
   const int Kc = c.n_feat * c.feat_dim;
@@ -431,7 +432,8 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
   if (ws_bytes < ws.bytes) return DFLASH_ERR_WORKSPACE;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  GemmScratch scratch{ws.gemm_partial, kGemmPartialFloats, ws.gemm_counters, kGemmCounters, ws.status};
+  GemmScratch scratch{ws.gemm_partial, kGemmPartialFloats, ws.gemm_counters, kGemmCounters, ws.status,
+                      h->num_sms};
   h->prof_used = 0;
   const int M = B * gamma;
   const int R = B * (gamma - 1);

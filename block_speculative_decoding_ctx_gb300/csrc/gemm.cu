@@ -87,7 +87,15 @@ __device__ __forceinline__ void store_bf16_pair(const GemmEpi& e, size_t o_hi, s
 // Epilogue of up to 16 tokens of this thread's row: v[j] is token
 // tok_base + j * tok_step, the first `ntok` are real.  `xchg` holds the
 // chunk as [16][128] floats so that partner rows can be read.  Every thread
-// of the CTA calls it (it synchronises).
+// of the CTA (kNamed: of the four epilogue warps) calls it: it synchronises.
+__device__ __forceinline__ void epi_sync(bool named) {
+  if (named)
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+  else
+    __syncthreads();
+}
+
+template <bool kNamed = false>
 __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const float (&v)[16],
                                int tok_base, int tok_step, int ntok, int tile_n, int r,
                                float* xchg) {
@@ -96,7 +104,7 @@ __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const floa
   if (needs_xchg) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) xchg[j * 128 + r] = v[j];
-    __syncthreads();
+    epi_sync(kNamed);
   }
   if (kind == EPI_F32 || kind == EPI_BF16 || kind == EPI_RESID) {
     const int n = tile_n * 128 + r;
@@ -182,7 +190,7 @@ __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const floa
       }
     }
   }
-  if (needs_xchg) __syncthreads();
+  if (needs_xchg) epi_sync(kNamed);
 }
 
 template <int BN, int STAGES>
@@ -449,6 +457,184 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+// Persistent, warp-specialised variant for many token columns (no split-K):
+// one CTA per SM walks the tiles t = blockIdx.x, blockIdx.x + gridDim.x, ...
+// (token tiles fastest, so CTAs running at the same time share weight tiles in
+// L2).  Warp 0 lane 0 issues TMA, warp 1 lane 0 issues MMAs, warps 2-5 run
+// the epilogue.  Two TMEM accumulators let the epilogue of one tile overlap
+// the mainloop of the next.
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    gemm_bf16_tc_persistent_kernel(const __grid_constant__ GemmAMaps A,
+                                   const __grid_constant__ CUtensorMap tmB, const GemmAOpts ao,
+                                   const GemmArgs args, const GemmEpi epi, int n_tiles, int m_tiles) {
+  constexpr int kBBytes = BN * kBK * 2;
+  constexpr int kStage = kABytes + kBBytes;
+  constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
+  static_assert(kStage % 1024 == 0, "stage buffers must keep 1024-byte alignment");
+  static_assert(kTmemCols <= 512, "two accumulators must fit tensor memory");
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t accf_bar[2];
+  __shared__ __align__(8) uint64_t acce_bar[2];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* xchg = reinterpret_cast<float*>(smem + STAGES * kStage);
+  const int T = ao.split ? BN / 2 : BN;
+  const int kb_total = (args.K + kBK - 1) / kBK;
+  const int total = n_tiles * m_tiles;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf_bar[b], 1);
+      mbar_init(&acce_bar[b], 4);
+    }
+    abort_sh = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < ao.n_maps; ++i) tma_prefetch_desc(&A.map[i]);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  grid_dependents_launch();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      bool waited = false;
+      int it = 0;
+      for (int t = blockIdx.x; t < total && !abort_sh; t += gridDim.x) {
+        const int tile_m = t % m_tiles, tile_n = t / m_tiles;
+        int map_i = 0, row0;
+        if (ao.dual) {
+          row0 = ao.row_offset + tile_n * 64;
+        } else {
+          map_i = tile_n / ao.tiles_per_map;
+          row0 = ao.row_offset + (tile_n % ao.tiles_per_map) * 128;
+        }
+        const int tok0 = tile_m * T;
+        for (int kb = 0; kb < kb_total; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1u, &abort_sh, args.status)) break;
+          uint8_t* sa = smem + s * kStage;
+          mbar_arrive_expect_tx(&full_bar[s], kStage);
+          const int kc = kb * kBK;
+          if (ao.dual) {
+            tma_load_2d(sa, &A.map[0], &full_bar[s], kc, row0, pol_w);
+            tma_load_2d(sa + 64 * 128, &A.map[1], &full_bar[s], kc, row0, pol_w);
+          } else {
+            tma_load_2d(sa, &A.map[map_i], &full_bar[s], kc, row0, pol_w);
+          }
+          if (!waited) {  // activations come from the previous kernel
+            grid_dependency_wait();
+            waited = true;
+          }
+          tma_load_2d(sa + kABytes, &tmB, &full_bar[s], kc, tok0, pol_x);
+          if (ao.split) tma_load_2d(sa + kABytes + T * 128, &tmB, &full_bar[s], kc, epi.M + tok0, pol_x);
+        }
+      }
+      if (abort_sh) {
+        int dummy = 0;
+        for (int i = (it > STAGES ? it - STAGES : 0); i < it; ++i)
+          (void)mbar_wait_bounded(&full_bar[i % STAGES], (uint32_t)(i / STAGES) & 1u, &dummy, nullptr,
+                                  100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
+      int it = 0, lt = 0;
+      for (int t = blockIdx.x; t < total && !abort_sh; t += gridDim.x, ++lt) {
+        const int buf = lt & 1;
+        const uint32_t use = (uint32_t)(lt >> 1);
+        if (!mbar_wait_bounded(&acce_bar[buf], (use & 1u) ^ 1u, &abort_sh, args.status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * BN);
+        for (int kb = 0; kb < kb_total; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          if (!mbar_wait_bounded(&full_bar[s], ph, &abort_sh, args.status)) break;
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + s * kStage);
+          const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            tc_mma_bf16(d, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), idesc,
+                        (kb | k) ? 1u : 0u);
+          tc_commit(&empty_bar[s]);
+        }
+        tc_commit(&accf_bar[buf]);
+      }
+    }
+  } else {
+    // --------------------------------------------------------- epilogue
+    const int r = 32 * (warp & 3) + lane;  // TMEM lane quarter of this warp
+    const uint32_t t_row = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const int ntok = T < 16 ? T : 16;
+    const int n_chunks = (T + 15) / 16;
+    int lt = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
+      const int tile_m = t % m_tiles, tile_n = t / m_tiles;
+      const int buf = lt & 1;
+      const uint32_t use = (uint32_t)(lt >> 1);
+      const bool ok = mbar_wait_bounded(&accf_bar[buf], use & 1u, &abort_sh, args.status);
+      // the four epilogue warps agree before acting on the outcome
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (!ok || abort_sh) break;
+      tc_fence_after();
+      const uint32_t base = t_row + (uint32_t)(buf * BN);
+      for (int c = 0; c < n_chunks; ++c) {
+        float v[16];
+        uint32_t raw[16];
+        if (!ao.split) {
+          tmem_ld_x16(base + c * 16, raw);
+          tc_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]);
+        } else {
+          uint32_t lo[16];
+          tmem_ld_x16(base + c * 16, raw);
+          tmem_ld_x16(base + T + c * 16, lo);
+          tc_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]) + __uint_as_float(lo[j]);
+        }
+        if (c == n_chunks - 1) {
+          // every column of this accumulator is in registers: hand it back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acce_bar[buf]);
+        }
+        epilogue_chunk<true>(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
 // ------------------------------------------------------------------ host
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -493,6 +679,37 @@ int launch_one(const GemmAMaps& A, const CUtensorMap& tmB, const GemmAOpts& ao, 
   cfg.attrs = attr;
   cfg.numAttrs = na;
   if (cudaLaunchKernelEx(&cfg, kern, A, tmB, ao, args, epi) != cudaSuccess) return DFLASH_ERR_LAUNCH;
+  return DFLASH_OK;
+}
+
+
+
+template <int BN, int STAGES>
+int launch_persistent(const GemmAMaps& A, const CUtensorMap& tmB, const GemmAOpts& ao,
+                      const GemmArgs& args, const GemmEpi& epi, int n_tiles, int m_tiles,
+                      int num_sms, cudaStream_t s, bool pdl) {
+  auto kern = gemm_bf16_tc_persistent_kernel<BN, STAGES>;
+  constexpr size_t smem = (size_t)STAGES * (kABytes + BN * kBK * 2) + 16 * 128 * 4 + 1024;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return DFLASH_ERR_LAUNCH;
+    attr_set = true;
+  }
+  const int total = n_tiles * m_tiles;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(total < num_sms ? total : num_sms);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, kern, A, tmB, ao, args, epi, n_tiles, m_tiles) != cudaSuccess)
+    return DFLASH_ERR_LAUNCH;
   return DFLASH_OK;
 }
 
@@ -553,7 +770,11 @@ int launch_gemm(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void
   if (splits > kb) splits = kb;
   const size_t tiles = (size_t)n_tiles * m_tiles;
   const size_t per_split = (size_t)((T + 15) / 16) * 16 * 128;
-  const bool cluster = splits > 1 && splits <= DFLASH_SPLITK_CLUSTER_MAX;
+  // Measured on GB300: with small token tiles (8-16 tokens, partials of
+  // 4-8 KiB) the ticketed reduction wins — non-last splits leave at once;
+  // with 32+ token tiles the partials are large and the cluster reduction
+  // through distributed shared memory wins.
+  const bool cluster = splits > 1 && splits <= DFLASH_SPLITK_CLUSTER_MAX && T >= 32;
   if (splits > 1 && !cluster) {
     if (tiles > (size_t)scratch.counters_cap || !scratch.partial) splits = 1;
     while (splits > 1 && tiles * splits * per_split > scratch.partial_cap_floats) --splits;
@@ -565,6 +786,11 @@ int launch_gemm(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void
   args.partial = scratch.partial;
   args.counters = scratch.counters;
   args.status = scratch.status;
+  // many token columns and no split-K: the persistent kernel
+  if (splits == 1 && T >= 64 && (size_t)n_tiles * m_tiles >= (size_t)scratch.num_sms) {
+    if (BN == 256) return launch_persistent<256, 4>(A, tmB, ao, args, epi, n_tiles, m_tiles, scratch.num_sms, s, pdl);
+    if (BN == 128) return launch_persistent<128, 6>(A, tmB, ao, args, epi, n_tiles, m_tiles, scratch.num_sms, s, pdl);
+  }
   dim3 grid(n_tiles, m_tiles, splits);
   switch (BN) {
     case 16: return launch_one<16, 6>(A, tmB, ao, args, epi, grid, s, pdl);

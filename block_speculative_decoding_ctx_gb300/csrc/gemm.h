@@ -83,6 +83,7 @@ struct GemmScratch {
   int* counters;    // tickets, zero between launches
   int counters_cap;
   int* status;      // device status word
+  int num_sms;      // persistent kernels launch one CTA per SM
 };
 
 // Largest K-split count reduced through a cluster; above it the ticketed
