@@ -267,7 +267,7 @@ def run_ours(args, rank, ws):
     dims = dict(DIMS_FULL, n_layers=args.layers)
     B, G = args.batch, args.gamma
     W = gpu_weights(dims, 1234, dev)
-    h = dfl.dflash_create(lib_cfg(dims, max(B, 1), G, dims["window"]), W)
+    h = dfl.dflash_create(lib_cfg(dims, max(B, 1), G, max(min(args.context, dims["window"]), G)), W)
     cyc = Cycle(dfl, h, dims, B, G, args.context, args.sigma, dev, 99 + rank)
     stream = torch.cuda.Stream(device=dev)
     if args.profile_cycles:
@@ -449,10 +449,20 @@ def run_extras(args, dfl, dims, W, dev, stream):
         flops += 2.0 * B * (G - 1) * d * V
         gemm_tflops = flops / (gemm_ms * 1e-3) / 1e12
         key = f"batch{B}_gamma{G}"
+        M_ = B * G
+        qd_ = dims["n_q"] * dims["hd"]
+        fl = [2.0 * M_ * d * qkv, 2.0 * M_ * d * qd_, 2.0 * M_ * d * 2 * F, 2.0 * M_ * F * d]
+        gl = [p for p in prof if p[2] == "gemm"][:4]
+        layer0 = [[n, round(p[0] * 1e3, 1), round(f / (p[0] * 1e-3) / 1e12, 1)]
+                  for n, p, f in zip(("qkv", "o", "gate_up", "down"), gl, fl)]
+        head = [p for p in prof if p[2] == "gemm"][-1]
+        layer0.append(["lm_head", round(head[0] * 1e3, 1),
+                       round(2.0 * B * (G - 1) * d * V / (head[0] * 1e-3) / 1e12, 1)])
         out[key] = {"draft_blocks_per_s": round(B * 1000.0 / t, 2), "ms_per_pass": round(t, 4),
                     "gemm_ms": round(gemm_ms, 4), "attention_ms": round(attn_ms, 4),
                     "gemm_tflops": round(gemm_tflops, 1),
                     "gemm_frac_of_bf16_peak": round(gemm_tflops / tf_sus, 4),
+                    "first_layer_gemms_us_tflops": layer0,
                     "peak_tflops_sustained": tf_sus, "peak_source": src}
         del h, rk, rv, ws, g
         torch.cuda.empty_cache()

@@ -34,6 +34,10 @@ DIMS = {
     # head dim 128 like the full model, ragged vocabulary
     "small128": dict(d=1280, n_q=10, n_kv=2, hd=128, ffn=2560, vocab=3001, n_layers=1,
                      n_feat=5, feat_dim=640, window=512),
+    # enough weight tiles (SwiGLU 9728 = 152 x 64, vocabulary 20000) that batches
+    # of 16-32 blocks take the persistent GEMM path
+    "wide": dict(d=640, n_q=10, n_kv=2, hd=64, ffn=9728, vocab=20000, n_layers=1,
+                 n_feat=5, feat_dim=384, window=256),
 }
 
 

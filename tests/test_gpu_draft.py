@@ -32,6 +32,9 @@ CASES = [
     ("small", 3, 8, [300, 256, 17]),
     ("small128", 2, 16, [512, 700]),
     ("small128", 4, 8, [100, 513, 1, 2000]),
+    ("wide", 16, 8, [256] * 8 + [10, 300, 40, 999, 257, 255, 1, 0]),
+    ("wide", 32, 8, [300] * 32),
+    ("wide", 20, 16, [180] * 20),
 ]
 
 
