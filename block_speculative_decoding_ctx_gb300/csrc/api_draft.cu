@@ -195,6 +195,16 @@ GemmEpi epi_base(int kind, int M, int N, void* out, long long ld) {
   return e;
 }
 
+// inv_freq_j = theta^(-2j/hd) in double, kept as a float pair for the kernels.
+void set_rope_table(GemmEpi& e, const dflash_config& c) {
+  const int half = c.head_dim / 2;
+  for (int j = 0; j < 64; ++j) {
+    const double inv = j < half ? std::pow((double)c.rope_theta, -2.0 * j / c.head_dim) : 0.0;
+    const float hi = (float)inv;
+    e.rope_inv[j] = make_float2(hi, (float)(inv - (double)hi));
+  }
+}
+
 int splits_for(const dflash_handle* h, int n_tiles, int M, int K, int split) {
   const int BN = gemm_token_tile(split ? 2 * M : M);
   const int T = split ? BN / 2 : BN;
@@ -381,7 +391,7 @@ int dflash_ctx_append(dflash_handle* h, int B, int n_max, const void* feats, con
     ao.split = 1;
     GemmEpi e = epi_base(EPI_KV_RING, M, nl * 2 * kvd, nullptr, 0);
     e.ctx_len = ctx_len;
-    e.rope_theta = c.rope_theta;
+    set_rope_table(e, c);
     e.hd = c.head_dim;
     e.ring_k = ring_k;
     e.ring_v = ring_v;
@@ -486,7 +496,7 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
       GemmEpi e = epi_base(EPI_QKV, M, qkv_dim, ws.qkv, qkv_dim);
       e.ctx_len = ctx_len;
       e.gamma = gamma;
-      e.rope_theta = c.rope_theta;
+      set_rope_table(e, c);
       e.rope_rows = (c.n_q_heads + c.n_kv_heads) * hd;
       e.hd = hd;
       e.out_lo = ws.q_lo;

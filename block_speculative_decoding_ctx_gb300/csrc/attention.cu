@@ -82,6 +82,16 @@ __device__ __forceinline__ void store_pair2(__nv_bfloat16* hi, __nv_bfloat16* lo
         __floats2bfloat162_rn(y0 - __low2float(h), y1 - __high2float(h));
 }
 
+// 16-byte asynchronous global -> shared copy; zero-fills when !valid.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -297,39 +307,34 @@ __global__ void __launch_bounds__((MT + 1) * 32)
   if (warp > 0) {
     // ----------------------------------------------------------- consumers
     const int ctid = threadIdx.x - 32;
-    // Q rows ri = hh * gamma + i  <-  qkv row b*gamma + i, column (g*group + hh) * hd
+    // Q rows ri = hh * gamma + i  <-  qkv row b*gamma + i, column (g*group + hh) * hd,
+    // and the block's own K/V rows: asynchronous 16-byte copies, all in flight
+    // together (rows past the block are zero-filled).
     for (int idx = ctid; idx < kMq * (HD / 8); idx += kConsumers) {
       const int ri = idx / (HD / 8), ch = idx % (HD / 8);
-      uint4 v = make_uint4(0, 0, 0, 0), vl = make_uint4(0, 0, 0, 0);
-      if (ri < rows) {
-        const int hh = ri / a.gamma, i = ri % a.gamma;
-        v = *reinterpret_cast<const uint4*>(a.qkv + (size_t)(b * a.gamma + i) * a.ld_qkv +
-                                            (size_t)(g * group + hh) * HD + ch * 8);
-        if (a.q_lo)
-          vl = *reinterpret_cast<const uint4*>(a.q_lo + (size_t)(b * a.gamma + i) * a.ld_q_lo +
-                                               (size_t)(g * group + hh) * HD + ch * 8);
-      }
+      const bool ok = ri < rows;
+      const int hh = ok ? ri / a.gamma : 0, i = ok ? ri % a.gamma : 0;
+      const size_t src = (size_t)(b * a.gamma + i) * a.ld_qkv + (size_t)(g * group + hh) * HD + ch * 8;
       const int col = ch * 8;
-      *reinterpret_cast<uint4*>(q_s + (col >> 6) * (kMq * 128) + swz(ri, col & 63)) = v;
-      *reinterpret_cast<uint4*>(ql_s + (col >> 6) * (kMq * 128) + swz(ri, col & 63)) = vl;
+      const uint32_t off = (col >> 6) * (kMq * 128) + swz(ri, col & 63);
+      cp_async16(q_s + off, a.qkv + src, ok);
+      const size_t src_lo = (size_t)(b * a.gamma + i) * a.ld_q_lo + (size_t)(g * group + hh) * HD + ch * 8;
+      cp_async16(ql_s + off, a.q_lo ? a.q_lo + src_lo : a.qkv + src, ok && a.q_lo);
     }
     if (do_block) {
       const size_t kcol = (size_t)a.n_q * HD + (size_t)g * HD;
       const size_t vcol = (size_t)(a.n_q + a.n_kv) * HD + (size_t)g * HD;
       for (int idx = ctid; idx < kBlkKeys * (HD / 8); idx += kConsumers) {
         const int r = idx / (HD / 8), ch = idx % (HD / 8);
-        uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-        if (r < a.gamma) {
-          const __nv_bfloat16* row = a.qkv + (size_t)(b * a.gamma + r) * a.ld_qkv;
-          kv = *reinterpret_cast<const uint4*>(row + kcol + ch * 8);
-          vv = *reinterpret_cast<const uint4*>(row + vcol + ch * 8);
-        }
+        const bool ok = r < a.gamma;
+        const __nv_bfloat16* row = a.qkv + (size_t)(b * a.gamma + (ok ? r : 0)) * a.ld_qkv;
         const int col = ch * 8;
         const uint32_t off = (col >> 6) * (kBlkKeys * 128) + swz(r, col & 63);
-        *reinterpret_cast<uint4*>(bk_s + off) = kv;
-        *reinterpret_cast<uint4*>(bv_s + off) = vv;
+        cp_async16(bk_s + off, row + kcol + ch * 8, ok);
+        cp_async16(bv_s + off, row + vcol + ch * 8, ok);
       }
     }
+    cp_async_wait_all();
     named_sync(1, kConsumers);
 
     const int mt = warp - 1;
@@ -425,28 +430,47 @@ __global__ void __launch_bounds__((MT + 1) * 32)
   const int my_rows = (rows - rank + S - 1) / S;           // rows rank, rank + S, ...
   if ((int)threadIdx.x < my_rows) {
     const int ri = rank + (int)threadIdx.x * S;
+    float mv[16], lv[16];
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+      if (s < S) {
+        const float* ml = cluster.map_shared_rank(ml_s, s);
+        mv[s] = ml[ri * 2];
+        lv[s] = ml[ri * 2 + 1];
+      }
+    }
     float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, cluster.map_shared_rank(ml_s, s)[ri * 2]);
+#pragma unroll
+    for (int s = 0; s < 16; ++s)
+      if (s < S) M = fmaxf(M, mv[s]);
     float den = 0.0f;
-    for (int s = 0; s < S; ++s) {
-      const float* ml = cluster.map_shared_rank(ml_s, s);
-      const float ms = ml[ri * 2];
-      const float w = ms == -INFINITY ? 0.0f : exp2f(ms - M);
-      w_s[threadIdx.x * 16 + s] = w;
-      den += w * ml[ri * 2 + 1];
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+      if (s < S) {
+        mv[s] = mv[s] == -INFINITY ? 0.0f : exp2f(mv[s] - M);
+        den += mv[s] * lv[s];
+      }
     }
     const float inv = 1.0f / den;
-    for (int s = 0; s < S; ++s) w_s[threadIdx.x * 16 + s] *= inv;
+#pragma unroll
+    for (int s = 0; s < 16; ++s)
+      if (s < S) w_s[threadIdx.x * 16 + s] = mv[s] * inv;
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < my_rows * (HD / 2); idx += blockDim.x) {
     const int k = idx / (HD / 2), d = (idx % (HD / 2)) * 2;
     const int ri = rank + k * S;
+    float2 pv[16];
+#pragma unroll
+    for (int s = 0; s < 16; ++s)
+      if (s < S) pv[s] = *reinterpret_cast<const float2*>(cluster.map_shared_rank(part_s, s) + ri * HD + d);
     float o0 = 0.0f, o1 = 0.0f;
-    for (int s = 0; s < S; ++s) {
-      const float2 p = *reinterpret_cast<const float2*>(cluster.map_shared_rank(part_s, s) + ri * HD + d);
-      o0 += w_s[k * 16 + s] * p.x;
-      o1 += w_s[k * 16 + s] * p.y;
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+      if (s < S) {
+        o0 += w_s[k * 16 + s] * pv[s].x;
+        o1 += w_s[k * 16 + s] * pv[s].y;
+      }
     }
     const int hh = ri / a.gamma, i = ri % a.gamma;
     store_pair2(a.out, a.out_lo,

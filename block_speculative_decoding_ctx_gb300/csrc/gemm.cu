@@ -43,8 +43,9 @@ constexpr int kABytes = 128 * kBK * 2;    // weight box per stage
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
 
 // Rotation angle pos * inv_freq reduced to [-pi, pi] with float-float
-// arithmetic: inv_freq = hi + lo (from a double), the product error is
-// recovered with an FMA, and 2*pi is split into two floats (Cody-Waite).
+// arithmetic: inv_freq = hi + lo (computed in double on the host), the
+// product error is recovered with an FMA, and 2*pi is split into two floats
+// (Cody-Waite).
 __device__ __forceinline__ void rope_sincos(float pos, float inv_hi, float inv_lo, float* s,
                                             float* c) {
   const float a = pos * inv_hi;
@@ -60,13 +61,11 @@ struct RopeRow {
   float inv_hi, inv_lo;
   bool first_half;
 };
-__device__ __forceinline__ RopeRow rope_row(int d, int hd, float theta) {
+__device__ __forceinline__ RopeRow rope_row(int d, int hd, const float2* inv) {
   const int half = hd >> 1;
-  const int j = d % half;
-  const double inv = pow((double)theta, -2.0 * (double)j / (double)hd);
   RopeRow rr;
-  rr.inv_hi = (float)inv;
-  rr.inv_lo = (float)(inv - (double)rr.inv_hi);
+  rr.inv_hi = inv[d % half].x;
+  rr.inv_lo = inv[d % half].y;
   rr.first_half = d < half;
   return rr;
 }
@@ -128,7 +127,7 @@ __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const floa
     if (n < e.N) {
       const bool rot = n < e.rope_rows;
       const int d = n % e.hd;
-      const RopeRow rr = rope_row(d, e.hd, e.rope_theta);
+      const RopeRow rr = rope_row(d, e.hd, e.rope_inv);
       const int pr = r ^ (e.hd >> 1);
 #pragma unroll 4
       for (int j = 0; j < 16; ++j) {
@@ -165,7 +164,7 @@ __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const floa
     const int kv = local / e.kv_dim;            // 0 = K, 1 = V
     const int g = (local % e.kv_dim) / e.hd;
     const int d = local % e.hd;
-    const RopeRow rr = rope_row(d, e.hd, e.rope_theta);
+    const RopeRow rr = rope_row(d, e.hd, e.rope_inv);
     const int pr = r ^ (e.hd >> 1);
     __nv_bfloat16* ring = static_cast<__nv_bfloat16*>(kv ? e.ring_v : e.ring_k);
 #pragma unroll 4

@@ -60,7 +60,7 @@ struct GemmEpi {
   // rotary positions
   const int64_t* ctx_len;
   int gamma;
-  float rope_theta;
+  float2 rope_inv[64];  // inv_freq_j = theta^(-2j/hd) as a float pair (hi, lo), j < hd/2
   int rope_rows;
   int hd;
   // context ring scatter
