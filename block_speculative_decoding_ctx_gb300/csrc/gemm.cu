@@ -465,11 +465,13 @@ __device__ __forceinline__ int streamk_cta(long long it, long long iters, int G)
   return c;
 }
 
-// Persistent, warp-specialised stream-K variant: G CTAs share the I = tiles x
-// k-blocks iterations evenly, CTA c taking [floor(c I / G), floor((c+1) I / G)),
-// so no CTA waits on a partly filled last wave.  Iterations run in tile order
-// (token tiles fastest, so CTAs working at the same time share weight tiles
-// in L2).  A CTA's run of iterations inside one tile is a segment: a segment
+// Persistent, warp-specialised stream-K variant.  The G CTAs form m_tiles
+// groups (CTA c serves token tile g = c mod m_tiles with rank i = c / m_tiles);
+// the Gg = G / m_tiles CTAs of a group share the I = weight tiles x k-blocks
+// iterations evenly, rank i taking [floor(i I / Gg), floor((i+1) I / Gg)), so
+// no CTA waits on a partly filled last wave, and CTAs of equal rank in the
+// different groups work on the same weight tile at the same moment (one HBM
+// read of it serves every token tile).  A CTA's run of iterations inside one tile is a segment: a segment
 // covering the whole tile goes straight to the epilogue; otherwise its fp32
 // part is stored (slot: CTA x {first, last} segment of the CTA), a ticket is
 // taken, and the tile's last segment to arrive sums the parts in k order —
@@ -501,9 +503,11 @@ __global__ void __launch_bounds__(192, 1)
   float* xchg = reinterpret_cast<float*>(smem + STAGES * kStage);
   const int T = ao.split ? BN / 2 : BN;
   const int kb_total = (args.K + kBK - 1) / kBK;
-  const long long iters = (long long)n_tiles * m_tiles * kb_total;
-  const int G = gridDim.x, c = blockIdx.x;
-  const long long it_begin = (long long)c * iters / G, it_end = (long long)(c + 1) * iters / G;
+  const long long iters = (long long)n_tiles * kb_total;  // per group
+  const int c = blockIdx.x;
+  const int G = gridDim.x / m_tiles;                      // CTAs per group
+  const int grp = c % m_tiles, rank = c / m_tiles;
+  const long long it_begin = (long long)rank * iters / G, it_end = (long long)(rank + 1) * iters / G;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -543,7 +547,7 @@ __global__ void __launch_bounds__(192, 1)
         const int tile = (int)(it / kb_total), kb = (int)(it % kb_total);
         if (tile != cur_tile) {
           cur_tile = tile;
-          const int tile_m = tile % m_tiles, tile_n = tile / m_tiles;
+          const int tile_m = grp, tile_n = tile;
           if (ao.dual) {
             map_i = 0;
             row0 = ao.row_offset + tile_n * 64;
@@ -619,12 +623,12 @@ __global__ void __launch_bounds__(192, 1)
     const size_t per_part = (size_t)n_chunks * 16 * 128;
     int seg = 0;
     for (long long it = it_begin; it < it_end; ++seg) {
-      const int tile = (int)(it / kb_total);
+      const int tile = (int)(it / kb_total);  // weight tile; token tile = grp
       const long long t0 = (long long)tile * kb_total, t1 = t0 + kb_total;
       const long long seg_end = t1 < it_end ? t1 : it_end;
       const bool whole = (it == t0) && (seg_end == t1);
       const int which = (it == it_begin) ? 0 : 1;  // first or last segment of this CTA
-      const int tile_m = tile % m_tiles, tile_n = tile / m_tiles;
+      const int tile_m = grp, tile_n = tile;
       const int buf = seg & 1;
       const uint32_t use = (uint32_t)(seg >> 1);
       it = seg_end;
@@ -673,10 +677,11 @@ __global__ void __launch_bounds__(192, 1)
       }
       if (whole) continue;
       // a part of the tile: take a ticket; the tile's last part reduces
-      const int c0 = streamk_cta(t0, iters, G), c1 = streamk_cta(t1 - 1, iters, G);
+      const int c0 = streamk_cta(t0, iters, G), c1 = streamk_cta(t1 - 1, iters, G);  // ranks
+      const int tile_id = tile * m_tiles + grp;
       __threadfence();
       asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (threadIdx.x == 64) last_sh = (atomicAdd(&args.counters[tile], 1) == c1 - c0);
+      if (threadIdx.x == 64) last_sh = (atomicAdd(&args.counters[tile_id], 1) == c1 - c0);
       asm volatile("bar.sync 1, 128;" ::: "memory");
       if (!last_sh) continue;
       __threadfence();
@@ -686,13 +691,13 @@ __global__ void __launch_bounds__(192, 1)
         for (int j = 0; j < 16; ++j) v[j] = 0.0f;
         for (int cc = c0; cc <= c1; ++cc) {
           const int w = ((long long)cc * iters / G >= t0) ? 0 : 1;
-          const float* ps = args.partial + ((size_t)cc * 2 + w) * per_part;
+          const float* ps = args.partial + ((size_t)(cc * m_tiles + grp) * 2 + w) * per_part;
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] += __ldcg(ps + (ch * 16 + j) * 128 + r);
         }
         epilogue_chunk<true>(epi, ao, v, tile_m * T + ch * 16, 1, ntok, tile_n, r, xchg);
       }
-      if (threadIdx.x == 64) atomicExch(&args.counters[tile], 0);
+      if (threadIdx.x == 64) atomicExch(&args.counters[tile_id], 0);
     }
   }
   tc_fence_before();
@@ -853,10 +858,11 @@ int launch_gemm(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void
   // Token tiles of DFLASH_STREAMK_MIN_T+ columns: the persistent stream-K kernel
   // (one CTA per SM), when its parts fit the partial buffer.
   if (T >= DFLASH_STREAMK_MIN_T && scratch.partial && tiles <= (size_t)scratch.counters_cap) {
-    const long long iters = (long long)tiles * kb;
-    int grid = scratch.num_sms;
-    if ((long long)grid > iters) grid = (int)iters;
-    if ((size_t)grid * 2 * per_split <= scratch.partial_cap_floats) {
+    // CTAs per token-tile group: as many as fill the SMs, at most one per iteration
+    long long per_group = scratch.num_sms / m_tiles;
+    if (per_group > (long long)n_tiles * kb) per_group = (long long)n_tiles * kb;
+    const int grid = (int)(per_group * m_tiles);
+    if (per_group >= 1 && (size_t)grid * 2 * per_split <= scratch.partial_cap_floats) {
       args.splits = 1;
       args.cluster = 0;
       switch (BN) {
