@@ -26,7 +26,7 @@
 
 using namespace dfl;
 
-constexpr size_t kGemmPartialFloats = 12u << 20;  // split-K / stream-K partial tiles (48 MiB)
+constexpr size_t kGemmPartialFloats = 4u << 20;  // ticketed split-K partial tiles (16 MiB)
 constexpr int kGemmCounters = 8192;
 
 struct LayerMaps {

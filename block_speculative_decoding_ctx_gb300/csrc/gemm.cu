@@ -456,28 +456,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// CTA whose stream-K range [start(c), start(c + 1)) holds iteration `it`,
-// with start(c) = floor(c * iters / G).
-__device__ __forceinline__ int streamk_cta(long long it, long long iters, int G) {
-  int c = (int)((it * G) / iters);
-  while (c + 1 < G && (long long)(c + 1) * iters / G <= it) ++c;
-  while (c > 0 && (long long)c * iters / G > it) --c;
-  return c;
-}
-
-// Persistent, warp-specialised stream-K variant.  The G CTAs form m_tiles
-// groups (CTA c serves token tile g = c mod m_tiles with rank i = c / m_tiles);
-// the Gg = G / m_tiles CTAs of a group share the I = weight tiles x k-blocks
-// iterations evenly, rank i taking [floor(i I / Gg), floor((i+1) I / Gg)), so
-// no CTA waits on a partly filled last wave, and CTAs of equal rank in the
-// different groups work on the same weight tile at the same moment (one HBM
-// read of it serves every token tile).  A CTA's run of iterations inside one tile is a segment: a segment
-// covering the whole tile goes straight to the epilogue; otherwise its fp32
-// part is stored (slot: CTA x {first, last} segment of the CTA), a ticket is
-// taken, and the tile's last segment to arrive sums the parts in k order —
-// deterministic — and runs the epilogue.  Warp 0 lane 0 issues TMA, warp 1
-// lane 0 issues MMAs, warps 2-5 run the epilogue; two TMEM accumulators let
-// one segment's epilogue overlap the next segment's mainloop.
+// Persistent, warp-specialised variant for many token columns (no split-K):
+// one CTA per SM walks the tiles t = blockIdx.x, blockIdx.x + gridDim.x, ...
+// (token tiles fastest, so CTAs running at the same time share weight tiles in
+// L2).  Warp 0 lane 0 issues TMA, warp 1 lane 0 issues MMAs, warps 2-5 run
+// the epilogue.  Two TMEM accumulators let the epilogue of one tile overlap
+// the mainloop of the next.
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(192, 1)
     gemm_bf16_tc_persistent_kernel(const __grid_constant__ GemmAMaps A,
@@ -485,9 +469,9 @@ __global__ void __launch_bounds__(192, 1)
                                    const GemmArgs args, const GemmEpi epi, int n_tiles, int m_tiles) {
   constexpr int kBBytes = BN * kBK * 2;
   constexpr int kStage = kABytes + kBBytes;
-  constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;  // two accumulators
+  constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
   static_assert(kStage % 1024 == 0, "stage buffers must keep 1024-byte alignment");
-  static_assert(2 * BN <= 512, "two accumulators must fit tensor memory");
+  static_assert(kTmemCols <= 512, "two accumulators must fit tensor memory");
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
@@ -496,18 +480,13 @@ __global__ void __launch_bounds__(192, 1)
   __shared__ __align__(8) uint64_t acce_bar[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
-  __shared__ int last_sh;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* xchg = reinterpret_cast<float*>(smem + STAGES * kStage);
   const int T = ao.split ? BN / 2 : BN;
   const int kb_total = (args.K + kBK - 1) / kBK;
-  const long long iters = (long long)n_tiles * kb_total;  // per group
-  const int c = blockIdx.x;
-  const int G = gridDim.x / m_tiles;                      // CTAs per group
-  const int grp = c % m_tiles, rank = c / m_tiles;
-  const long long it_begin = (long long)rank * iters / G, it_end = (long long)(rank + 1) * iters / G;
+  const int total = n_tiles * m_tiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -541,44 +520,41 @@ __global__ void __launch_bounds__(192, 1)
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
       bool waited = false;
-      int n = 0;
-      int cur_tile = -1, map_i = 0, row0 = 0, tok0 = 0;
-      for (long long it = it_begin; it < it_end && !abort_sh; ++it, ++n) {
-        const int tile = (int)(it / kb_total), kb = (int)(it % kb_total);
-        if (tile != cur_tile) {
-          cur_tile = tile;
-          const int tile_m = grp, tile_n = tile;
-          if (ao.dual) {
-            map_i = 0;
-            row0 = ao.row_offset + tile_n * 64;
-          } else {
-            map_i = tile_n / ao.tiles_per_map;
-            row0 = ao.row_offset + (tile_n % ao.tiles_per_map) * 128;
-          }
-          tok0 = tile_m * T;
-        }
-        const int s = n % STAGES;
-        const uint32_t ph = (uint32_t)(n / STAGES) & 1u;
-        if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1u, &abort_sh, args.status)) break;
-        uint8_t* sa = smem + s * kStage;
-        mbar_arrive_expect_tx(&full_bar[s], kStage);
-        const int kc = kb * kBK;
+      int it = 0;
+      for (int t = blockIdx.x; t < total && !abort_sh; t += gridDim.x) {
+        const int tile_m = t % m_tiles, tile_n = t / m_tiles;
+        int map_i = 0, row0;
         if (ao.dual) {
-          tma_load_2d(sa, &A.map[0], &full_bar[s], kc, row0, pol_w);
-          tma_load_2d(sa + 64 * 128, &A.map[1], &full_bar[s], kc, row0, pol_w);
+          row0 = ao.row_offset + tile_n * 64;
         } else {
-          tma_load_2d(sa, &A.map[map_i], &full_bar[s], kc, row0, pol_w);
+          map_i = tile_n / ao.tiles_per_map;
+          row0 = ao.row_offset + (tile_n % ao.tiles_per_map) * 128;
         }
-        if (!waited) {  // activations come from the previous kernel
-          grid_dependency_wait();
-          waited = true;
+        const int tok0 = tile_m * T;
+        for (int kb = 0; kb < kb_total; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1u, &abort_sh, args.status)) break;
+          uint8_t* sa = smem + s * kStage;
+          mbar_arrive_expect_tx(&full_bar[s], kStage);
+          const int kc = kb * kBK;
+          if (ao.dual) {
+            tma_load_2d(sa, &A.map[0], &full_bar[s], kc, row0, pol_w);
+            tma_load_2d(sa + 64 * 128, &A.map[1], &full_bar[s], kc, row0, pol_w);
+          } else {
+            tma_load_2d(sa, &A.map[map_i], &full_bar[s], kc, row0, pol_w);
+          }
+          if (!waited) {  // activations come from the previous kernel
+            grid_dependency_wait();
+            waited = true;
+          }
+          tma_load_2d(sa + kABytes, &tmB, &full_bar[s], kc, tok0, pol_x);
+          if (ao.split) tma_load_2d(sa + kABytes + T * 128, &tmB, &full_bar[s], kc, epi.M + tok0, pol_x);
         }
-        tma_load_2d(sa + kABytes, &tmB, &full_bar[s], kc, tok0, pol_x);
-        if (ao.split) tma_load_2d(sa + kABytes + T * 128, &tmB, &full_bar[s], kc, epi.M + tok0, pol_x);
       }
       if (abort_sh) {
         int dummy = 0;
-        for (int i = (n > STAGES ? n - STAGES : 0); i < n; ++i)
+        for (int i = (it > STAGES ? it - STAGES : 0); i < it; ++i)
           (void)mbar_wait_bounded(&full_bar[i % STAGES], (uint32_t)(i / STAGES) & 1u, &dummy, nullptr,
                                   100000000ull);
       }
@@ -587,19 +563,16 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       // ------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
-      int n = 0, seg = 0;
-      for (long long it = it_begin; it < it_end && !abort_sh; ++seg) {
-        const long long seg_end = ((it / kb_total) + 1) * kb_total < it_end ? ((it / kb_total) + 1) * kb_total
-                                                                            : it_end;
-        const int buf = seg & 1;
-        const uint32_t use = (uint32_t)(seg >> 1);
+      int it = 0, lt = 0;
+      for (int t = blockIdx.x; t < total && !abort_sh; t += gridDim.x, ++lt) {
+        const int buf = lt & 1;
+        const uint32_t use = (uint32_t)(lt >> 1);
         if (!mbar_wait_bounded(&acce_bar[buf], (use & 1u) ^ 1u, &abort_sh, args.status)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * BN);
-        bool first = true;
-        for (; it < seg_end; ++it, ++n) {
-          const int s = n % STAGES;
-          const uint32_t ph = (uint32_t)(n / STAGES) & 1u;
+        for (int kb = 0; kb < kb_total; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
           if (!mbar_wait_bounded(&full_bar[s], ph, &abort_sh, args.status)) break;
           tc_fence_after();
           const uint32_t a_addr = smem_u32(smem + s * kStage);
@@ -607,8 +580,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
             tc_mma_bf16(d, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), idesc,
-                        (!first || k) ? 1u : 0u);
-          first = false;
+                        (kb | k) ? 1u : 0u);
           tc_commit(&empty_bar[s]);
         }
         tc_commit(&accf_bar[buf]);
@@ -620,84 +592,41 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t t_row = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const int ntok = T < 16 ? T : 16;
     const int n_chunks = (T + 15) / 16;
-    const size_t per_part = (size_t)n_chunks * 16 * 128;
-    int seg = 0;
-    for (long long it = it_begin; it < it_end; ++seg) {
-      const int tile = (int)(it / kb_total);  // weight tile; token tile = grp
-      const long long t0 = (long long)tile * kb_total, t1 = t0 + kb_total;
-      const long long seg_end = t1 < it_end ? t1 : it_end;
-      const bool whole = (it == t0) && (seg_end == t1);
-      const int which = (it == it_begin) ? 0 : 1;  // first or last segment of this CTA
-      const int tile_m = grp, tile_n = tile;
-      const int buf = seg & 1;
-      const uint32_t use = (uint32_t)(seg >> 1);
-      it = seg_end;
+    int lt = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
+      const int tile_m = t % m_tiles, tile_n = t / m_tiles;
+      const int buf = lt & 1;
+      const uint32_t use = (uint32_t)(lt >> 1);
       const bool ok = mbar_wait_bounded(&accf_bar[buf], use & 1u, &abort_sh, args.status);
       // the four epilogue warps agree before acting on the outcome
       asm volatile("bar.sync 1, 128;" ::: "memory");
       if (!ok || abort_sh) break;
       tc_fence_after();
       const uint32_t base = t_row + (uint32_t)(buf * BN);
-      float* part = args.partial + ((size_t)c * 2 + which) * per_part;
-      for (int ch = 0; ch < n_chunks; ++ch) {
+      for (int c = 0; c < n_chunks; ++c) {
         float v[16];
         uint32_t raw[16];
         if (!ao.split) {
-          tmem_ld_x16(base + ch * 16, raw);
+          tmem_ld_x16(base + c * 16, raw);
           tc_wait_ld();
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]);
-        } else if (T >= 16) {
+        } else {
           uint32_t lo[16];
-          tmem_ld_x16(base + ch * 16, raw);
-          tmem_ld_x16(base + T + ch * 16, lo);
+          tmem_ld_x16(base + c * 16, raw);
+          tmem_ld_x16(base + T + c * 16, lo);
           tc_wait_ld();
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]) + __uint_as_float(lo[j]);
-        } else {
-          tmem_ld_x16(base, raw);
-          tc_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(raw[j]) + __uint_as_float(raw[j + 8]);
-#pragma unroll
-          for (int j = 8; j < 16; ++j) v[j] = 0.0f;
         }
-        if (ch == n_chunks - 1) {
+        if (c == n_chunks - 1) {
           // every column of this accumulator is in registers: hand it back
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acce_bar[buf]);
         }
-        if (whole) {
-          epilogue_chunk<true>(epi, ao, v, tile_m * T + ch * 16, 1, ntok, tile_n, r, xchg);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) part[(ch * 16 + j) * 128 + r] = v[j];
-        }
+        epilogue_chunk<true>(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg);
       }
-      if (whole) continue;
-      // a part of the tile: take a ticket; the tile's last part reduces
-      const int c0 = streamk_cta(t0, iters, G), c1 = streamk_cta(t1 - 1, iters, G);  // ranks
-      const int tile_id = tile * m_tiles + grp;
-      __threadfence();
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (threadIdx.x == 64) last_sh = (atomicAdd(&args.counters[tile_id], 1) == c1 - c0);
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (!last_sh) continue;
-      __threadfence();
-      for (int ch = 0; ch < n_chunks; ++ch) {
-        float v[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = 0.0f;
-        for (int cc = c0; cc <= c1; ++cc) {
-          const int w = ((long long)cc * iters / G >= t0) ? 0 : 1;
-          const float* ps = args.partial + ((size_t)(cc * m_tiles + grp) * 2 + w) * per_part;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] += __ldcg(ps + (ch * 16 + j) * 128 + r);
-        }
-        epilogue_chunk<true>(epi, ao, v, tile_m * T + ch * 16, 1, ntok, tile_n, r, xchg);
-      }
-      if (threadIdx.x == 64) atomicExch(&args.counters[tile_id], 0);
     }
   }
   tc_fence_before();
@@ -756,8 +685,8 @@ int launch_one(const GemmAMaps& A, const CUtensorMap& tmB, const GemmAOpts& ao, 
 
 template <int BN, int STAGES>
 int launch_persistent(const GemmAMaps& A, const CUtensorMap& tmB, const GemmAOpts& ao,
-                      GemmArgs args, const GemmEpi& epi, int n_tiles, int m_tiles, int grid,
-                      cudaStream_t s, bool pdl) {
+                      const GemmArgs& args, const GemmEpi& epi, int n_tiles, int m_tiles,
+                      int num_sms, cudaStream_t s, bool pdl) {
   auto kern = gemm_bf16_tc_persistent_kernel<BN, STAGES>;
   constexpr size_t smem = (size_t)STAGES * (kABytes + BN * kBK * 2) + 16 * 128 * 4 + 1024;
   static bool attr_set = false;
@@ -767,8 +696,9 @@ int launch_persistent(const GemmAMaps& A, const CUtensorMap& tmB, const GemmAOpt
       return DFLASH_ERR_LAUNCH;
     attr_set = true;
   }
+  const int total = n_tiles * m_tiles;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = dim3(total < num_sms ? total : num_sms);
   cfg.blockDim = dim3(192);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -855,23 +785,10 @@ int launch_gemm(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void
   args.partial = scratch.partial;
   args.counters = scratch.counters;
   args.status = scratch.status;
-  // Token tiles of DFLASH_STREAMK_MIN_T+ columns: the persistent stream-K kernel
-  // (one CTA per SM), when its parts fit the partial buffer.
-  if (T >= DFLASH_STREAMK_MIN_T && scratch.partial && tiles <= (size_t)scratch.counters_cap) {
-    // CTAs per token-tile group: as many as fill the SMs, at most one per iteration
-    long long per_group = scratch.num_sms / m_tiles;
-    if (per_group > (long long)n_tiles * kb) per_group = (long long)n_tiles * kb;
-    const int grid = (int)(per_group * m_tiles);
-    if (per_group >= 1 && (size_t)grid * 2 * per_split <= scratch.partial_cap_floats) {
-      args.splits = 1;
-      args.cluster = 0;
-      switch (BN) {
-        case 16: return launch_persistent<16, 8>(A, tmB, ao, args, epi, n_tiles, m_tiles, grid, s, pdl);
-        case 64: return launch_persistent<64, 6>(A, tmB, ao, args, epi, n_tiles, m_tiles, grid, s, pdl);
-        case 128: return launch_persistent<128, 6>(A, tmB, ao, args, epi, n_tiles, m_tiles, grid, s, pdl);
-        default: return launch_persistent<256, 4>(A, tmB, ao, args, epi, n_tiles, m_tiles, grid, s, pdl);
-      }
-    }
+  // many token columns and no split-K: the persistent kernel
+  if (splits == 1 && T >= 64 && (size_t)n_tiles * m_tiles >= (size_t)scratch.num_sms) {
+    if (BN == 256) return launch_persistent<256, 4>(A, tmB, ao, args, epi, n_tiles, m_tiles, scratch.num_sms, s, pdl);
+    if (BN == 128) return launch_persistent<128, 6>(A, tmB, ao, args, epi, n_tiles, m_tiles, scratch.num_sms, s, pdl);
   }
   dim3 grid(n_tiles, m_tiles, splits);
   switch (BN) {

@@ -86,12 +86,6 @@ struct GemmScratch {
   int num_sms;      // persistent kernels launch one CTA per SM
 };
 
-// Smallest token tile (columns per tile) that uses the persistent stream-K
-// kernel; smaller tiles use the one-tile-per-CTA kernel with split-K.
-#ifndef DFLASH_STREAMK_MIN_T
-#define DFLASH_STREAMK_MIN_T 64
-#endif
-
 // Largest K-split count reduced through a cluster; above it the ticketed
 // reduction through global memory is used.
 #ifndef DFLASH_SPLITK_CLUSTER_MAX
