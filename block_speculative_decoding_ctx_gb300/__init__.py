@@ -24,7 +24,7 @@ DFLASH_VERIFY_SAMPLED = 1
 ERRORS = {
     -1: "DFLASH_ERR_ARG", -2: "DFLASH_ERR_SHAPE", -3: "DFLASH_ERR_ALIGN",
     -4: "DFLASH_ERR_UNSUPPORTED", -5: "DFLASH_ERR_LAUNCH", -6: "DFLASH_ERR_DEVICE_TIMEOUT",
-    -7: "DFLASH_ERR_WORKSPACE", -8: "DFLASH_ERR_CUDA",
+    -7: "DFLASH_ERR_WORKSPACE", -8: "DFLASH_ERR_CUDA", -9: "DFLASH_ERR_RANGE",
 }
 
 

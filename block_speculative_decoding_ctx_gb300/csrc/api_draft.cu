@@ -3,8 +3,9 @@
 //
 // ctx_append  ("DFlash vs DFlash 2" blog, section "Conditioning on the target
 //              model", H_t equation and K/V injection equation):
-//   W_c GEMM (fp32 out) -> RMSNorm(g_c) -> per-layer K/V GEMM whose epilogue
-//   rotates K and scatters K and V into ring slot pos mod W -> ctx_len += n.
+//   W_c GEMM (bf16 features, fp32 out) -> RMSNorm(g_c) (fp16) -> per-layer
+//   K/V GEMM whose epilogue rotates K and scatters K and V into ring slot
+//   pos mod W -> ctx_len += n.
 // draft_block ("DFlash: generate the block all at once"):
 //   embed [anchor, MASK...] + RMSNorm -> for each layer: QKV GEMM (+RoPE) ->
 //   block attention over [ring window ; block] -> O GEMM (+residual) ->
@@ -12,6 +13,9 @@
 //   (final RMSNorm gathers the gamma-1 MASK rows) -> LM head GEMM (fp32
 //   logits) -> top-k + log-sum-exp [-> q = top_p(softmax(logits / T)) ->
 //   y ~ q].
+// Every drafter contraction runs on fp16 operands: the handle holds an fp16
+// copy of the matrices (exact re-encoding of the bf16 values) and every
+// activation between kernels is stored as fp16.
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -30,7 +34,7 @@ constexpr size_t kGemmPartialFloats = 4u << 20;  // ticketed split-K partial til
 constexpr int kGemmCounters = 8192;
 
 struct LayerMaps {
-  CUtensorMap qkv, o, gate, up, down;
+  CUtensorMap qkv, o, gate, up, down;  // over the fp16 copies
 };
 
 struct dflash_handle {
@@ -38,7 +42,8 @@ struct dflash_handle {
   dflash_weights w;
   std::vector<dflash_layer_weights> layers;
   std::vector<LayerMaps> maps;
-  CUtensorMap lm_head, w_c;
+  CUtensorMap lm_head, w_c;  // lm_head: fp16 copy; w_c: the caller's bf16 matrix
+  void* f16 = nullptr;       // fp16 copies of every layer's matrices and the LM head
   int num_sms;
   int mask_id;
   // benchmark hook: event pairs around the GEMM launches of draft_block
@@ -97,7 +102,6 @@ struct DraftWs {
   void* attn;
   void* mlp;
   void* hf;
-  void* q_lo;
   float* logits;
   float* gemm_partial;
   unsigned long long* topk_keys;
@@ -119,14 +123,13 @@ DraftWs draft_layout(const dflash_handle* h, void* base) {
   w.gemm_counters = cv.take<int>(kGemmCounters);
   w.topk_counters = cv.take<int>(R);
   w.samp_counters = cv.take<int>(R);
-  // bf16 GEMM operands are [2, rows, K]: bf16 values, then their bf16 remainders
+  // fp32 residual stream; fp16 GEMM operands
   w.x = cv.take<float>(M * c.hidden);
-  w.h = cv.take<uint16_t>(2 * M * c.hidden);
+  w.h = cv.take<uint16_t>(M * c.hidden);
   w.qkv = cv.take<uint16_t>(M * qkv_dim);
-  w.attn = cv.take<uint16_t>(2 * M * q_dim);
-  w.mlp = cv.take<uint16_t>(2 * M * c.ffn);
-  w.hf = cv.take<uint16_t>(2 * R * c.hidden);
-  w.q_lo = cv.take<uint16_t>(M * q_dim);
+  w.attn = cv.take<uint16_t>(M * q_dim);
+  w.mlp = cv.take<uint16_t>(M * c.ffn);
+  w.hf = cv.take<uint16_t>(R * c.hidden);
   w.logits = cv.take<float>(R * c.vocab);
   w.gemm_partial = cv.take<float>(kGemmPartialFloats);
   w.topk_keys = cv.take<unsigned long long>(R * chunks * 16);
@@ -153,38 +156,22 @@ AppendWs append_layout(const dflash_handle* h, void* base) {
   w.status = static_cast<int*>(base);
   w.gemm_counters = cv.take<int>(kGemmCounters);
   w.fused = cv.take<float>(M * c.hidden);
-  w.ht = cv.take<uint16_t>(2 * M * c.hidden);
+  w.ht = cv.take<uint16_t>(M * c.hidden);
   w.gemm_partial = cv.take<float>(kGemmPartialFloats);
   w.bytes = cv.off;
   return w;
 }
 
-GemmAOpts single_map(int split = 0) {
+GemmAOpts single_map() {
   GemmAOpts o;
   o.n_maps = 1;
   o.tiles_per_map = 1 << 30;
   o.row_offset = 0;
   o.dual = 0;
-  o.split = split;
   return o;
 }
 
-// Token operands are fed as a bf16 (value, remainder) pair — twice the MMA
-// columns, about 16 significant bits.  Which GEMMs get the pair: while the
-// doubled token count still fits the tile the plain operand would use the
-// extra MMA work is free (the GEMM streams weights), so every GEMM gets it;
-// beyond that, the QKV, O and down inputs keep it and the gate|up and LM-head
-// inputs do not.  On the full-size drafter with random weights that choice
-// holds the normwise logit error near 0.65% for +46% MMA work, where bf16
-// everywhere gives 1.5% and the pair on QKV and gate|up gives 0.66% for +65%.
-constexpr int kFreeSplitTokens = 64;
-
-template <typename T>
-T* lo_half(void* base, size_t rows, size_t cols) {
-  return static_cast<T*>(base) + rows * cols;
-}
-
-GemmEpi epi_base(int kind, int M, int N, void* out, long long ld) {
+GemmEpi epi_base(int kind, int M, int N, void* out, long long ld, int* status) {
   GemmEpi e;
   std::memset(&e, 0, sizeof(e));
   e.kind = kind;
@@ -192,6 +179,7 @@ GemmEpi epi_base(int kind, int M, int N, void* out, long long ld) {
   e.N = N;
   e.out = out;
   e.ld = ld;
+  e.status = status;
   return e;
 }
 
@@ -205,27 +193,36 @@ void set_rope_table(GemmEpi& e, const dflash_config& c) {
   }
 }
 
-int splits_for(const dflash_handle* h, int n_tiles, int M, int K, int split) {
-  const int BN = gemm_token_tile(split ? 2 * M : M);
-  const int T = split ? BN / 2 : BN;
-  const int m_tiles = (M + T - 1) / T;
+int splits_for(const dflash_handle* h, int n_tiles, int M, int K) {
+  const int BN = gemm_token_tile(M);
+  const int m_tiles = (M + BN - 1) / BN;
   const int per_sm = BN <= 64 ? 2 : 1;
   return gemm_plan_splits(n_tiles * m_tiles, K, h->num_sms * per_sm);
 }
 
 // Profiling brackets around one launch of the pass (no-ops unless enabled).
+// While the stream is captured, external records become event nodes (with
+// timestamps) of the graph; otherwise they are plain records.
+bool prof_record(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  const cudaError_t rc = cs == cudaStreamCaptureStatusActive
+                             ? cudaEventRecordWithFlags(e, s, cudaEventRecordExternal)
+                             : cudaEventRecord(e, s);
+  if (rc != cudaSuccess) (void)cudaGetLastError();
+  return rc == cudaSuccess;
+}
 int prof_begin(dflash_handle* h, cudaStream_t s) {
   const int i = h->prof_used;
   if (2 * (i + 1) > (int)h->prof_events.size()) return -1;
-  // external records become event nodes (with timestamps) when the stream is captured
-  return cudaEventRecordWithFlags(h->prof_events[2 * i], s, cudaEventRecordExternal) == cudaSuccess
-             ? i
-             : -1;
+  return prof_record(h->prof_events[2 * i], s) ? i : -1;
 }
 void prof_end(dflash_handle* h, cudaStream_t s, int slot, double bytes, int kind) {
   if (slot < 0) return;
-  if (cudaEventRecordWithFlags(h->prof_events[2 * slot + 1], s, cudaEventRecordExternal) != cudaSuccess)
-    return;
+  if (!prof_record(h->prof_events[2 * slot + 1], s)) return;
   h->prof_bytes[slot] = bytes;
   h->prof_kinds[slot] = kind;
   h->prof_used = slot + 1;
@@ -235,7 +232,7 @@ void prof_end(dflash_handle* h, cudaStream_t s, int slot, double bytes, int kind
 int draft_gemm(dflash_handle* h, const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void* x,
                int M, int K, const GemmEpi& e, const GemmScratch& sc, cudaStream_t s, double bytes) {
   const int slot = prof_begin(h, s);
-  const int rc = launch_gemm(A, ao, n_tiles, x, M, K, e, sc, splits_for(h, n_tiles, M, K, ao.split),
+  const int rc = launch_gemm(A, ao, n_tiles, x, OPND_F16, M, K, e, sc, splits_for(h, n_tiles, M, K),
                              s, true);
   if (rc) return rc;
   prof_end(h, s, slot, bytes, DFLASH_KIND_GEMM);
@@ -307,20 +304,62 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
   const dflash_config& c = *cfg;
   const uint64_t d = c.hidden, F = c.ffn, qd = (uint64_t)c.n_q_heads * c.head_dim;
   const uint64_t qkv_rows = (uint64_t)(c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
-  h->maps.resize(c.n_layers);
-  rc = encode_bf16_2d(&h->lm_head, w->lm_head, d, c.vocab, 64, 128);
-  if (!rc) rc = encode_bf16_2d(&h->w_c, w->w_c, (uint64_t)c.n_feat * c.feat_dim, d, 64, 128);
-  for (int l = 0; l < c.n_layers && !rc; ++l) {
+
+  // fp16 copies: per layer qkv, o, gate, up, down, then the LM head; a flag word last
+  struct Mat {
+    const void* src;
+    size_t n;
+    size_t off;
+  };
+  std::vector<Mat> mats;
+  size_t total = 0;
+  auto add = [&](const void* src, size_t n) {
+    mats.push_back({src, n, total});
+    total += align_up(n * 2, 256);
+  };
+  for (int l = 0; l < c.n_layers; ++l) {
     const dflash_layer_weights& L = h->layers[l];
+    add(L.w_qkv, qkv_rows * d);
+    add(L.w_o, d * qd);
+    add(L.w_gate, F * d);
+    add(L.w_up, F * d);
+    add(L.w_down, d * F);
+  }
+  add(w->lm_head, (size_t)c.vocab * d);
+  if (cudaMalloc(&h->f16, total + 256) != cudaSuccess) {
+    (void)cudaGetLastError();
+    h->f16 = nullptr;
+    dflash_destroy(h);
+    return DFLASH_ERR_CUDA;
+  }
+  char* base = static_cast<char*>(h->f16);
+  int* flag = reinterpret_cast<int*>(base + total);
+  // the weights may have been written on any stream: wait for all of it
+  rc = cudaDeviceSynchronize() == cudaSuccess && cudaMemset(flag, 0, sizeof(int)) == cudaSuccess
+           ? DFLASH_OK
+           : DFLASH_ERR_CUDA;
+  for (size_t i = 0; i < mats.size() && !rc; ++i)
+    rc = launch_to_f16(mats[i].src, base + mats[i].off, mats[i].n, flag, 4 * h->num_sms, 0);
+  int bad = 0;
+  if (!rc && cudaMemcpy(&bad, flag, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    rc = DFLASH_ERR_CUDA;
+  if (!rc && bad) rc = DFLASH_ERR_RANGE;
+
+  h->maps.resize(c.n_layers);
+  auto mat = [&](size_t i) { return static_cast<const void*>(base + mats[i].off); };
+  if (!rc) rc = encode_2d(&h->lm_head, mat(mats.size() - 1), OPND_F16, d, c.vocab, 64, 128);
+  if (!rc) rc = encode_2d(&h->w_c, w->w_c, OPND_BF16, (uint64_t)c.n_feat * c.feat_dim, d, 64, 128);
+  for (int l = 0; l < c.n_layers && !rc; ++l) {
     LayerMaps& m = h->maps[l];
-    rc = encode_bf16_2d(&m.qkv, L.w_qkv, d, qkv_rows, 64, 128);
-    if (!rc) rc = encode_bf16_2d(&m.o, L.w_o, qd, d, 64, 128);
-    if (!rc) rc = encode_bf16_2d(&m.gate, L.w_gate, d, F, 64, 64);
-    if (!rc) rc = encode_bf16_2d(&m.up, L.w_up, d, F, 64, 64);
-    if (!rc) rc = encode_bf16_2d(&m.down, L.w_down, F, d, 64, 128);
+    const size_t i = (size_t)l * 5;
+    rc = encode_2d(&m.qkv, mat(i), OPND_F16, d, qkv_rows, 64, 128);
+    if (!rc) rc = encode_2d(&m.o, mat(i + 1), OPND_F16, qd, d, 64, 128);
+    if (!rc) rc = encode_2d(&m.gate, mat(i + 2), OPND_F16, d, F, 64, 64);
+    if (!rc) rc = encode_2d(&m.up, mat(i + 3), OPND_F16, d, F, 64, 64);
+    if (!rc) rc = encode_2d(&m.down, mat(i + 4), OPND_F16, F, d, 64, 128);
   }
   if (rc) {
-    delete h;
+    dflash_destroy(h);
     return rc;
   }
   *out = h;
@@ -328,8 +367,10 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
 }
 
 int dflash_destroy(dflash_handle* h) {
-  if (h)
+  if (h) {
     for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
+    if (h->f16) cudaFree(h->f16);
+  }
   delete h;
   return DFLASH_OK;
 }
@@ -368,13 +409,14 @@ int dflash_ctx_append(dflash_handle* h, int B, int n_max, const void* feats, con
   {
     GemmAMaps A;
     A.map[0] = h->w_c;
-    GemmEpi e = epi_base(EPI_F32, M, d, ws.fused, d);
+    GemmEpi e = epi_base(EPI_F32, M, d, ws.fused, d, ws.status);
     const int nt = (d + 127) / 128;
-    rc = launch_gemm(A, single_map(), nt, feats, M, Kc, e, scratch, splits_for(h, nt, M, Kc, 0), s, true);
+    rc = launch_gemm(A, single_map(), nt, feats, OPND_BF16, M, Kc, e, scratch, splits_for(h, nt, M, Kc),
+                     s, true);
     if (rc) return rc;
   }
-  rc = launch_rmsnorm(ws.fused, M, d, static_cast<const float*>(h->w.g_c), c.eps, 0, ws.ht,
-                      lo_half<uint16_t>(ws.ht, M, d), s);
+  rc = launch_rmsnorm(ws.fused, M, d, static_cast<const float*>(h->w.g_c), c.eps, 0, ws.ht, ws.status,
+                      s);
   if (rc) return rc;
   // K/V of every layer into the ring, up to kMaxAMaps layers per launch
   const int kvd = c.n_kv_heads * c.head_dim;
@@ -388,8 +430,7 @@ int dflash_ctx_append(dflash_handle* h, int B, int n_max, const void* feats, con
     ao.tiles_per_map = tiles_per_layer;
     ao.row_offset = c.n_q_heads * c.head_dim;
     ao.dual = 0;
-    ao.split = 1;
-    GemmEpi e = epi_base(EPI_KV_RING, M, nl * 2 * kvd, nullptr, 0);
+    GemmEpi e = epi_base(EPI_KV_RING, M, nl * 2 * kvd, nullptr, 0, ws.status);
     e.ctx_len = ctx_len;
     set_rope_table(e, c);
     e.hd = c.head_dim;
@@ -403,9 +444,8 @@ int dflash_ctx_append(dflash_handle* h, int B, int n_max, const void* feats, con
     e.n_new = n_new;
     e.req_slot = req_slot;
     e.layer0 = l0;
-    e.status = ws.status;
     const int nt = nl * tiles_per_layer;
-    rc = launch_gemm(A, ao, nt, ws.ht, M, d, e, scratch, splits_for(h, nt, M, d, 1), s, true);
+    rc = launch_gemm(A, ao, nt, ws.ht, OPND_F16, M, d, e, scratch, splits_for(h, nt, M, d), s, true);
     if (rc) return rc;
   }
   return launch_add_lengths(B, n_new, ctx_len, s);
@@ -453,22 +493,17 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
   const size_t ring_layer = (size_t)ring_batch * c.n_kv_heads * c.window * hd;
   int rc;
 
-  const bool split_gu = M <= kFreeSplitTokens;   // gate|up input
-  const bool split_head = R <= kFreeSplitTokens;
   int slot = prof_begin(h, s);
   rc = launch_embed_norm(h->w.embed, anchor, B, gamma, h->mask_id, c.vocab, d,
-                         static_cast<const float*>(h->layers[0].g_attn), c.eps, ws.x, ws.h,
-                         lo_half<uint16_t>(ws.h, M, d), ws.status, s);
+                         static_cast<const float*>(h->layers[0].g_attn), c.eps, ws.x, ws.h, ws.status,
+                         s);
   if (rc) return rc;
   prof_end(h, s, slot, (double)M * d * (2 + 4 + 4), DFLASH_KIND_NORM);
   AttnArgs aa;
-  aa.qkv = static_cast<const __nv_bfloat16*>(ws.qkv);
+  aa.qkv = static_cast<const __half*>(ws.qkv);
   aa.ld_qkv = qkv_dim;
-  aa.out = static_cast<__nv_bfloat16*>(ws.attn);
-  aa.out_lo = lo_half<__nv_bfloat16>(ws.attn, M, qd);
+  aa.out = static_cast<__half*>(ws.attn);
   aa.ld_out = qd;
-  aa.q_lo = static_cast<const __nv_bfloat16*>(ws.q_lo);
-  aa.ld_q_lo = qd;
   aa.ctx_len = ctx_len;
   aa.req_slot = req_slot;
   aa.gamma = gamma;
@@ -493,17 +528,14 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
     {  // QKV (+RoPE on q and k)
       GemmAMaps A;
       A.map[0] = lm.qkv;
-      GemmEpi e = epi_base(EPI_QKV, M, qkv_dim, ws.qkv, qkv_dim);
+      GemmEpi e = epi_base(EPI_QKV, M, qkv_dim, ws.qkv, qkv_dim, ws.status);
       e.ctx_len = ctx_len;
       e.gamma = gamma;
       set_rope_table(e, c);
       e.rope_rows = (c.n_q_heads + c.n_kv_heads) * hd;
       e.hd = hd;
-      e.out_lo = ws.q_lo;
-      e.ld_lo = qd;
-      e.lo_cols = qd;
       const int nt = (qkv_dim + 127) / 128;
-      rc = draft_gemm(h, A, single_map(1), nt, ws.h, M, d, e, scratch, s,
+      rc = draft_gemm(h, A, single_map(), nt, ws.h, M, d, e, scratch, s,
                       2.0 * qkv_dim * d + 2.0 * M * d + 2.0 * M * qkv_dim);
       if (rc) return rc;
     }
@@ -515,27 +547,24 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
     {  // O projection + residual
       GemmAMaps A;
       A.map[0] = lm.o;
-      GemmEpi e = epi_base(EPI_RESID, M, d, ws.x, d);
+      GemmEpi e = epi_base(EPI_RESID, M, d, ws.x, d, ws.status);
       const int nt = (d + 127) / 128;
-      rc = draft_gemm(h, A, single_map(1), nt, ws.attn, M, qd, e, scratch, s,
+      rc = draft_gemm(h, A, single_map(), nt, ws.attn, M, qd, e, scratch, s,
                       2.0 * d * qd + 2.0 * M * qd + 8.0 * M * d);
       if (rc) return rc;
     }
     slot = prof_begin(h, s);
-    rc = launch_rmsnorm(ws.x, M, d, static_cast<const float*>(L.g_mlp), c.eps, 0, ws.h,
-                        split_gu ? lo_half<uint16_t>(ws.h, M, d) : nullptr, s);
+    rc = launch_rmsnorm(ws.x, M, d, static_cast<const float*>(L.g_mlp), c.eps, 0, ws.h, ws.status, s);
     if (rc) return rc;
     prof_end(h, s, slot, (double)M * d * 8, DFLASH_KIND_NORM);
     {  // gate | up + SwiGLU
       GemmAMaps A;
       A.map[0] = lm.gate;
       A.map[1] = lm.up;
-      GemmAOpts ao = single_map(split_gu);
+      GemmAOpts ao = single_map();
       ao.n_maps = 2;
       ao.dual = 1;
-      GemmEpi e = epi_base(EPI_SWIGLU, M, c.ffn, ws.mlp, c.ffn);
-      e.out_lo = lo_half<uint16_t>(ws.mlp, M, c.ffn);
-      e.ld_lo = c.ffn;
+      GemmEpi e = epi_base(EPI_SWIGLU, M, c.ffn, ws.mlp, c.ffn, ws.status);
       const int nt = c.ffn / 64;
       rc = draft_gemm(h, A, ao, nt, ws.h, M, d, e, scratch, s,
                       4.0 * c.ffn * d + 2.0 * M * d + 2.0 * M * c.ffn);
@@ -544,19 +573,19 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
     {  // down + residual
       GemmAMaps A;
       A.map[0] = lm.down;
-      GemmEpi e = epi_base(EPI_RESID, M, d, ws.x, d);
+      GemmEpi e = epi_base(EPI_RESID, M, d, ws.x, d, ws.status);
       const int nt = (d + 127) / 128;
-      rc = draft_gemm(h, A, single_map(1), nt, ws.mlp, M, c.ffn, e, scratch, s,
+      rc = draft_gemm(h, A, single_map(), nt, ws.mlp, M, c.ffn, e, scratch, s,
                       2.0 * d * c.ffn + 2.0 * M * c.ffn + 8.0 * M * d);
       if (rc) return rc;
     }
     slot = prof_begin(h, s);
     if (l + 1 < c.n_layers)
       rc = launch_rmsnorm(ws.x, M, d, static_cast<const float*>(h->layers[l + 1].g_attn), c.eps, 0,
-                          ws.h, lo_half<uint16_t>(ws.h, M, d), s);
+                          ws.h, ws.status, s);
     else
       rc = launch_rmsnorm(ws.x, R, d, static_cast<const float*>(h->w.g_final), c.eps, gamma, ws.hf,
-                          split_head ? lo_half<uint16_t>(ws.hf, R, d) : nullptr, s);
+                          ws.status, s);
     if (rc) return rc;
     prof_end(h, s, slot, (double)(l + 1 < c.n_layers ? M : R) * d * 8, DFLASH_KIND_NORM);
   }
@@ -564,9 +593,9 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
   {  // shared LM head on the gamma - 1 MASK rows
     GemmAMaps A;
     A.map[0] = h->lm_head;
-    GemmEpi e = epi_base(EPI_F32, R, c.vocab, logits, c.vocab);
+    GemmEpi e = epi_base(EPI_F32, R, c.vocab, logits, c.vocab, ws.status);
     const int nt = (c.vocab + 127) / 128;
-    rc = draft_gemm(h, A, single_map(split_head), nt, ws.hf, R, d, e, scratch, s,
+    rc = draft_gemm(h, A, single_map(), nt, ws.hf, R, d, e, scratch, s,
                     2.0 * c.vocab * d + 2.0 * R * d + 4.0 * R * c.vocab);
     if (rc) return rc;
   }

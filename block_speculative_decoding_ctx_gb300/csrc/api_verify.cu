@@ -127,6 +127,7 @@ const char* dflash_strerror(int code) {
     case DFLASH_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait gave up";
     case DFLASH_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case DFLASH_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case DFLASH_ERR_RANGE: return "a weight or an activation is beyond the fp16 range";
     default: return "unknown error code";
   }
 }

@@ -11,8 +11,11 @@
 // the full size) is packed into 16-row MMA tiles, one consumer warp per tile,
 // so every K/V byte read from HBM is used by all query heads of its group.
 // A producer warp streams 64-key K/V tiles of the context ring into shared
-// memory with TMA (128-byte swizzle, evict-first), STAGES deep.  Scores and
-// P.V run on mma.sync bf16 with fp32 accumulation; the softmax is online
+// memory with TMA (128-byte swizzle, evict-first), STAGES deep.  Scores run
+// on mma.sync with fp16 operands (queries are fp16; ring keys, stored bf16,
+// are widened to fp16 in registers — exact in fp16's range) and P.V on bf16
+// operands against the bf16 ring values (fp16 for the block's own values),
+// all with fp32 accumulation; the softmax is online
 // (running max and sum per row, reduced with warp shuffles); the window and
 // block masks are arithmetic (context slot j is visible iff j < min(L, W),
 // every block key is visible).  Splits of the key range write unnormalised
@@ -67,19 +70,34 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+// Two bf16 values (one 32-bit register) as two fp16 values: exact for
+// magnitudes 2^-14 .. 65504, saturated to +-65504 beyond.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  const float lo = __uint_as_float(w << 16);
+  const float hi = __uint_as_float(w & 0xFFFF0000u);
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 
-// Two adjacent outputs as bf16 hi parts, and their bf16 remainders when lo != null.
-__device__ __forceinline__ void store_pair2(__nv_bfloat16* hi, __nv_bfloat16* lo, size_t o, float y0,
-                                            float y1) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
-  *reinterpret_cast<__nv_bfloat162*>(hi + o) = h;
-  if (lo)
-    *reinterpret_cast<__nv_bfloat162*>(lo + o) =
-        __floats2bfloat162_rn(y0 - __low2float(h), y1 - __high2float(h));
+__device__ __forceinline__ void store_h2(__half* out, size_t o, float y0, float y1) {
+  *reinterpret_cast<__half2*>(out + o) = __floats2half2_rn(y0, y1);
 }
 
 // 16-byte asynchronous global -> shared copy; zero-fills when !valid.
@@ -101,13 +119,13 @@ struct WarpState {
   static constexpr int NT = HD / 8;  // output n-tiles of 8 dims
   float o[NT][4];
   float m[2], l[2];
-  uint32_t qa[HD / 16][4];           // Q fragments (A operand), k-steps of 16 dims
-  uint32_t ql[HD / 16][4];           // fragments of the bf16 remainder of Q
+  uint32_t qa[HD / 16][4];           // fp16 Q fragments (A operand), k-steps of 16 dims
 };
 
 // Scores, online softmax and P.V of one key tile held in shared memory as
-// HD/64 swizzled halves [NK keys][64 dims] for K and for V.
-template <int HD, int NK, bool QLO>
+// HD/64 swizzled halves [NK keys][64 dims] for K and for V: bf16 context-ring
+// tiles (RING) or the block's own fp16 keys and values.
+template <int HD, int NK, bool RING>
 __device__ __forceinline__ void process_tile(WarpState<HD>& st, uint32_t k_base, uint32_t v_base,
                                              int n_valid, float scale_log2) {
   constexpr int NT_S = NK / 8;
@@ -117,10 +135,9 @@ __device__ __forceinline__ void process_tile(WarpState<HD>& st, uint32_t k_base,
 #pragma unroll
   for (int j = 0; j < NT_S; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.0f;
 
-  // S = Q K^T.  For each 16-dim k-step the K fragments of all key n-tiles are
-  // loaded first, then every accumulator receives its hi-part MMA and only
-  // then its remainder MMA, so consecutive MMAs on one accumulator are NT_S
-  // instructions apart instead of back to back.
+  // S = Q K^T on fp16 operands.  For each 16-dim k-step the K fragments of
+  // all key n-tiles are loaded (and widened) first, then every accumulator
+  // receives its MMA.
 #pragma unroll
   for (int kk = 0; kk < HD / 16; ++kk) {
     uint32_t bk[NT_S / 2][4];
@@ -130,20 +147,16 @@ __device__ __forceinline__ void process_tile(WarpState<HD>& st, uint32_t k_base,
       const int dim = kk * 16 + (((lane >> 3) & 1) << 3);
       ldsm_x4(k_base + (dim >> 6) * kHalf + swz(key, dim & 63), bk[kp][0], bk[kp][1], bk[kp][2],
               bk[kp][3]);
+      if (RING) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) bk[kp][e] = bf16x2_to_f16x2(bk[kp][e]);
+      }
     }
 #pragma unroll
     for (int kp = 0; kp < NT_S / 2; ++kp) {
-      mma_bf16(s[2 * kp], st.qa[kk][0], st.qa[kk][1], st.qa[kk][2], st.qa[kk][3], bk[kp][0], bk[kp][1]);
-      mma_bf16(s[2 * kp + 1], st.qa[kk][0], st.qa[kk][1], st.qa[kk][2], st.qa[kk][3], bk[kp][2],
-               bk[kp][3]);
-    }
-    if (QLO) {
-#pragma unroll
-      for (int kp = 0; kp < NT_S / 2; ++kp) {
-        mma_bf16(s[2 * kp], st.ql[kk][0], st.ql[kk][1], st.ql[kk][2], st.ql[kk][3], bk[kp][0], bk[kp][1]);
-        mma_bf16(s[2 * kp + 1], st.ql[kk][0], st.ql[kk][1], st.ql[kk][2], st.ql[kk][3], bk[kp][2],
-                 bk[kp][3]);
-      }
+      mma_f16(s[2 * kp], st.qa[kk][0], st.qa[kk][1], st.qa[kk][2], st.qa[kk][3], bk[kp][0], bk[kp][1]);
+      mma_f16(s[2 * kp + 1], st.qa[kk][0], st.qa[kk][1], st.qa[kk][2], st.qa[kk][3], bk[kp][2],
+              bk[kp][3]);
     }
   }
   // mask and scale; rows r0 = lane/4 (regs 0,1) and r1 = lane/4 + 8 (regs 2,3)
@@ -185,16 +198,19 @@ __device__ __forceinline__ void process_tile(WarpState<HD>& st, uint32_t k_base,
       st.l[e >> 1] += s[j][e];
     }
   }
-  // O += P V: k-steps of 16 keys; V^T fragments through ldmatrix.trans.  Keys
-  // past n_valid have P = 0, and their V halves are zeroed in registers so
-  // that whatever those slots hold cannot turn 0 * V into NaN.
+  // O += P V: k-steps of 16 keys; V^T fragments through ldmatrix.trans; P in
+  // the type of V (bf16 for ring tiles, fp16 for the block).  Keys past
+  // n_valid have P = 0, and their V halves are zeroed in registers so that
+  // whatever those slots hold cannot turn 0 * V into NaN.
   const int kq = (lane & 3) << 1;
 #pragma unroll
   for (int ks = 0; ks < NK / 16; ++ks) {
-    const uint32_t a0 = pack_bf16(s[2 * ks][0], s[2 * ks][1]);
-    const uint32_t a1 = pack_bf16(s[2 * ks][2], s[2 * ks][3]);
-    const uint32_t a2 = pack_bf16(s[2 * ks + 1][0], s[2 * ks + 1][1]);
-    const uint32_t a3 = pack_bf16(s[2 * ks + 1][2], s[2 * ks + 1][3]);
+    const uint32_t a0 = RING ? pack_bf16(s[2 * ks][0], s[2 * ks][1]) : pack_f16(s[2 * ks][0], s[2 * ks][1]);
+    const uint32_t a1 = RING ? pack_bf16(s[2 * ks][2], s[2 * ks][3]) : pack_f16(s[2 * ks][2], s[2 * ks][3]);
+    const uint32_t a2 = RING ? pack_bf16(s[2 * ks + 1][0], s[2 * ks + 1][1])
+                             : pack_f16(s[2 * ks + 1][0], s[2 * ks + 1][1]);
+    const uint32_t a3 = RING ? pack_bf16(s[2 * ks + 1][2], s[2 * ks + 1][3])
+                             : pack_f16(s[2 * ks + 1][2], s[2 * ks + 1][3]);
     const int k0 = ks * 16 + kq;  // keys of the low (k0, k0+1) and high (k0+8, k0+9) halves
     const uint32_t m_lo = (k0 < n_valid ? 0x0000FFFFu : 0u) | (k0 + 1 < n_valid ? 0xFFFF0000u : 0u);
     const uint32_t m_hi = (k0 + 8 < n_valid ? 0x0000FFFFu : 0u) | (k0 + 9 < n_valid ? 0xFFFF0000u : 0u);
@@ -209,8 +225,13 @@ __device__ __forceinline__ void process_tile(WarpState<HD>& st, uint32_t k_base,
       b2 &= m_lo;
       b1 &= m_hi;
       b3 &= m_hi;
-      mma_bf16(st.o[2 * dp], a0, a1, a2, a3, b0, b1);
-      mma_bf16(st.o[2 * dp + 1], a0, a1, a2, a3, b2, b3);
+      if (RING) {
+        mma_bf16(st.o[2 * dp], a0, a1, a2, a3, b0, b1);
+        mma_bf16(st.o[2 * dp + 1], a0, a1, a2, a3, b2, b3);
+      } else {
+        mma_f16(st.o[2 * dp], a0, a1, a2, a3, b0, b1);
+        mma_f16(st.o[2 * dp + 1], a0, a1, a2, a3, b2, b3);
+      }
     }
   }
 }
@@ -234,9 +255,8 @@ __global__ void __launch_bounds__((MT + 1) * 32)
   __shared__ int abort_sh;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* q_s = smem + kStages * kStageBytes;            // [kMq][HD] swizzled halves
-  uint8_t* ql_s = q_s + kMq * HD * 2;                     // remainder of Q, same layout
-  uint8_t* bk_s = ql_s + kMq * HD * 2;                    // block K [16][HD]
+  uint8_t* q_s = smem + kStages * kStageBytes;            // fp16 [kMq][HD] swizzled halves
+  uint8_t* bk_s = q_s + kMq * HD * 2;                     // block K, fp16 [16][HD]
   uint8_t* bv_s = bk_s + kBlkKeys * HD * 2;               // block V [16][HD]
   float* part_s = reinterpret_cast<float*>(smem);         // after the loop: [kMq][HD] partial O
   float* ml_s = part_s + kMq * HD;                        // [kMq][2] running max (log2) and sum
@@ -318,8 +338,6 @@ __global__ void __launch_bounds__((MT + 1) * 32)
       const int col = ch * 8;
       const uint32_t off = (col >> 6) * (kMq * 128) + swz(ri, col & 63);
       cp_async16(q_s + off, a.qkv + src, ok);
-      const size_t src_lo = (size_t)(b * a.gamma + i) * a.ld_q_lo + (size_t)(g * group + hh) * HD + ch * 8;
-      cp_async16(ql_s + off, a.q_lo ? a.q_lo + src_lo : a.qkv + src, ok && a.q_lo);
     }
     if (do_block) {
       const size_t kcol = (size_t)a.n_q * HD + (size_t)g * HD;
@@ -327,7 +345,7 @@ __global__ void __launch_bounds__((MT + 1) * 32)
       for (int idx = ctid; idx < kBlkKeys * (HD / 8); idx += kConsumers) {
         const int r = idx / (HD / 8), ch = idx % (HD / 8);
         const bool ok = r < a.gamma;
-        const __nv_bfloat16* row = a.qkv + (size_t)(b * a.gamma + (ok ? r : 0)) * a.ld_qkv;
+        const __half* row = a.qkv + (size_t)(b * a.gamma + (ok ? r : 0)) * a.ld_qkv;
         const int col = ch * 8;
         const uint32_t off = (col >> 6) * (kBlkKeys * 128) + swz(r, col & 63);
         cp_async16(bk_s + off, row + kcol + ch * 8, ok);
@@ -346,8 +364,6 @@ __global__ void __launch_bounds__((MT + 1) * 32)
         const int col = kk * 16 + ((lane >> 4) << 3);
         ldsm_x4(qb + (col >> 6) * (kMq * 128) + swz(row, col & 63), st.qa[kk][0], st.qa[kk][1],
                 st.qa[kk][2], st.qa[kk][3]);
-        ldsm_x4(qb + kMq * HD * 2 + (col >> 6) * (kMq * 128) + swz(row, col & 63), st.ql[kk][0],
-                st.ql[kk][1], st.ql[kk][2], st.ql[kk][3]);
       }
     }
 #pragma unroll
@@ -355,13 +371,8 @@ __global__ void __launch_bounds__((MT + 1) * 32)
     st.m[0] = st.m[1] = -INFINITY;
     st.l[0] = st.l[1] = 0.0f;
 
-    const bool qlo = a.q_lo != nullptr;
-    if (do_block) {
-      if (qlo)
-        process_tile<HD, kBlkKeys, true>(st, smem_u32(bk_s), smem_u32(bv_s), a.gamma, a.scale_log2);
-      else
-        process_tile<HD, kBlkKeys, false>(st, smem_u32(bk_s), smem_u32(bv_s), a.gamma, a.scale_log2);
-    }
+    if (do_block)
+      process_tile<HD, kBlkKeys, false>(st, smem_u32(bk_s), smem_u32(bv_s), a.gamma, a.scale_log2);
     for (int i = 0; i < nt; ++i) {
       const int s = i % kStages;
       const uint32_t ph = (uint32_t)(i / kStages) & 1u;
@@ -370,10 +381,7 @@ __global__ void __launch_bounds__((MT + 1) * 32)
       uint8_t* vs = ks + kTileBytes;
       const int slot0 = (t0 + i) * kKeys;
       const int valid = n_valid - slot0 < kKeys ? n_valid - slot0 : kKeys;
-      if (qlo)
-        process_tile<HD, kKeys, true>(st, smem_u32(ks), smem_u32(vs), valid, a.scale_log2);
-      else
-        process_tile<HD, kKeys, false>(st, smem_u32(ks), smem_u32(vs), valid, a.scale_log2);
+      process_tile<HD, kKeys, true>(st, smem_u32(ks), smem_u32(vs), valid, a.scale_log2);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[s]);
     }
@@ -398,7 +406,7 @@ __global__ void __launch_bounds__((MT + 1) * 32)
 #pragma unroll
           for (int t = 0; t < WarpState<HD>::NT; ++t) {
             const int d = t * 8 + ((lane & 3) << 1);
-            store_pair2(a.out, a.out_lo, off + d, st.o[t][2 * h] * inv, st.o[t][2 * h + 1] * inv);
+            store_h2(a.out, off + d, st.o[t][2 * h] * inv, st.o[t][2 * h + 1] * inv);
           }
         }
       }
@@ -473,8 +481,7 @@ __global__ void __launch_bounds__((MT + 1) * 32)
       }
     }
     const int hh = ri / a.gamma, i = ri % a.gamma;
-    store_pair2(a.out, a.out_lo,
-                (size_t)(b * a.gamma + i) * a.ld_out + (size_t)(g * group + hh) * HD + d, o0, o1);
+    store_h2(a.out, (size_t)(b * a.gamma + i) * a.ld_out + (size_t)(g * group + hh) * HD + d, o0, o1);
   }
   // no CTA may leave while another still reads its shared memory
   cluster.sync();
@@ -482,7 +489,7 @@ __global__ void __launch_bounds__((MT + 1) * 32)
 
 template <int HD, int MT>
 int launch_t(const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a, int B, cudaStream_t s) {
-  constexpr size_t smem = 1024 + (size_t)kStages * 2 * kKeys * HD * 2 + 2 * (size_t)MT * 16 * HD * 2 +
+  constexpr size_t smem = 1024 + (size_t)kStages * 2 * kKeys * HD * 2 + (size_t)MT * 16 * HD * 2 +
                           2 * 16 * HD * 2;
   auto kern = attn_kernel<HD, MT>;
   static bool attr = false;
@@ -546,9 +553,9 @@ int launch_attention(const void* ring_k_layer, const void* ring_v_layer, const A
                      cudaStream_t s) {
   CUtensorMap tk, tv;
   const uint64_t rows = (uint64_t)a.ring_batch * a.n_kv * a.window;
-  int rc = encode_bf16_2d(&tk, ring_k_layer, (uint64_t)a.hd, rows, 64, kKeys);
+  int rc = encode_2d(&tk, ring_k_layer, OPND_BF16, (uint64_t)a.hd, rows, 64, kKeys);
   if (rc) return rc;
-  rc = encode_bf16_2d(&tv, ring_v_layer, (uint64_t)a.hd, rows, 64, kKeys);
+  rc = encode_2d(&tv, ring_v_layer, OPND_BF16, (uint64_t)a.hd, rows, 64, kKeys);
   if (rc) return rc;
   const int mt = attn_row_tiles(a.n_q, a.n_kv, a.gamma);
   if (a.hd == 128) {

@@ -2,18 +2,16 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace dfl {
 
 struct AttnArgs {
-  const __nv_bfloat16* qkv;  // [B*gamma, (Hq + 2 Hkv) hd]: rotated q, rotated k, v
+  const __half* qkv;         // fp16 [B*gamma, (Hq + 2 Hkv) hd]: rotated q, rotated k, v
   long long ld_qkv;
-  const __nv_bfloat16* q_lo; // [B*gamma, Hq hd] bf16 remainders of the rotated queries (or null)
-  long long ld_q_lo;
-  __nv_bfloat16* out;        // [B*gamma, Hq hd]
-  __nv_bfloat16* out_lo;     // bf16 remainders of the output (or null)
+  __half* out;               // fp16 [B*gamma, Hq hd]
   long long ld_out;
   const int64_t* ctx_len;    // [B] context lengths L
   const int32_t* req_slot;   // [B] ring rows or nullptr

@@ -6,6 +6,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -300,8 +301,9 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate.
-__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+// D[tmem] (+)= A[smem] * B[smem]^T, 16-bit inputs (fp16 or bf16, as the
+// instruction descriptor says), fp32 accumulate.
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -348,13 +350,23 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t smem_addr) {
   return d;
 }
 
-// Instruction descriptor: kind::f16, A = B = bf16, D = fp32, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+// Instruction descriptor: kind::f16, D = fp32, both operands K-major and of
+// one type: bf16 (format code 1) when `bf16`, else fp16 (format code 0).
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool bf16) {
   return (1u << 4)                          // D format fp32
-         | (1u << 7)                        // A format bf16
-         | (1u << 10)                       // B format bf16
+         | ((bf16 ? 1u : 0u) << 7)          // A format
+         | ((bf16 ? 1u : 0u) << 10)         // B format
          | ((uint32_t)(N >> 3) << 17)       // N / 8
          | ((uint32_t)(M >> 4) << 24);      // M / 16
+}
+
+// Largest finite fp16 value.  Activations written as fp16 are checked
+// against it (DFLASH_ERR_RANGE) instead of silently becoming infinite.
+constexpr float kF16Max = 65504.0f;
+
+__device__ __forceinline__ __half to_f16_checked(float y, int* status) {
+  if (!(fabsf(y) <= kF16Max)) report_status(status, DFLASH_ERR_RANGE);
+  return __float2half_rn(y);
 }
 
 // ------------------------------------------------------ PDL (grid control)

@@ -4,9 +4,11 @@
 // per-layer context K/V projections) is Y[tokens, rows] = X[tokens, K] W[rows,
 // K]^T with few tokens (8 at batch 1) and many weight rows.  The kernel is
 // therefore "swap-AB": the weight tile is the 128-row A operand of
-// tcgen05.mma, the tokens are the N side (16..128 columns), and the fp32
+// tcgen05.mma, the tokens are the N side (16..256 columns), and the fp32
 // accumulator lives in tensor memory as 128 lanes (weight rows) x BN columns
-// (tokens).
+// (tokens).  Operands are fp16 (the drafter's matrices re-encoded exactly,
+// activations rounded to 11 significant bits) or bf16 (W_c with the target's
+// bf16 features); kind::f16 takes both, A and B of one type.
 //
 // Pipeline (one CTA = 4 warps):
 //   warp 0 lane 0   TMA producer: 128x64 weight box + BNx64 token box per
@@ -16,11 +18,12 @@
 //   all 4 warps     epilogue: tcgen05.ld of their 32-lane quarter, then the
 //                   fused epilogue of the layer (RoPE, residual add, SwiGLU,
 //                   fp32 logits, or scatter into the context ring).
-// Split-K: the grid's z dimension partitions K and the splits of one tile run
-// as a thread-block cluster; each split keeps its fp32 partial tile in shared
-// memory and, after a cluster barrier, every CTA of the cluster sums a
-// disjoint subset of the tile's tokens over distributed shared memory (in
-// split order — deterministic) and runs the epilogue on it.
+// Split-K: the grid's z dimension partitions K.  The splits of one tile
+// either run as a thread-block cluster (each keeps its fp32 partial tile in
+// shared memory and, after a cluster barrier, every CTA of the cluster sums a
+// disjoint subset of the tile's tokens over distributed shared memory, in
+// split order — deterministic) or store their partials in global memory, the
+// last to arrive summing them in split order.
 // All waits are bounded (see mbar_wait_bounded).
 #include <cooperative_groups.h>
 #include <cudaTypedefs.h>
@@ -37,7 +40,7 @@ namespace {
 namespace cg = cooperative_groups;
 
 constexpr int kThreads = 128;
-constexpr int kBK = 64;                   // K elements per stage (128 bytes of bf16)
+constexpr int kBK = 64;                   // K elements per stage (128 bytes of 16-bit values)
 constexpr int kABytes = 128 * kBK * 2;    // weight box per stage
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
@@ -76,11 +79,8 @@ __device__ __forceinline__ float rope_apply(float x, float partner, const RopeRo
   return rr.first_half ? fmaf(x, c, -partner * s) : fmaf(x, c, partner * s);
 }
 
-__device__ __forceinline__ void store_bf16_pair(const GemmEpi& e, size_t o_hi, size_t o_lo, float y) {
-  const __nv_bfloat16 hi = __float2bfloat16_rn(y);
-  static_cast<__nv_bfloat16*>(e.out)[o_hi] = hi;
-  if (e.out_lo)
-    static_cast<__nv_bfloat16*>(e.out_lo)[o_lo] = __float2bfloat16_rn(y - __bfloat162float(hi));
+__device__ __forceinline__ void store_f16(const GemmEpi& e, size_t o, float y) {
+  static_cast<__half*>(e.out)[o] = to_f16_checked(y, e.status);
 }
 
 // Epilogue of up to 16 tokens of this thread's row: v[j] is token
@@ -105,7 +105,7 @@ __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const floa
     for (int j = 0; j < 16; ++j) xchg[j * 128 + r] = v[j];
     epi_sync(kNamed);
   }
-  if (kind == EPI_F32 || kind == EPI_BF16 || kind == EPI_RESID) {
+  if (kind == EPI_F32 || kind == EPI_F16 || kind == EPI_RESID) {
     const int n = tile_n * 128 + r;
     if (n < e.N) {
 #pragma unroll
@@ -115,8 +115,8 @@ __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const floa
           const size_t o = (size_t)tok * e.ld + n;
           if (kind == EPI_F32)
             static_cast<float*>(e.out)[o] = v[j];
-          else if (kind == EPI_BF16)
-            store_bf16_pair(e, o, (size_t)tok * e.ld_lo + n, v[j]);
+          else if (kind == EPI_F16)
+            store_f16(e, o, v[j]);
           else
             static_cast<float*>(e.out)[o] += v[j];
         }
@@ -138,11 +138,7 @@ __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const floa
             const float pos = (float)(e.ctx_len[tok / e.gamma] + tok % e.gamma);
             y = rope_apply(v[j], xchg[j * 128 + pr], rr, pos);
           }
-          const __nv_bfloat16 hi = __float2bfloat16_rn(y);
-          static_cast<__nv_bfloat16*>(e.out)[(size_t)tok * e.ld + n] = hi;
-          if (e.out_lo && n < e.lo_cols)
-            static_cast<__nv_bfloat16*>(e.out_lo)[(size_t)tok * e.ld_lo + n] =
-                __float2bfloat16_rn(y - __bfloat162float(hi));
+          store_f16(e, (size_t)tok * e.ld + n, y);
         }
       }
     }
@@ -154,7 +150,7 @@ __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const floa
         const int tok = tok_base + j * tok_step;
         if (j < ntok && tok < e.M) {
           const float g = v[j], u = xchg[j * 128 + r + 64];
-          store_bf16_pair(e, (size_t)tok * e.ld + f, (size_t)tok * e.ld_lo + f, silu(g) * u);
+          store_f16(e, (size_t)tok * e.ld + f, silu(g) * u);
         }
       }
     }
@@ -181,6 +177,8 @@ __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const floa
           }
           float y = v[j];
           if (kv == 0) y = rope_apply(v[j], xchg[j * 128 + pr], rr, (float)pos);
+          // the attention kernel reads ring entries as fp16
+          if (!(fabsf(y) <= kF16Max)) report_status(e.status, DFLASH_ERR_RANGE);
           const size_t o =
               ((((size_t)layer * e.ring_batch + slot_b) * e.n_kv + g) * e.window + (size_t)(pos % e.window)) *
                   e.hd + d;
@@ -194,7 +192,7 @@ __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const floa
 
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_bf16_tc_kernel(const __grid_constant__ GemmAMaps A, const __grid_constant__ CUtensorMap tmB,
+    gemm_tc_kernel(const __grid_constant__ GemmAMaps A, const __grid_constant__ CUtensorMap tmB,
                         const GemmAOpts ao, const GemmArgs args, const GemmEpi epi) {
   constexpr int kBBytes = BN * kBK * 2;
   constexpr int kStage = kABytes + kBBytes;
@@ -256,8 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       map_i = tile_n / ao.tiles_per_map;
       row0 = ao.row_offset + (tile_n % ao.tiles_per_map) * 128;
     }
-    const int T = ao.split ? BN / 2 : BN;  // tokens per tile
-    const int tok0 = tile_m * T;
+    const int tok0 = tile_m * BN;
     // weights do not depend on the previous kernel: start streaming them
     // before waiting for it (programmatic dependent launch)
     const int pre = nkb < STAGES ? nkb : STAGES;
@@ -273,11 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     grid_dependency_wait();
-    for (int i = 0; i < pre; ++i) {
-      uint8_t* sb = smem + i * kStage + kABytes;
-      tma_load_2d(sb, &tmB, &full_bar[i], (kb0 + i) * kBK, tok0, pol_x);
-      if (ao.split) tma_load_2d(sb + T * 128, &tmB, &full_bar[i], (kb0 + i) * kBK, epi.M + tok0, pol_x);
-    }
+    for (int i = 0; i < pre; ++i)
+      tma_load_2d(smem + i * kStage + kABytes, &tmB, &full_bar[i], (kb0 + i) * kBK, tok0, pol_x);
     issued = pre;
     for (int i = pre; i < nkb; ++i) {
       const int s = i % STAGES;
@@ -293,12 +287,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sa, &A.map[map_i], &full_bar[s], kc, row0, pol_w);
       }
       tma_load_2d(sa + kABytes, &tmB, &full_bar[s], kc, tok0, pol_x);
-      if (ao.split) tma_load_2d(sa + kABytes + T * 128, &tmB, &full_bar[s], kc, epi.M + tok0, pol_x);
       issued = i + 1;
     }
   } else if (warp == 1 && lane == 0) {
     // --------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
+    const uint32_t idesc = idesc_f32acc(128, BN, args.type == OPND_BF16);
     for (int i = 0; i < nkb; ++i) {
       const int s = i % STAGES;
       const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
@@ -308,8 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t b_addr = a_addr + kABytes;
 #pragma unroll
       for (int k = 0; k < kBK / 16; ++k)
-        tc_mma_bf16(tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), idesc,
-                    (i | k) ? 1u : 0u);
+        tc_mma_f16(tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), idesc,
+                   (i | k) ? 1u : 0u);
       tc_commit(&empty_bar[s]);
     }
     tc_commit(&acc_bar);
@@ -332,32 +325,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* xchg = reinterpret_cast<float*>(smem);
   const bool aborted = abort_sh != 0 || !acc_ok;
 
-  // tokens per tile; with split operands column j (hi) pairs with column T + j (lo)
-  const int T = ao.split ? BN / 2 : BN;
-  const int ntok = T < 16 ? T : 16;
-  const int n_chunks = (T + 15) / 16;
+  constexpr int T = BN;  // tokens per tile
+  constexpr int ntok = 16;
+  constexpr int n_chunks = T / 16;
   auto load_chunk = [&](int c, float (&v)[16]) {
     uint32_t raw[16];
-    if (!ao.split) {
-      tmem_ld_x16(t_row + c * 16, raw);
-      tc_wait_ld();
+    tmem_ld_x16(t_row + c * 16, raw);
+    tc_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]);
-    } else if (T >= 16) {
-      uint32_t lo[16];
-      tmem_ld_x16(t_row + c * 16, raw);
-      tmem_ld_x16(t_row + T + c * 16, lo);
-      tc_wait_ld();
-#pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]) + __uint_as_float(lo[j]);
-    } else {
-      tmem_ld_x16(t_row, raw);
-      tc_wait_ld();
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(raw[j]) + __uint_as_float(raw[j + 8]);
-#pragma unroll
-      for (int j = 8; j < 16; ++j) v[j] = 0.0f;
-    }
+    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]);
   };
 
   if (args.splits == 1) {
@@ -464,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // the mainloop of the next.
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(192, 1)
-    gemm_bf16_tc_persistent_kernel(const __grid_constant__ GemmAMaps A,
+    gemm_tc_persistent_kernel(const __grid_constant__ GemmAMaps A,
                                    const __grid_constant__ CUtensorMap tmB, const GemmAOpts ao,
                                    const GemmArgs args, const GemmEpi epi, int n_tiles, int m_tiles) {
   constexpr int kBBytes = BN * kBK * 2;
@@ -484,7 +460,7 @@ __global__ void __launch_bounds__(192, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* xchg = reinterpret_cast<float*>(smem + STAGES * kStage);
-  const int T = ao.split ? BN / 2 : BN;
+  constexpr int T = BN;
   const int kb_total = (args.K + kBK - 1) / kBK;
   const int total = n_tiles * m_tiles;
 
@@ -549,7 +525,6 @@ __global__ void __launch_bounds__(192, 1)
             waited = true;
           }
           tma_load_2d(sa + kABytes, &tmB, &full_bar[s], kc, tok0, pol_x);
-          if (ao.split) tma_load_2d(sa + kABytes + T * 128, &tmB, &full_bar[s], kc, epi.M + tok0, pol_x);
         }
       }
       if (abort_sh) {
@@ -562,7 +537,7 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
+      const uint32_t idesc = idesc_f32acc(128, BN, args.type == OPND_BF16);
       int it = 0, lt = 0;
       for (int t = blockIdx.x; t < total && !abort_sh; t += gridDim.x, ++lt) {
         const int buf = lt & 1;
@@ -579,8 +554,8 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t b_addr = a_addr + kABytes;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
-            tc_mma_bf16(d, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), idesc,
-                        (kb | k) ? 1u : 0u);
+            tc_mma_f16(d, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), idesc,
+                       (kb | k) ? 1u : 0u);
           tc_commit(&empty_bar[s]);
         }
         tc_commit(&accf_bar[buf]);
@@ -590,8 +565,8 @@ __global__ void __launch_bounds__(192, 1)
     // --------------------------------------------------------- epilogue
     const int r = 32 * (warp & 3) + lane;  // TMEM lane quarter of this warp
     const uint32_t t_row = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-    const int ntok = T < 16 ? T : 16;
-    const int n_chunks = (T + 15) / 16;
+    constexpr int ntok = 16;
+    constexpr int n_chunks = T / 16;
     int lt = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
       const int tile_m = t % m_tiles, tile_n = t / m_tiles;
@@ -606,19 +581,10 @@ __global__ void __launch_bounds__(192, 1)
       for (int c = 0; c < n_chunks; ++c) {
         float v[16];
         uint32_t raw[16];
-        if (!ao.split) {
-          tmem_ld_x16(base + c * 16, raw);
-          tc_wait_ld();
+        tmem_ld_x16(base + c * 16, raw);
+        tc_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]);
-        } else {
-          uint32_t lo[16];
-          tmem_ld_x16(base + c * 16, raw);
-          tmem_ld_x16(base + T + c * 16, lo);
-          tc_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]) + __uint_as_float(lo[j]);
-        }
+        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]);
         if (c == n_chunks - 1) {
           // every column of this accumulator is in registers: hand it back
           tc_fence_before();
@@ -647,7 +613,7 @@ constexpr size_t smem_bytes() {
 template <int BN, int STAGES>
 int launch_one(const GemmAMaps& A, const CUtensorMap& tmB, const GemmAOpts& ao, const GemmArgs& args,
                const GemmEpi& epi, dim3 grid, cudaStream_t s, bool pdl) {
-  auto kern = gemm_bf16_tc_kernel<BN, STAGES>;
+  auto kern = gemm_tc_kernel<BN, STAGES>;
   constexpr size_t smem = smem_bytes<BN, STAGES>();
   static bool attr_set = false;
   if (!attr_set) {
@@ -687,7 +653,7 @@ template <int BN, int STAGES>
 int launch_persistent(const GemmAMaps& A, const CUtensorMap& tmB, const GemmAOpts& ao,
                       const GemmArgs& args, const GemmEpi& epi, int n_tiles, int m_tiles,
                       int num_sms, cudaStream_t s, bool pdl) {
-  auto kern = gemm_bf16_tc_persistent_kernel<BN, STAGES>;
+  auto kern = gemm_tc_persistent_kernel<BN, STAGES>;
   constexpr size_t smem = (size_t)STAGES * (kABytes + BN * kBK * 2) + 16 * 128 * 4 + 1024;
   static bool attr_set = false;
   if (!attr_set) {
@@ -714,8 +680,8 @@ int launch_persistent(const GemmAMaps& A, const CUtensorMap& tmB, const GemmAOpt
 
 }  // namespace
 
-int encode_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
-                   uint32_t box_inner, uint32_t box_outer) {
+int encode_2d(CUtensorMap* map, const void* ptr, int type, uint64_t inner, uint64_t outer,
+              uint32_t box_inner, uint32_t box_outer) {
   std::call_once(g_encode_once, [] {
     cudaDriverEntryPointQueryResult q;
     void* fn = nullptr;
@@ -730,7 +696,9 @@ int encode_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t o
   cuuint64_t strides[1] = {inner * 2};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+  const CUtensorMapDataType dt =
+      type == OPND_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = g_encode(map, dt, 2, const_cast<void*>(ptr), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -739,6 +707,7 @@ int encode_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t o
 
 int gemm_token_tile(int M) {
   if (M <= 16) return 16;
+  if (M <= 32) return 32;
   if (M <= 64) return 64;
   if (M <= 128) return 128;
   return 256;
@@ -755,20 +724,20 @@ int gemm_plan_splits(int tiles, int K, int target_ctas) {
   return s;
 }
 
-int launch_gemm(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void* x, int M, int K,
-                const GemmEpi& epi, const GemmScratch& scratch, int splits, cudaStream_t s,
-                bool pdl) {
-  const int BN = gemm_token_tile(ao.split ? 2 * M : M);
-  const int T = ao.split ? BN / 2 : BN;
+int launch_gemm(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void* x, int type,
+                int M, int K, const GemmEpi& epi, const GemmScratch& scratch, int splits,
+                cudaStream_t s, bool pdl) {
+  const int BN = gemm_token_tile(M);
+  const int T = BN;
   CUtensorMap tmB;
-  int rc = encode_bf16_2d(&tmB, x, (uint64_t)K, (uint64_t)(ao.split ? 2 * M : M), kBK, (uint32_t)T);
+  int rc = encode_2d(&tmB, x, type, (uint64_t)K, (uint64_t)M, kBK, (uint32_t)T);
   if (rc) return rc;
   const int m_tiles = (M + T - 1) / T;
   const int kb = (K + kBK - 1) / kBK;
   if (splits < 1) splits = 1;
   if (splits > kb) splits = kb;
   const size_t tiles = (size_t)n_tiles * m_tiles;
-  const size_t per_split = (size_t)((T + 15) / 16) * 16 * 128;
+  const size_t per_split = (size_t)T * 128;
   // Measured on GB300: with small token tiles (8-16 tokens, partials of
   // 4-8 KiB) the ticketed reduction wins — non-last splits leave at once;
   // with 32+ token tiles the partials are large and the cluster reduction
@@ -780,6 +749,7 @@ int launch_gemm(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void
   }
   GemmArgs args;
   args.K = K;
+  args.type = type;
   args.splits = splits;
   args.cluster = cluster ? 1 : 0;
   args.partial = scratch.partial;
@@ -793,6 +763,7 @@ int launch_gemm(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void
   dim3 grid(n_tiles, m_tiles, splits);
   switch (BN) {
     case 16: return launch_one<16, 6>(A, tmB, ao, args, epi, grid, s, pdl);
+    case 32: return launch_one<32, 5>(A, tmB, ao, args, epi, grid, s, pdl);
     case 64: return launch_one<64, 4>(A, tmB, ao, args, epi, grid, s, pdl);
     case 128: return launch_one<128, 6>(A, tmB, ao, args, epi, grid, s, pdl);
     default: return launch_one<256, 4>(A, tmB, ao, args, epi, grid, s, pdl);

@@ -15,23 +15,20 @@ namespace {
 
 constexpr int kNormThreads = 256;
 
-// y as a bf16 pair: hi = bf16(y) and lo = bf16(y - hi), so that hi + lo
-// carries y to about 16 bits for the split-operand GEMMs.
-__device__ __forceinline__ void store_pair(__nv_bfloat16* hi, __nv_bfloat16* lo, size_t o, float y) {
-  const __nv_bfloat16 h = __float2bfloat16_rn(y);
-  hi[o] = h;
-  if (lo) lo[o] = __float2bfloat16_rn(y - __bfloat162float(h));
+// Two adjacent GEMM operand values as fp16 (range-checked).
+__device__ __forceinline__ void store_h2(__half* out, size_t o, float y0, float y1, int* status) {
+  *reinterpret_cast<__half2*>(out + o) =
+      __halves2half2(to_f16_checked(y0, status), to_f16_checked(y1, status));
 }
 
 // One CTA per block row m = b * gamma + i: x[m] = embed[id] (fp32 residual
-// stream), h[m] = RMSNorm(x[m]) * g as a bf16 pair (h_lo may be null),
-// id = anchor[b] for i = 0, MASK after.  The row is staged in shared memory
+// stream), h[m] = RMSNorm(x[m]) * g in fp16, id = anchor[b] for i = 0, MASK
+// after.  The row is staged in shared memory
 // (dynamic, 4 d bytes) with 16-byte loads issued together.
 __global__ void __launch_bounds__(kNormThreads)
     embed_norm_kernel(const __nv_bfloat16* __restrict__ embed, const int32_t* __restrict__ anchor,
                       int gamma, int mask_id, int vocab, int d, const float* __restrict__ g, float eps,
-                      float* __restrict__ x, __nv_bfloat16* __restrict__ h,
-                      __nv_bfloat16* __restrict__ h_lo, int* status) {
+                      float* __restrict__ x, __half* __restrict__ h, int* status) {
   pdl_enter();
   extern __shared__ float row_s[];
   __shared__ float red[33];
@@ -57,21 +54,21 @@ __global__ void __launch_bounds__(kNormThreads)
   }
   ss = block_sum(ss, red);
   const float rs = rsqrtf(ss / (float)d + eps);
-  for (int c = threadIdx.x; c < d; c += kNormThreads) {
-    const float v = row_s[c];
-    x[(size_t)m * d + c] = v;
-    store_pair(h, h_lo, (size_t)m * d + c, v * rs * g[c]);
+  for (int c = threadIdx.x; c < d / 2; c += kNormThreads) {
+    const float2 v = reinterpret_cast<const float2*>(row_s)[c];
+    const float2 gg = reinterpret_cast<const float2*>(g)[c];
+    reinterpret_cast<float2*>(x + (size_t)m * d)[c] = v;
+    store_h2(h, (size_t)m * d + 2 * c, v.x * rs * gg.x, v.y * rs * gg.y, status);
   }
 }
 
-// out row r = RMSNorm(x[src(r)]) * g as a bf16 pair (out_lo may be null).
+// out row r = RMSNorm(x[src(r)]) * g in fp16.
 // gather_gamma = 0: src(r) = r; otherwise the MASK rows:
 // src(r) = (r / (G - 1)) * G + r % (G - 1) + 1.  The row is staged in
 // shared memory (dynamic, 4 d bytes) with 16-byte loads issued together.
 __global__ void __launch_bounds__(kNormThreads)
     rmsnorm_kernel(const float* __restrict__ x, int d, const float* __restrict__ g, float eps,
-                   int gather_gamma, __nv_bfloat16* __restrict__ out,
-                   __nv_bfloat16* __restrict__ out_lo) {
+                   int gather_gamma, __half* __restrict__ out, int* status) {
   pdl_enter();
   extern __shared__ float row_s[];
   __shared__ float red[33];
@@ -88,8 +85,35 @@ __global__ void __launch_bounds__(kNormThreads)
   }
   ss = block_sum(ss, red);
   const float rs = rsqrtf(ss / (float)d + eps);
-  for (int c = threadIdx.x; c < d; c += kNormThreads)
-    store_pair(out, out_lo, (size_t)r * d + c, row_s[c] * rs * g[c]);
+  for (int c = threadIdx.x; c < d / 2; c += kNormThreads) {
+    const float2 v = reinterpret_cast<const float2*>(row_s)[c];
+    const float2 gg = reinterpret_cast<const float2*>(g)[c];
+    store_h2(out, (size_t)r * d + 2 * c, v.x * rs * gg.x, v.y * rs * gg.y, status);
+  }
+}
+
+// dst = fp16(src) for a bf16 array of n8 * 8 elements (16-byte aligned);
+// *flag = 1 if an element is NaN or beyond the fp16 range (+-65504).  Every
+// other bf16 value is exactly an fp16 value, or (below 2^-14) rounds to an
+// fp16 subnormal within 2^-25.
+__global__ void __launch_bounds__(256)
+    to_f16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t n8, int* flag) {
+  bool bad = false;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const uint4 u = __ldg(src + i);
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+    uint4 o;
+    __half2* h = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(b[k]);
+      bad |= !(fabsf(f.x) <= kF16Max) || !(fabsf(f.y) <= kF16Max);
+      h[k] = __floats2half2_rn(f.x, f.y);
+    }
+    dst[i] = o;
+  }
+  if (bad) atomicExch(flag, 1);
 }
 
 // ------------------------------------------------------ top-k and LSE
@@ -256,18 +280,30 @@ __global__ void add_lengths_kernel(int B, const int32_t* __restrict__ n_new, int
 }  // namespace
 
 int launch_embed_norm(const void* embed, const int32_t* anchor, int B, int gamma, int mask_id,
-                      int vocab, int d, const float* g, float eps, float* x, void* h, void* h_lo,
-                      int* status, cudaStream_t s) {
+                      int vocab, int d, const float* g, float eps, float* x, void* h, int* status,
+                      cudaStream_t s) {
   return launch_pdl(embed_norm_kernel, dim3(B * gamma), dim3(kNormThreads), (size_t)d * 4, s,
                     static_cast<const __nv_bfloat16*>(embed), anchor, gamma, mask_id, vocab, d, g, eps,
-                    x, static_cast<__nv_bfloat16*>(h), static_cast<__nv_bfloat16*>(h_lo), status);
+                    x, static_cast<__half*>(h), status);
 }
 
 int launch_rmsnorm(const float* x, int rows, int d, const float* g, float eps, int gather_gamma,
-                   void* out, void* out_lo, cudaStream_t s) {
+                   void* out, int* status, cudaStream_t s) {
   return launch_pdl(rmsnorm_kernel, dim3(rows), dim3(kNormThreads), (size_t)d * 4, s, x, d, g, eps,
-                    gather_gamma,
-                    static_cast<__nv_bfloat16*>(out), static_cast<__nv_bfloat16*>(out_lo));
+                    gather_gamma, static_cast<__half*>(out), status);
+}
+
+int launch_to_f16(const void* src, void* dst, size_t n, int* flag, int grid, cudaStream_t s) {
+  if (n % 8 || (reinterpret_cast<uintptr_t>(src) & 15) || (reinterpret_cast<uintptr_t>(dst) & 15))
+    return DFLASH_ERR_ALIGN;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  return cudaLaunchKernelEx(&cfg, to_f16_kernel, static_cast<const uint4*>(src), static_cast<uint4*>(dst),
+                            n / 8, flag) == cudaSuccess
+             ? DFLASH_OK
+             : DFLASH_ERR_LAUNCH;
 }
 
 int topk_slots(int k) { return k <= 4 ? 4 : 16; }

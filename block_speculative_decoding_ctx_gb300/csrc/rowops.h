@@ -8,12 +8,16 @@
 
 namespace dfl {
 
+// x: fp32 [B gamma, d] residual stream; h: fp16 [B gamma, d]
 int launch_embed_norm(const void* embed, const int32_t* anchor, int B, int gamma, int mask_id,
-                      int vocab, int d, const float* g, float eps, float* x, void* h, void* h_lo,
-                      int* status, cudaStream_t s);
-// out (and out_lo, the bf16 remainder, when not null): [rows, d]
+                      int vocab, int d, const float* g, float eps, float* x, void* h, int* status,
+                      cudaStream_t s);
+// out: fp16 [rows, d]; status receives DFLASH_ERR_RANGE for values beyond fp16
 int launch_rmsnorm(const float* x, int rows, int d, const float* g, float eps, int gather_gamma,
-                   void* out, void* out_lo, cudaStream_t s);
+                   void* out, int* status, cudaStream_t s);
+// dst (fp16) = src (bf16), n elements (a multiple of 8, 16-byte aligned
+// pointers); *flag = 1 if a value is NaN or beyond the fp16 range.
+int launch_to_f16(const void* src, void* dst, size_t n, int* flag, int grid, cudaStream_t s);
 // Slots per row and chunk of the top-k partials (4 or 16).
 int topk_slots(int k);
 int launch_topk_lse(const float* logits, int rows, int V, int k, unsigned long long* part_keys,

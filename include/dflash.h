@@ -38,11 +38,23 @@
  *     evaluated exactly; every draw is an integer inverse CDF over
  *     floor(weight * 2^45).
  *
+ * Arithmetic.  The drafter's matrices arrive as bf16.  dflash_create copies
+ * the five matrices of every layer and the LM head into one fp16 buffer of the
+ * handle: every bf16 value of magnitude 2^-14 .. 65504 is exactly an fp16
+ * value, and smaller ones keep an absolute error below 2^-25.  Every
+ * contraction of the draft pass then runs on fp16 operands with fp32
+ * accumulation, and the activations between kernels are stored as fp16:
+ * 11 significant bits where bf16 keeps 8, at the same tensor-core rate.  An
+ * activation beyond the fp16 range sets DFLASH_ERR_RANGE in the workspace
+ * status word.  W_c and the target features stay bf16 (the features are
+ * bf16 as given), and so does the context K/V ring.
+ *
  * Memory and ownership.  Every pointer argument, unless it says "host", is
- * device memory owned by the caller.  The handle holds only host metadata
- * (sizes and TMA descriptors of the caller's weights); no call allocates
- * device memory.  Calls are asynchronous on the given stream, never
- * synchronise the host, and may be captured into a CUDA graph.
+ * device memory owned by the caller.  dflash_create allocates the handle's
+ * fp16 matrix copy (2 bytes per element of those matrices; dflash_destroy
+ * frees it); no other call allocates device memory.  Calls other than
+ * create/destroy are asynchronous on the given stream, never synchronise the
+ * host, and may be captured into a CUDA graph.
  *
  * Workspace.  draft_block, ctx_append, probs and verify take a caller-owned
  * device workspace of at least the size the matching *_workspace_bytes
@@ -78,7 +90,9 @@ enum {
   DFLASH_ERR_LAUNCH = -5,         /* a kernel launch failed */
   DFLASH_ERR_DEVICE_TIMEOUT = -6, /* device status: a bounded wait gave up */
   DFLASH_ERR_WORKSPACE = -7,      /* workspace missing or too small */
-  DFLASH_ERR_CUDA = -8            /* a CUDA runtime / driver call failed */
+  DFLASH_ERR_CUDA = -8,           /* a CUDA runtime / driver call failed */
+  DFLASH_ERR_RANGE = -9           /* a weight or (device status) an activation is beyond
+                                     the fp16 range */
 };
 
 enum { DFLASH_VERIFY_GREEDY = 0, DFLASH_VERIFY_SAMPLED = 1 };
@@ -130,10 +144,15 @@ typedef struct dflash_weights {
 
 typedef struct dflash_handle dflash_handle;
 
-/* Validate cfg, record the weight pointers and encode their TMA descriptors.
- * The weights must stay alive and unchanged while the handle is used.
- * Must be called with the weights' device current.  Returns DFLASH_OK and
- * *out, or an error (then *out is NULL). */
+/* Validate cfg, copy w_qkv, w_o, w_gate, w_up, w_down of every layer and
+ * lm_head into the handle's fp16 buffer (allocated here; synchronises the
+ * device), record the other weight pointers and encode the TMA descriptors.
+ * embed, w_c and the gains are read from the caller's memory later: they
+ * must stay alive and unchanged while the handle is used; the copied
+ * matrices need not.  Must be called with the weights' device current.
+ * Returns DFLASH_OK and *out, or an error (then *out is NULL):
+ * DFLASH_ERR_RANGE if a copied matrix holds a value beyond +-65504 (or a
+ * NaN), DFLASH_ERR_CUDA if the buffer cannot be allocated. */
 int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_handle** out);
 int dflash_destroy(dflash_handle* h);
 

@@ -160,3 +160,27 @@ def test_host_validation_rejects_bad_draft_calls():
     with pytest.raises(dfl.DflashError) as e:
         dfl.dflash_draft_block(h, a, L, rk, rv, 8, ws, topk=17)
     assert e.value.code == -2
+
+
+def test_weights_beyond_fp16_range_are_rejected_at_create():
+    dims = synth.DIMS["small"]
+    W = synth.weights(dims, 95)
+    W["layers"][1]["w_down"][3, 7] = 1.0e5                    # bf16 holds it, fp16 does not
+    with pytest.raises(dfl.DflashError) as e:
+        dfl.dflash_create(tu.lib_cfg(dims, batch_max=1, gamma_max=4), tu.to_dev(W))
+    assert e.value.code == -9
+
+
+def test_activation_beyond_fp16_range_is_reported():
+    dims = synth.DIMS["small"]
+    W = synth.weights(dims, 96)
+    W["layers"][0]["g_mlp"] = W["layers"][0]["g_mlp"] * 1.0e5   # normed values ~N(0, 1e10)
+    h = dfl.dflash_create(tu.lib_cfg(dims, batch_max=1, gamma_max=4), tu.to_dev(W))
+    rk, rv = synth.ring(dims, 1, 97)
+    dev = torch.device("cuda")
+    ws = dfl.workspace(dfl.dflash_draft_workspace_bytes(h))
+    dfl.dflash_draft_block(h, torch.tensor([3], dtype=torch.int32, device=dev),
+                           torch.tensor([50], dtype=torch.int64, device=dev), rk.cuda(), rv.cuda(), 4,
+                           ws, out=dict(draft=torch.empty((1, 3), dtype=torch.int32, device=dev)))
+    torch.cuda.synchronize()
+    assert dfl.dflash_read_status(ws) == -9
