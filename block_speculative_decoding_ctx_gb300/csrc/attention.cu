@@ -8,8 +8,11 @@
 //
 // One CTA serves one (request, KV head, key split).  The group of query heads
 // that share the KV head times the gamma block positions (5 x 8 = 40 rows at
-// the full size) is packed into 16-row MMA tiles, one consumer warp per tile,
-// so every K/V byte read from HBM is used by all query heads of its group.
+// the full size) is packed into 16-row MMA tiles, so every K/V byte read from
+// HBM is used by all query heads of its group.  Each row tile has KW consumer
+// warps that take alternate key tiles (more warps in flight per SM: one warp's
+// chain of dependent MMAs, shuffles and exponentials leaves the SM idle) and
+// merge their softmax states at the end.
 // A producer warp streams 64-key K/V tiles of the context ring into shared
 // memory with TMA (128-byte swizzle, evict-first), STAGES deep.  Scores run
 // on mma.sync with fp16 operands (queries are fp16; ring keys, stored bf16,
@@ -42,7 +45,12 @@ namespace cg = cooperative_groups;
 #endif
 
 constexpr int kKeys = 64;      // keys per context tile
-constexpr int kStages = 3;
+
+// Stage buffers: each key-split group owns its own stages (2 each; 3 when
+// there is one group), so every consumer waits on its stages' phases in
+// order.  Key tile i goes to group i % KW, stage (i % KW) * SPG + (i / KW) % SPG.
+__host__ __device__ constexpr int attn_spg(int KW) { return KW == 1 ? 3 : 2; }
+__host__ __device__ constexpr int attn_stages(int KW) { return KW * attn_spg(KW); }
 
 // Byte offset of element (row, col) in a [rows][64] bf16 tile with the
 // 128-byte swizzle (16-byte chunk index XOR row % 8).
@@ -238,9 +246,10 @@ __device__ __forceinline__ void process_tile(WarpState<HD>& st, uint32_t k_base,
 
 // One CTA per (key split, KV head, request); the S splits of a (request, KV
 // head) form one thread-block cluster and merge their partial softmax states
-// through distributed shared memory.
-template <int HD, int MT>
-__global__ void __launch_bounds__((MT + 1) * 32)
+// through distributed shared memory.  Warp 0 produces; warp 1 + mt + MT * kw
+// is the consumer of row tile mt taking key tiles kw, kw + KW, ...
+template <int HD, int MT, int KW>
+__global__ void __launch_bounds__((MT * KW + 1) * 32)
     attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 const AttnArgs a) {
   pdl_enter();
@@ -248,7 +257,13 @@ __global__ void __launch_bounds__((MT + 1) * 32)
   constexpr int kStageBytes = 2 * kTileBytes;
   constexpr int kMq = MT * 16;
   constexpr int kBlkKeys = 16;
-  constexpr int kConsumers = MT * 32;
+  constexpr int kConsumers = MT * KW * 32;
+  constexpr int SPG = attn_spg(KW);
+  constexpr int kStages = attn_stages(KW);
+  static_assert((KW - 1) * kMq * (HD + 2) * 4 <= kStages * kStageBytes,
+                "key-split states must fit the stage buffers");
+  auto stage_of = [](int i) { return (i % KW) * SPG + (i / KW) % SPG; };
+  auto phase_of = [](int i) { return (uint32_t)((i / KW) / SPG) & 1u; };
   static_assert(kMq * (HD + 2 + 16) * 4 <= kStages * kStageBytes, "partials must fit the stage buffers");
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages];
@@ -299,8 +314,8 @@ __global__ void __launch_bounds__((MT + 1) * 32)
       const uint64_t pol = policy_evict_first();
       int issued = 0;
       for (int i = 0; i < nt; ++i) {
-        const int s = i % kStages;
-        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+        const int s = stage_of(i);
+        const uint32_t ph = phase_of(i);
         if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1u, &abort_sh, a.status)) break;
         uint8_t* ks = smem + s * kStageBytes;
         uint8_t* vs = ks + kTileBytes;
@@ -317,8 +332,7 @@ __global__ void __launch_bounds__((MT + 1) * 32)
         // a wait gave up: let the copies in flight land before reusing the buffers
         int dummy = 0;
         for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
-          (void)mbar_wait_bounded(&full_bar[i % kStages], (uint32_t)(i / kStages) & 1u, &dummy,
-                                  nullptr, 100000000ull);
+          (void)mbar_wait_bounded(&full_bar[stage_of(i)], phase_of(i), &dummy, nullptr, 100000000ull);
       }
     }
   }
@@ -355,7 +369,7 @@ __global__ void __launch_bounds__((MT + 1) * 32)
     cp_async_wait_all();
     named_sync(1, kConsumers);
 
-    const int mt = warp - 1;
+    const int mt = (warp - 1) % MT, kw = (warp - 1) / MT;
     {
       const uint32_t qb = smem_u32(q_s);
 #pragma unroll
@@ -371,11 +385,12 @@ __global__ void __launch_bounds__((MT + 1) * 32)
     st.m[0] = st.m[1] = -INFINITY;
     st.l[0] = st.l[1] = 0.0f;
 
-    if (do_block)
+    // the block's own keys go to the key-split warp with the fewest ring tiles
+    if (do_block && kw == (KW - 1 - (nt % KW)) % KW)
       process_tile<HD, kBlkKeys, false>(st, smem_u32(bk_s), smem_u32(bv_s), a.gamma, a.scale_log2);
-    for (int i = 0; i < nt; ++i) {
-      const int s = i % kStages;
-      const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+    for (int i = kw; i < nt; i += KW) {
+      const int s = stage_of(i);
+      const uint32_t ph = phase_of(i);
       if (!mbar_wait_bounded(&full_bar[s], ph, &abort_sh, a.status)) break;
       uint8_t* ks = smem + s * kStageBytes;
       uint8_t* vs = ks + kTileBytes;
@@ -393,9 +408,64 @@ __global__ void __launch_bounds__((MT + 1) * 32)
     }
   }
 
-  const int r0 = (warp - 1) * 16 + (lane >> 2), r1 = r0 + 8;
+  const int cw = warp > 0 ? (warp - 1) % MT : 0;          // row tile of a consumer warp
+  const bool lead = warp > 0 && warp <= MT;                // kw == 0: holds the merged state
+  if (KW > 1) {
+    // Merge the key-split states of each row tile into its kw == 0 warp,
+    // through the stage buffers (every stage has been consumed, or the CTA
+    // gave up).  State (o, m, l) of warp kw >= 1 sits at [kw - 1][row].
+    __syncthreads();
+    float* kst = reinterpret_cast<float*>(smem);
+    constexpr int kRowF = HD + 2;                          // o[HD], m, l
+    if (warp > MT) {
+      const int kw = (warp - 1) / MT;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float* row = kst + ((size_t)(kw - 1) * kMq + cw * 16 + (lane >> 2) + 8 * h) * kRowF;
+#pragma unroll
+        for (int t = 0; t < WarpState<HD>::NT; ++t)
+          *reinterpret_cast<float2*>(row + t * 8 + ((lane & 3) << 1)) =
+              make_float2(st.o[t][2 * h], st.o[t][2 * h + 1]);
+        if ((lane & 3) == 0) {
+          row[HD] = st.m[h];
+          row[HD + 1] = st.l[h];
+        }
+      }
+    }
+    __syncthreads();
+    if (lead) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float M = st.m[h];
+        for (int k = 1; k < KW; ++k)
+          M = fmaxf(M, kst[((size_t)(k - 1) * kMq + cw * 16 + (lane >> 2) + 8 * h) * kRowF + HD]);
+        const float base = M == -INFINITY ? 0.0f : M;
+        const float c0 = exp2f(st.m[h] - base);
+        st.l[h] *= c0;
+#pragma unroll
+        for (int t = 0; t < WarpState<HD>::NT; ++t) {
+          st.o[t][2 * h] *= c0;
+          st.o[t][2 * h + 1] *= c0;
+        }
+        for (int k = 1; k < KW; ++k) {
+          const float* row = kst + ((size_t)(k - 1) * kMq + cw * 16 + (lane >> 2) + 8 * h) * kRowF;
+          const float ck = exp2f(row[HD] - base);
+          st.l[h] += ck * row[HD + 1];
+#pragma unroll
+          for (int t = 0; t < WarpState<HD>::NT; ++t) {
+            const float2 v = *reinterpret_cast<const float2*>(row + t * 8 + ((lane & 3) << 1));
+            st.o[t][2 * h] += ck * v.x;
+            st.o[t][2 * h + 1] += ck * v.y;
+          }
+        }
+        st.m[h] = M;
+      }
+    }
+  }
+
+  const int r0 = cw * 16 + (lane >> 2), r1 = r0 + 8;
   if (S == 1) {
-    if (warp > 0) {
+    if (lead) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int ri = h ? r1 : r0;
@@ -417,7 +487,7 @@ __global__ void __launch_bounds__((MT + 1) * 32)
   // ------------------------------------------------ merge across the cluster
   // every stage buffer has been consumed (or the CTA gave up): reuse them
   __syncthreads();
-  if (warp > 0) {
+  if (lead) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int ri = h ? r1 : r0;
@@ -487,11 +557,22 @@ __global__ void __launch_bounds__((MT + 1) * 32)
   cluster.sync();
 }
 
+// Key-split warps per row tile: 3 for up to 3 row tiles, 2 for 4-5, else 1
+// (at most 10 consumer warps, so that the registers of one SM suffice).
+#ifndef DFLASH_ATTN_KW_MAX
+#define DFLASH_ATTN_KW_MAX 3
+#endif
+constexpr int attn_kw(int MT) {
+  return MT <= 3 && DFLASH_ATTN_KW_MAX >= 3 ? 3 : (MT <= 5 && DFLASH_ATTN_KW_MAX >= 2 ? 2 : 1);
+}
+
 template <int HD, int MT>
 int launch_t(const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a, int B, cudaStream_t s) {
-  constexpr size_t smem = 1024 + (size_t)kStages * 2 * kKeys * HD * 2 + (size_t)MT * 16 * HD * 2 +
-                          2 * 16 * HD * 2;
-  auto kern = attn_kernel<HD, MT>;
+  constexpr int KW = attn_kw(MT);
+  constexpr int kThreadsT = (MT * KW + 1) * 32;
+  constexpr size_t smem = 1024 + (size_t)attn_stages(KW) * 2 * kKeys * HD * 2 +
+                          (size_t)MT * 16 * HD * 2 + 2 * 16 * HD * 2;
+  auto kern = attn_kernel<HD, MT, KW>;
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -508,7 +589,7 @@ int launch_t(const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a, in
     for (int c = DFLASH_ATTN_MAX_CLUSTER; c >= 2; c >>= 1) {
       cudaLaunchConfig_t q = {};
       q.gridDim = dim3(c, 1, 1);
-      q.blockDim = dim3((MT + 1) * 32);
+      q.blockDim = dim3(kThreadsT);
       q.dynamicSmemBytes = smem;
       cudaLaunchAttribute qa[1];
       qa[0].id = cudaLaunchAttributeClusterDimension;
@@ -529,7 +610,7 @@ int launch_t(const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a, in
   while (aa.splits > max_cluster) aa.splits >>= 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(aa.splits, aa.n_kv, B);
-  cfg.blockDim = dim3((MT + 1) * 32);
+  cfg.blockDim = dim3(kThreadsT);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr_c[2];
