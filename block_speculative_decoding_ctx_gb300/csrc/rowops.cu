@@ -154,27 +154,35 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
   }
 }
 
-// Select the k largest of n keys in `cand` (shared memory), in order, by
-// repeated warp-wide maxima; taken entries are zeroed.  Warp 0 only.
-__device__ void select_topk(unsigned long long* cand, int n, int k, unsigned long long* out) {
-  const int lane = threadIdx.x & 31;
-  for (int j = 0; j < k; ++j) {
-    unsigned long long best = 0;
-    int where = -1;
-    for (int i = lane; i < n; i += 32) {
-      if (cand[i] > best) {
-        best = cand[i];
-        where = i;
-      }
-    }
-    const unsigned long long wbest = warp_max_u64(best);
-    const unsigned ball = __ballot_sync(0xffffffffu, best == wbest && where >= 0);
-    if (lane == __ffs(ball) - 1 && ball) cand[where] = 0;
-    if (lane == 0) out[j] = wbest;
-    __syncwarp();
+// One round of a warp-wide tournament over per-lane lists sorted in
+// descending order: the largest head of the warp is returned and its lane
+// drops it.  Keys are distinct (they carry the vocabulary id) or zero (empty).
+template <int KT>
+__device__ __forceinline__ unsigned long long warp_pop_max(unsigned long long (&lst)[KT]) {
+  const unsigned long long best = warp_max_u64(lst[0]);
+  const unsigned ball = __ballot_sync(0xffffffffu, best != 0 && lst[0] == best);
+  if (ball && (int)(threadIdx.x & 31) == __ffs(ball) - 1) {
+#pragma unroll
+    for (int j = 0; j + 1 < KT; ++j) lst[j] = lst[j + 1];
+    lst[KT - 1] = 0;
+  }
+  return best;
+}
+
+// (max, sum of exp(x - max)) merged over the 32 lanes of a warp.
+__device__ __forceinline__ void warp_lse(float& m, float& s) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    lse_merge(m, s, m2, s2);
   }
 }
 
+// Per-row top-k and log-sum-exp.  CTA (c, r) covers chunk c of row r: every
+// thread keeps a sorted top-KT of its 32 values and a running (max, sum);
+// warp tournaments reduce the lists to the CTA's top-k; the last CTA of the
+// row (atomic ticket) merges the chunks' lists and (max, sum) pairs the same
+// way, one chunk per lane (a row has at most 32 chunks: V <= 2^18).
 template <int KT>
 __global__ void __launch_bounds__(kTopkThreads)
     topk_lse_kernel(const float* __restrict__ logits, int V, int k, int chunks,
@@ -182,11 +190,12 @@ __global__ void __launch_bounds__(kTopkThreads)
                     int* counters, int32_t* __restrict__ ids, float* __restrict__ vals,
                     float* __restrict__ lse, int32_t* __restrict__ draft) {
   pdl_enter();
-  __shared__ unsigned long long cand[kTopkThreads * KT];
-  __shared__ unsigned long long sel[KT];
-  __shared__ float redm[32], reds[32];
+  constexpr int kWarps = kTopkThreads / 32;
+  __shared__ unsigned long long wsel[kWarps][KT];
+  __shared__ float redm[kWarps], reds[kWarps];
   __shared__ int s_last;
   const int c = blockIdx.x, r = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* row = logits + (size_t)r * V;
   const int v0 = c * kRowChunk, v1 = min(V, v0 + kRowChunk);
 
@@ -213,61 +222,69 @@ __global__ void __launch_bounds__(kTopkThreads)
       insert_key<KT>(top, vkey(xv[j], v));
     }
   }
+  warp_lse(m, s);
 #pragma unroll
-  for (int j = 0; j < KT; ++j) cand[threadIdx.x * KT + j] = top[j];
-  // (m, s) across the block
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    lse_merge(m, s, m2, s2);
+  for (int j = 0; j < KT; ++j) {
+    if (j < k) {
+      const unsigned long long b = warp_pop_max(top);
+      if (lane == 0) wsel[warp][j] = b;
+    }
   }
-  if ((threadIdx.x & 31) == 0) {
-    redm[threadIdx.x >> 5] = m;
-    reds[threadIdx.x >> 5] = s;
+  if (lane == 0) {
+    redm[warp] = m;
+    reds[warp] = s;
   }
   __syncthreads();
-  if (threadIdx.x < 32) {
-    float mm = threadIdx.x < kTopkThreads / 32 ? redm[threadIdx.x] : -INFINITY;
-    float ssum = threadIdx.x < kTopkThreads / 32 ? reds[threadIdx.x] : 0.0f;
+  if (warp == 0) {
+    unsigned long long lst[KT];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, mm, o), s2 = __shfl_xor_sync(0xffffffffu, ssum, o);
-      lse_merge(mm, ssum, m2, s2);
+    for (int j = 0; j < KT; ++j) lst[j] = (lane < kWarps && j < k) ? wsel[lane][j] : 0ull;
+    float mm = lane < kWarps ? redm[lane] : -INFINITY;
+    float ss = lane < kWarps ? reds[lane] : 0.0f;
+    warp_lse(mm, ss);
+    unsigned long long* pk = part_keys + ((size_t)r * chunks + c) * KT;
+#pragma unroll
+    for (int j = 0; j < KT; ++j) {
+      if (j < k) {
+        const unsigned long long b = warp_pop_max(lst);
+        if (lane == 0) pk[j] = b;
+      }
     }
-    select_topk(cand, kTopkThreads * KT, k, sel);
-    if (threadIdx.x == 0) {
-      unsigned long long* pk = part_keys + ((size_t)r * chunks + c) * KT;
-      for (int j = 0; j < k; ++j) pk[j] = sel[j];
+    if (lane == 0) {
       part_ml[((size_t)r * chunks + c) * 2 + 0] = mm;
-      part_ml[((size_t)r * chunks + c) * 2 + 1] = ssum;
+      part_ml[((size_t)r * chunks + c) * 2 + 1] = ss;
       __threadfence();
       s_last = (atomicAdd(&counters[r], 1) == chunks - 1);
     }
   }
   __syncthreads();
-  if (!s_last) return;
+  if (!s_last || warp != 0) return;
   __threadfence();
-  // merge the chunks of row r
-  const int n = chunks * k;
-  for (int i = threadIdx.x; i < n; i += kTopkThreads)
-    cand[i] = __ldcg(part_keys + ((size_t)r * chunks + i / k) * KT + i % k);
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    select_topk(cand, n, k, sel);
-    if (threadIdx.x == 0) {
-      float M = -INFINITY, S = 0.0f;
-      for (int cc = 0; cc < chunks; ++cc)
-        lse_merge(M, S, __ldcg(part_ml + ((size_t)r * chunks + cc) * 2),
-                  __ldcg(part_ml + ((size_t)r * chunks + cc) * 2 + 1));
-      if (lse) lse[r] = M + logf(S);
-      for (int j = 0; j < k; ++j) {
-        const unsigned long long key = sel[j];
+  // merge the chunks of row r: lane cc holds chunk cc
+  unsigned long long lst[KT];
+  float M = -INFINITY, S = 0.0f;
+#pragma unroll
+  for (int j = 0; j < KT; ++j)
+    lst[j] = (lane < chunks && j < k) ? __ldcg(part_keys + ((size_t)r * chunks + lane) * KT + j) : 0ull;
+  if (lane < chunks) {
+    M = __ldcg(part_ml + ((size_t)r * chunks + lane) * 2);
+    S = __ldcg(part_ml + ((size_t)r * chunks + lane) * 2 + 1);
+  }
+  warp_lse(M, S);
+#pragma unroll
+  for (int j = 0; j < KT; ++j) {
+    if (j < k) {
+      const unsigned long long key = warp_pop_max(lst);
+      if (lane == 0) {
         if (ids) ids[(size_t)r * k + j] = (int32_t)(~(uint32_t)(key & 0xFFFFFFFFull));
         if (vals) vals[(size_t)r * k + j] = key_to_float((uint32_t)(key >> 32));
+        if (draft && j == 0) draft[r] = (int32_t)(~(uint32_t)(key & 0xFFFFFFFFull));
       }
-      if (draft) draft[r] = (int32_t)(~(uint32_t)(sel[0] & 0xFFFFFFFFull));
-      atomicExch(&counters[r], 0);
     }
+  }
+  if (lane == 0) {
+    if (lse) lse[r] = M + logf(S);
+    atomicExch(&counters[r], 0);
   }
 }
 
