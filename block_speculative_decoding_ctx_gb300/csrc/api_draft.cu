@@ -43,6 +43,7 @@ struct dflash_handle {
   std::vector<dflash_layer_weights> layers;
   std::vector<LayerMaps> maps;
   CUtensorMap lm_head, w_c;  // lm_head: fp16 copy; w_c: the caller's bf16 matrix
+  RopeInv rope;              // inverse rotary frequencies (double -> float pairs)
   void* f16 = nullptr;       // fp16 copies of every layer's matrices and the LM head
   int num_sms;
   int mask_id;
@@ -103,6 +104,7 @@ struct DraftWs {
   void* mlp;
   void* hf;
   float* logits;
+  float2* rope_cs;
   float* gemm_partial;
   unsigned long long* topk_keys;
   float* topk_ml;
@@ -131,6 +133,7 @@ DraftWs draft_layout(const dflash_handle* h, void* base) {
   w.mlp = cv.take<uint16_t>(M * c.ffn);
   w.hf = cv.take<uint16_t>(R * c.hidden);
   w.logits = cv.take<float>(R * c.vocab);
+  w.rope_cs = cv.take<float2>(M * (c.head_dim / 2));
   w.gemm_partial = cv.take<float>(kGemmPartialFloats);
   w.topk_keys = cv.take<unsigned long long>(R * chunks * 16);
   w.topk_ml = cv.take<float>(R * chunks * 2);
@@ -145,6 +148,7 @@ struct AppendWs {
   float* fused;
   float* gemm_partial;
   void* ht;
+  float2* rope_cs;
   size_t bytes;
 };
 
@@ -157,6 +161,7 @@ AppendWs append_layout(const dflash_handle* h, void* base) {
   w.gemm_counters = cv.take<int>(kGemmCounters);
   w.fused = cv.take<float>(M * c.hidden);
   w.ht = cv.take<uint16_t>(M * c.hidden);
+  w.rope_cs = cv.take<float2>(M * (c.head_dim / 2));
   w.gemm_partial = cv.take<float>(kGemmPartialFloats);
   w.bytes = cv.off;
   return w;
@@ -184,13 +189,15 @@ GemmEpi epi_base(int kind, int M, int N, void* out, long long ld, int* status) {
 }
 
 // inv_freq_j = theta^(-2j/hd) in double, kept as a float pair for the kernels.
-void set_rope_table(GemmEpi& e, const dflash_config& c) {
+RopeInv rope_inv(const dflash_config& c) {
+  RopeInv r;
   const int half = c.head_dim / 2;
   for (int j = 0; j < 64; ++j) {
     const double inv = j < half ? std::pow((double)c.rope_theta, -2.0 * j / c.head_dim) : 0.0;
     const float hi = (float)inv;
-    e.rope_inv[j] = make_float2(hi, (float)(inv - (double)hi));
+    r.f[j] = make_float2(hi, (float)(inv - (double)hi));
   }
+  return r;
 }
 
 int splits_for(const dflash_handle* h, int n_tiles, int M, int K) {
@@ -295,6 +302,7 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
   h->layers.assign(w->layers, w->layers + cfg->n_layers);
   h->w.layers = h->layers.data();
   h->mask_id = cfg->mask_id < 0 ? cfg->vocab - 1 : cfg->mask_id;
+  h->rope = rope_inv(*cfg);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
@@ -415,8 +423,8 @@ int dflash_ctx_append(dflash_handle* h, int B, int n_max, const void* feats, con
                      s, true);
     if (rc) return rc;
   }
-  rc = launch_rmsnorm(ws.fused, M, d, static_cast<const float*>(h->w.g_c), c.eps, 0, ws.ht, ws.status,
-                      s);
+  rc = launch_rmsnorm_rope(ws.fused, M, d, static_cast<const float*>(h->w.g_c), c.eps, 0, ws.ht,
+                           ws.status, ctx_len, n_max, ws.rope_cs, c.head_dim / 2, h->rope, s);
   if (rc) return rc;
   // K/V of every layer into the ring, up to kMaxAMaps layers per launch
   const int kvd = c.n_kv_heads * c.head_dim;
@@ -432,7 +440,7 @@ int dflash_ctx_append(dflash_handle* h, int B, int n_max, const void* feats, con
     ao.dual = 0;
     GemmEpi e = epi_base(EPI_KV_RING, M, nl * 2 * kvd, nullptr, 0, ws.status);
     e.ctx_len = ctx_len;
-    set_rope_table(e, c);
+    e.rope_cs = ws.rope_cs;
     e.hd = c.head_dim;
     e.ring_k = ring_k;
     e.ring_v = ring_v;
@@ -496,7 +504,7 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
   int slot = prof_begin(h, s);
   rc = launch_embed_norm(h->w.embed, anchor, B, gamma, h->mask_id, c.vocab, d,
                          static_cast<const float*>(h->layers[0].g_attn), c.eps, ws.x, ws.h, ws.status,
-                         s);
+                         ctx_len, ws.rope_cs, hd / 2, h->rope, s);
   if (rc) return rc;
   prof_end(h, s, slot, (double)M * d * (2 + 4 + 4), DFLASH_KIND_NORM);
   AttnArgs aa;
@@ -531,7 +539,7 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
       GemmEpi e = epi_base(EPI_QKV, M, qkv_dim, ws.qkv, qkv_dim, ws.status);
       e.ctx_len = ctx_len;
       e.gamma = gamma;
-      set_rope_table(e, c);
+      e.rope_cs = ws.rope_cs;
       e.rope_rows = (c.n_q_heads + c.n_kv_heads) * hd;
       e.hd = hd;
       const int nt = (qkv_dim + 127) / 128;

@@ -279,6 +279,39 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
+// ------------------------------------------------------------------ RoPE
+
+// inv_freq_j = theta^(-2j/hd) for j < hd/2, each as a float pair (hi, lo)
+// computed in double on the host; passed by value to the kernels.
+struct RopeInv {
+  float2 f[64];
+};
+
+// (sin, cos) of pos * inv_freq with the angle reduced to [-pi, pi] in
+// float-float arithmetic: the product's rounding error is recovered with an
+// FMA, and 2*pi is split into two floats (Cody-Waite).
+__device__ __forceinline__ void rope_sincos(float pos, float inv_hi, float inv_lo, float* s,
+                                            float* c) {
+  const float a = pos * inv_hi;
+  const float e = fmaf(pos, inv_hi, -a) + pos * inv_lo;
+  const float k = rintf(a * 0.159154943091895336f);
+  float r = fmaf(-k, 6.28318548202514648f, a);
+  r = fmaf(-k, -1.74845560007448828e-7f, r);
+  r += e;
+  sincosf(r, s, c);
+}
+
+// Row `row` of a rotation table: cs[row * half + j] = (cos, sin) of
+// pos * inv_freq_j for j < half, computed by the calling threads t < half.
+__device__ __forceinline__ void rope_table_row(float2* cs, size_t row, int half, float pos,
+                                               const RopeInv& inv, int t) {
+  if (t < half) {
+    float s, c;
+    rope_sincos(pos, inv.f[t].x, inv.f[t].y, &s, &c);
+    cs[row * half + t] = make_float2(c, s);
+  }
+}
+
 // ------------------------------------------------------- PTX: tcgen05 / TMEM
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* smem_result, uint32_t ncols) {

@@ -45,38 +45,10 @@ constexpr int kABytes = 128 * kBK * 2;    // weight box per stage
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
 
-// Rotation angle pos * inv_freq reduced to [-pi, pi] with float-float
-// arithmetic: inv_freq = hi + lo (computed in double on the host), the
-// product error is recovered with an FMA, and 2*pi is split into two floats
-// (Cody-Waite).
-__device__ __forceinline__ void rope_sincos(float pos, float inv_hi, float inv_lo, float* s,
-                                            float* c) {
-  const float a = pos * inv_hi;
-  const float e = fmaf(pos, inv_hi, -a) + pos * inv_lo;
-  const float k = rintf(a * 0.159154943091895336f);
-  float r = fmaf(-k, 6.28318548202514648f, a);
-  r = fmaf(-k, -1.74845560007448828e-7f, r);
-  r += e;
-  sincosf(r, s, c);
-}
-
-struct RopeRow {
-  float inv_hi, inv_lo;
-  bool first_half;
-};
-__device__ __forceinline__ RopeRow rope_row(int d, int hd, const float2* inv) {
-  const int half = hd >> 1;
-  RopeRow rr;
-  rr.inv_hi = inv[d % half].x;
-  rr.inv_lo = inv[d % half].y;
-  rr.first_half = d < half;
-  return rr;
-}
-
-__device__ __forceinline__ float rope_apply(float x, float partner, const RopeRow& rr, float pos) {
-  float s, c;
-  rope_sincos(pos, rr.inv_hi, rr.inv_lo, &s, &c);
-  return rr.first_half ? fmaf(x, c, -partner * s) : fmaf(x, c, partner * s);
+// Rotate-half RoPE of dimension d (< hd) of one row: x pairs with the
+// partner dimension d +- hd/2; (cos, sin) come from the token's table row.
+__device__ __forceinline__ float rope_apply(float x, float partner, float2 cs, bool first_half) {
+  return first_half ? fmaf(x, cs.x, -partner * cs.y) : fmaf(x, cs.x, partner * cs.y);
 }
 
 __device__ __forceinline__ void store_f16(const GemmEpi& e, size_t o, float y) {
@@ -95,7 +67,7 @@ __device__ __forceinline__ void epi_sync(bool named) {
 }
 
 template <bool kNamed = false>
-__device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const float (&v)[16],
+__device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const float (&v)[16],
                                int tok_base, int tok_step, int ntok, int tile_n, int r,
                                float* xchg) {
   const int kind = e.kind;
@@ -105,20 +77,36 @@ __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const floa
     for (int j = 0; j < 16; ++j) xchg[j * 128 + r] = v[j];
     epi_sync(kNamed);
   }
+  // Every kind loads what it needs for its 16 tokens into registers first and
+  // stores afterwards: loads placed after stores that might alias them would
+  // each wait for a full memory round trip.
   if (kind == EPI_F32 || kind == EPI_F16 || kind == EPI_RESID) {
     const int n = tile_n * 128 + r;
     if (n < e.N) {
+      if (kind == EPI_RESID) {
+        float* out = static_cast<float*>(e.out);
+        float old[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int tok = tok_base + j * tok_step;
-        if (j < ntok && tok < e.M) {
-          const size_t o = (size_t)tok * e.ld + n;
-          if (kind == EPI_F32)
-            static_cast<float*>(e.out)[o] = v[j];
-          else if (kind == EPI_F16)
-            store_f16(e, o, v[j]);
-          else
-            static_cast<float*>(e.out)[o] += v[j];
+        for (int j = 0; j < 16; ++j) {
+          const int tok = tok_base + j * tok_step;
+          old[j] = (j < ntok && tok < e.M) ? __ldcg(out + (size_t)tok * e.ld + n) : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int tok = tok_base + j * tok_step;
+          if (j < ntok && tok < e.M) out[(size_t)tok * e.ld + n] = old[j] + v[j];
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int tok = tok_base + j * tok_step;
+          if (j < ntok && tok < e.M) {
+            const size_t o = (size_t)tok * e.ld + n;
+            if (kind == EPI_F32)
+              static_cast<float*>(e.out)[o] = v[j];
+            else
+              store_f16(e, o, v[j]);
+          }
         }
       }
     }
@@ -126,32 +114,42 @@ __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const floa
     const int n = tile_n * 128 + r;
     if (n < e.N) {
       const bool rot = n < e.rope_rows;
-      const int d = n % e.hd;
-      const RopeRow rr = rope_row(d, e.hd, e.rope_inv);
-      const int pr = r ^ (e.hd >> 1);
-#pragma unroll 4
+      const int d = n % e.hd, half = e.hd >> 1;
+      const float2* cs = e.rope_cs + d % half;
+      const int pr = r ^ half;
+      float y[16];
+      if (rot) {
+        float2 c[16];
+        float partner[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int tok = tok_base + j * tok_step;
+          const bool ok = j < ntok && tok < e.M;
+          c[j] = ok ? __ldg(cs + (size_t)tok * half) : make_float2(1.0f, 0.0f);
+          partner[j] = xchg[j * 128 + pr];
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) y[j] = rope_apply(v[j], partner[j], c[j], d < half);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) y[j] = v[j];
+      }
+#pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int tok = tok_base + j * tok_step;
-        if (j < ntok && tok < e.M) {
-          float y = v[j];
-          if (rot) {
-            const float pos = (float)(e.ctx_len[tok / e.gamma] + tok % e.gamma);
-            y = rope_apply(v[j], xchg[j * 128 + pr], rr, pos);
-          }
-          store_f16(e, (size_t)tok * e.ld + n, y);
-        }
+        if (j < ntok && tok < e.M) store_f16(e, (size_t)tok * e.ld + n, y[j]);
       }
     }
   } else if (kind == EPI_SWIGLU) {
     const int f = tile_n * 64 + r;
     if (r < 64 && f < e.N) {
+      float u[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) u[j] = xchg[j * 128 + r + 64];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int tok = tok_base + j * tok_step;
-        if (j < ntok && tok < e.M) {
-          const float g = v[j], u = xchg[j * 128 + r + 64];
-          store_f16(e, (size_t)tok * e.ld + f, silu(g) * u);
-        }
+        if (j < ntok && tok < e.M) store_f16(e, (size_t)tok * e.ld + f, silu(v[j]) * u[j]);
       }
     }
   } else if (kind == EPI_KV_RING) {
@@ -159,31 +157,42 @@ __device__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const floa
     const int layer = e.layer0 + tile_n / ao.tiles_per_map;
     const int kv = local / e.kv_dim;            // 0 = K, 1 = V
     const int g = (local % e.kv_dim) / e.hd;
-    const int d = local % e.hd;
-    const RopeRow rr = rope_row(d, e.hd, e.rope_inv);
-    const int pr = r ^ (e.hd >> 1);
+    const int d = local % e.hd, half = e.hd >> 1;
+    const float2* cs = e.rope_cs + d % half;
+    const int pr = r ^ half;
     __nv_bfloat16* ring = static_cast<__nv_bfloat16*>(kv ? e.ring_v : e.ring_k);
-#pragma unroll 4
+    // gather: position, ring row and rotation of each token
+    long long pos[16];
+    int slot[16];
+    float y[16];
+#pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int tok = tok_base + j * tok_step;
+      pos[j] = -1;
+      slot[j] = -1;
+      y[j] = v[j];
       if (j < ntok && tok < e.M) {
         const int b = tok / e.n_max, jr = tok % e.n_max;
-        if (jr < e.n_new[b]) {
-          const long long pos = e.ctx_len[b] + jr;
-          const int slot_b = e.req_slot ? e.req_slot[b] : b;
-          if (pos < 0 || slot_b < 0 || slot_b >= e.ring_batch) {
-            report_status(e.status, DFLASH_ERR_ARG);
-            continue;
-          }
-          float y = v[j];
-          if (kv == 0) y = rope_apply(v[j], xchg[j * 128 + pr], rr, (float)pos);
-          // the attention kernel reads ring entries as fp16
-          if (!(fabsf(y) <= kF16Max)) report_status(e.status, DFLASH_ERR_RANGE);
-          const size_t o =
-              ((((size_t)layer * e.ring_batch + slot_b) * e.n_kv + g) * e.window + (size_t)(pos % e.window)) *
-                  e.hd + d;
-          ring[o] = __float2bfloat16_rn(y);
+        if (jr < __ldg(e.n_new + b)) {
+          pos[j] = __ldg(e.ctx_len + b) + jr;
+          slot[j] = e.req_slot ? __ldg(e.req_slot + b) : b;
+          if (kv == 0) y[j] = rope_apply(v[j], xchg[j * 128 + pr], __ldg(cs + (size_t)tok * half), d < half);
         }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int tok = tok_base + j * tok_step;
+      if (j < ntok && tok < e.M && slot[j] != -1) {
+        if (pos[j] < 0 || slot[j] < 0 || slot[j] >= e.ring_batch) {
+          report_status(e.status, DFLASH_ERR_ARG);
+          continue;
+        }
+        // the attention kernel reads ring entries as fp16
+        if (!(fabsf(y[j]) <= kF16Max)) report_status(e.status, DFLASH_ERR_RANGE);
+        const size_t o = ((((size_t)layer * e.ring_batch + slot[j]) * e.n_kv + g) * e.window +
+                          (size_t)(pos[j] % e.window)) * e.hd + d;
+        ring[o] = __float2bfloat16_rn(y[j]);
       }
     }
   }

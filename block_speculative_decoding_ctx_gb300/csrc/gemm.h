@@ -14,7 +14,7 @@ constexpr int kMaxAMaps = 8;
 enum EpiKind : int {
   EPI_F32 = 0,     // out fp32 [M, ld] = acc
   EPI_F16 = 1,     // out fp16 [M, ld] = acc
-  EPI_QKV = 2,     // out fp16 [M, ld]; rows < rope_rows rotated at pos = ctx_len[m/gamma] + m%gamma
+  EPI_QKV = 2,     // out fp16 [M, ld]; rows < rope_rows rotated (table row m)
   EPI_RESID = 3,   // out fp32 [M, ld] += acc
   EPI_SWIGLU = 4,  // A tile = 64 gate rows + 64 up rows; out fp16 [M, ld] = silu(g) * u
   EPI_KV_RING = 5  // scatter K (rotated) / V rows into the bf16 context ring
@@ -57,7 +57,7 @@ struct GemmEpi {
   // rotary positions
   const int64_t* ctx_len;
   int gamma;
-  float2 rope_inv[64];  // inv_freq_j = theta^(-2j/hd) as a float pair (hi, lo), j < hd/2
+  const float2* rope_cs;  // [M][hd/2] (cos, sin) of token m's position x inv_freq_j
   int rope_rows;
   int hd;
   // context ring scatter

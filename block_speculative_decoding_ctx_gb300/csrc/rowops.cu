@@ -23,17 +23,21 @@ __device__ __forceinline__ void store_h2(__half* out, size_t o, float y0, float 
 
 // One CTA per block row m = b * gamma + i: x[m] = embed[id] (fp32 residual
 // stream), h[m] = RMSNorm(x[m]) * g in fp16, id = anchor[b] for i = 0, MASK
-// after.  The row is staged in shared memory
+// after; and row m of the rotation table at position ctx_len[b] + i (shared
+// by every head and layer of the pass).  The row is staged in shared memory
 // (dynamic, 4 d bytes) with 16-byte loads issued together.
 __global__ void __launch_bounds__(kNormThreads)
     embed_norm_kernel(const __nv_bfloat16* __restrict__ embed, const int32_t* __restrict__ anchor,
                       int gamma, int mask_id, int vocab, int d, const float* __restrict__ g, float eps,
-                      float* __restrict__ x, __half* __restrict__ h, int* status) {
+                      float* __restrict__ x, __half* __restrict__ h, int* status,
+                      const int64_t* __restrict__ ctx_len, float2* __restrict__ rope_cs, int half,
+                      const RopeInv inv) {
   pdl_enter();
   extern __shared__ float row_s[];
   __shared__ float red[33];
   const int m = blockIdx.x;
   const int b = m / gamma, i = m % gamma;
+  rope_table_row(rope_cs, m, half, (float)(ctx_len[b] + i), inv, threadIdx.x);
   int id = i == 0 ? anchor[b] : mask_id;
   if (id < 0 || id >= vocab) {
     if (threadIdx.x == 0) report_status(status, DFLASH_ERR_ARG);
@@ -62,17 +66,22 @@ __global__ void __launch_bounds__(kNormThreads)
   }
 }
 
-// out row r = RMSNorm(x[src(r)]) * g in fp16.
+// out row r = RMSNorm(x[src(r)]) * g in fp16.  With rope_cs, also row r of
+// the rotation table at position ctx_len[r / n_max] + r % n_max.
 // gather_gamma = 0: src(r) = r; otherwise the MASK rows:
 // src(r) = (r / (G - 1)) * G + r % (G - 1) + 1.  The row is staged in
 // shared memory (dynamic, 4 d bytes) with 16-byte loads issued together.
 __global__ void __launch_bounds__(kNormThreads)
     rmsnorm_kernel(const float* __restrict__ x, int d, const float* __restrict__ g, float eps,
-                   int gather_gamma, __half* __restrict__ out, int* status) {
+                   int gather_gamma, __half* __restrict__ out, int* status,
+                   const int64_t* __restrict__ ctx_len, int n_max, float2* __restrict__ rope_cs,
+                   int half, const RopeInv inv) {
   pdl_enter();
   extern __shared__ float row_s[];
   __shared__ float red[33];
   const int r = blockIdx.x;
+  if (rope_cs)
+    rope_table_row(rope_cs, r, half, (float)(ctx_len[r / n_max] + r % n_max), inv, threadIdx.x);
   int src = r;
   if (gather_gamma > 0) src = (r / (gather_gamma - 1)) * gather_gamma + r % (gather_gamma - 1) + 1;
   const float4* x4 = reinterpret_cast<const float4*>(x + (size_t)src * d);
@@ -298,16 +307,24 @@ __global__ void add_lengths_kernel(int B, const int32_t* __restrict__ n_new, int
 
 int launch_embed_norm(const void* embed, const int32_t* anchor, int B, int gamma, int mask_id,
                       int vocab, int d, const float* g, float eps, float* x, void* h, int* status,
+                      const int64_t* ctx_len, float2* rope_cs, int half, const RopeInv& inv,
                       cudaStream_t s) {
   return launch_pdl(embed_norm_kernel, dim3(B * gamma), dim3(kNormThreads), (size_t)d * 4, s,
                     static_cast<const __nv_bfloat16*>(embed), anchor, gamma, mask_id, vocab, d, g, eps,
-                    x, static_cast<__half*>(h), status);
+                    x, static_cast<__half*>(h), status, ctx_len, rope_cs, half, inv);
 }
 
 int launch_rmsnorm(const float* x, int rows, int d, const float* g, float eps, int gather_gamma,
                    void* out, int* status, cudaStream_t s) {
+  return launch_rmsnorm_rope(x, rows, d, g, eps, gather_gamma, out, status, nullptr, 1, nullptr, 0,
+                             RopeInv{}, s);
+}
+
+int launch_rmsnorm_rope(const float* x, int rows, int d, const float* g, float eps, int gather_gamma,
+                        void* out, int* status, const int64_t* ctx_len, int n_max, float2* rope_cs,
+                        int half, const RopeInv& inv, cudaStream_t s) {
   return launch_pdl(rmsnorm_kernel, dim3(rows), dim3(kNormThreads), (size_t)d * 4, s, x, d, g, eps,
-                    gather_gamma, static_cast<__half*>(out), status);
+                    gather_gamma, static_cast<__half*>(out), status, ctx_len, n_max, rope_cs, half, inv);
 }
 
 int launch_to_f16(const void* src, void* dst, size_t n, int* flag, int grid, cudaStream_t s) {

@@ -4,17 +4,25 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "common.cuh"
 #include "kernels.h"
 
 namespace dfl {
 
-// x: fp32 [B gamma, d] residual stream; h: fp16 [B gamma, d]
+// x: fp32 [B gamma, d] residual stream; h: fp16 [B gamma, d]; rope_cs:
+// [B gamma][half] (cos, sin) rotation table of the block positions
 int launch_embed_norm(const void* embed, const int32_t* anchor, int B, int gamma, int mask_id,
                       int vocab, int d, const float* g, float eps, float* x, void* h, int* status,
+                      const int64_t* ctx_len, float2* rope_cs, int half, const RopeInv& inv,
                       cudaStream_t s);
 // out: fp16 [rows, d]; status receives DFLASH_ERR_RANGE for values beyond fp16
 int launch_rmsnorm(const float* x, int rows, int d, const float* g, float eps, int gather_gamma,
                    void* out, int* status, cudaStream_t s);
+// launch_rmsnorm that also writes rope_cs [rows][half] for the positions
+// ctx_len[r / n_max] + r % n_max
+int launch_rmsnorm_rope(const float* x, int rows, int d, const float* g, float eps, int gather_gamma,
+                        void* out, int* status, const int64_t* ctx_len, int n_max, float2* rope_cs,
+                        int half, const RopeInv& inv, cudaStream_t s);
 // dst (fp16) = src (bf16), n elements (a multiple of 8, 16-byte aligned
 // pointers); *flag = 1 if a value is NaN or beyond the fp16 range.
 int launch_to_f16(const void* src, void* dst, size_t n, int* flag, int grid, cudaStream_t s);
