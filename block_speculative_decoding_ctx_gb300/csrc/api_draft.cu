@@ -7,10 +7,10 @@
 //   K/V GEMM whose epilogue rotates K and scatters K and V into ring slot
 //   pos mod W -> ctx_len += n.
 // draft_block ("DFlash: generate the block all at once"):
-//   embed [anchor, MASK...] + RMSNorm -> for each layer: QKV GEMM (+RoPE) ->
-//   block attention over [ring window ; block] -> O GEMM (+residual) ->
-//   RMSNorm -> gate|up GEMM (+SwiGLU) -> down GEMM (+residual) -> RMSNorm
-//   (final RMSNorm gathers the gamma-1 MASK rows) -> LM head GEMM (fp32
+//   embed [anchor, MASK...] + RMSNorm (+RoPE table) -> for each layer: QKV
+//   GEMM (+RoPE) -> block attention over [ring window ; block] -> O GEMM ->
+//   residual add + RMSNorm -> gate|up GEMM (+SwiGLU) -> down GEMM -> residual
+//   add + RMSNorm (final RMSNorm gathers the gamma-1 MASK rows) -> LM head GEMM (fp32
 //   logits) -> top-k + log-sum-exp [-> q = top_p(softmax(logits / T)) ->
 //   y ~ q].
 // Every drafter contraction runs on fp16 operands: the handle holds an fp16
@@ -32,6 +32,7 @@ using namespace dfl;
 
 constexpr size_t kGemmPartialFloats = 4u << 20;  // ticketed split-K partial tiles (16 MiB)
 constexpr int kGemmCounters = 8192;
+constexpr int kFreeResidTokens = 64;
 
 struct LayerMaps {
   CUtensorMap qkv, o, gate, up, down;  // over the fp16 copies
@@ -98,6 +99,7 @@ struct DraftWs {
   int* topk_counters;
   int* samp_counters;
   float* x;
+  float* y;
   void* h;
   void* qkv;
   void* attn;
@@ -127,6 +129,7 @@ DraftWs draft_layout(const dflash_handle* h, void* base) {
   w.samp_counters = cv.take<int>(R);
   // fp32 residual stream; fp16 GEMM operands
   w.x = cv.take<float>(M * c.hidden);
+  w.y = cv.take<float>(M * c.hidden);  // O / down output before its residual add
   w.h = cv.take<uint16_t>(M * c.hidden);
   w.qkv = cv.take<uint16_t>(M * qkv_dim);
   w.attn = cv.take<uint16_t>(M * q_dim);
@@ -530,6 +533,12 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
     attn_bytes = (double)B * c.n_kv_heads * win * hd * 2 * 2 + (double)M * (qkv_dim + qd) * 2;
   }
 
+  // With many tokens a GEMM tile's residual read-modify-write stalls its
+  // epilogue: O and down then store their fp32 output and the RMSNorm that
+  // follows (which reads the row anyway) adds it to the stream.  With few
+  // tokens the epilogue adds it itself and the latency-bound RMSNorm reads
+  // one array.
+  const bool defer = M > kFreeResidTokens;
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerMaps& lm = h->maps[l];
     const dflash_layer_weights& L = h->layers[l];
@@ -552,19 +561,21 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
                           static_cast<const char*>(ring_v) + l * ring_layer * 2, aa, B, s);
     if (rc) return rc;
     prof_end(h, s, slot, attn_bytes, DFLASH_KIND_ATTENTION);
-    {  // O projection + residual
+    {  // O projection (+ residual, here or in the next RMSNorm)
       GemmAMaps A;
       A.map[0] = lm.o;
-      GemmEpi e = epi_base(EPI_RESID, M, d, ws.x, d, ws.status);
+      GemmEpi e = defer ? epi_base(EPI_F32, M, d, ws.y, d, ws.status)
+                        : epi_base(EPI_RESID, M, d, ws.x, d, ws.status);
       const int nt = (d + 127) / 128;
       rc = draft_gemm(h, A, single_map(), nt, ws.attn, M, qd, e, scratch, s,
-                      2.0 * d * qd + 2.0 * M * qd + 8.0 * M * d);
+                      2.0 * d * qd + 2.0 * M * qd + (defer ? 4.0 : 8.0) * M * d);
       if (rc) return rc;
     }
     slot = prof_begin(h, s);
-    rc = launch_rmsnorm(ws.x, M, d, static_cast<const float*>(L.g_mlp), c.eps, 0, ws.h, ws.status, s);
+    rc = launch_add_rmsnorm(ws.x, defer ? ws.y : nullptr, 1, M, d, static_cast<const float*>(L.g_mlp),
+                            c.eps, 0, ws.h, ws.status, s);
     if (rc) return rc;
-    prof_end(h, s, slot, (double)M * d * 8, DFLASH_KIND_NORM);
+    prof_end(h, s, slot, (double)M * d * (defer ? 14 : 6), DFLASH_KIND_NORM);
     {  // gate | up + SwiGLU
       GemmAMaps A;
       A.map[0] = lm.gate;
@@ -578,24 +589,26 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
                       4.0 * c.ffn * d + 2.0 * M * d + 2.0 * M * c.ffn);
       if (rc) return rc;
     }
-    {  // down + residual
+    {  // down (+ residual, here or in the next RMSNorm)
       GemmAMaps A;
       A.map[0] = lm.down;
-      GemmEpi e = epi_base(EPI_RESID, M, d, ws.x, d, ws.status);
+      GemmEpi e = defer ? epi_base(EPI_F32, M, d, ws.y, d, ws.status)
+                        : epi_base(EPI_RESID, M, d, ws.x, d, ws.status);
       const int nt = (d + 127) / 128;
       rc = draft_gemm(h, A, single_map(), nt, ws.mlp, M, c.ffn, e, scratch, s,
-                      2.0 * d * c.ffn + 2.0 * M * c.ffn + 8.0 * M * d);
+                      2.0 * d * c.ffn + 2.0 * M * c.ffn + (defer ? 4.0 : 8.0) * M * d);
       if (rc) return rc;
     }
     slot = prof_begin(h, s);
+    const float* add = defer ? ws.y : nullptr;
     if (l + 1 < c.n_layers)
-      rc = launch_rmsnorm(ws.x, M, d, static_cast<const float*>(h->layers[l + 1].g_attn), c.eps, 0,
-                          ws.h, ws.status, s);
-    else
-      rc = launch_rmsnorm(ws.x, R, d, static_cast<const float*>(h->w.g_final), c.eps, gamma, ws.hf,
-                          ws.status, s);
+      rc = launch_add_rmsnorm(ws.x, add, 1, M, d, static_cast<const float*>(h->layers[l + 1].g_attn),
+                              c.eps, 0, ws.h, ws.status, s);
+    else  // the final RMSNorm reads only the MASK rows; the stream is not needed after it
+      rc = launch_add_rmsnorm(ws.x, add, 0, R, d, static_cast<const float*>(h->w.g_final), c.eps,
+                              gamma, ws.hf, ws.status, s);
     if (rc) return rc;
-    prof_end(h, s, slot, (double)(l + 1 < c.n_layers ? M : R) * d * 8, DFLASH_KIND_NORM);
+    prof_end(h, s, slot, (double)(l + 1 < c.n_layers ? M : R) * d * (defer ? 14 : 6), DFLASH_KIND_NORM);
   }
   float* logits = out->logits ? out->logits : ws.logits;
   {  // shared LM head on the gamma - 1 MASK rows

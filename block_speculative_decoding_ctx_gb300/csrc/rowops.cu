@@ -66,13 +66,17 @@ __global__ void __launch_bounds__(kNormThreads)
   }
 }
 
-// out row r = RMSNorm(x[src(r)]) * g in fp16.  With rope_cs, also row r of
-// the rotation table at position ctx_len[r / n_max] + r % n_max.
+// out row r = RMSNorm(x[src(r)] (+ add[src(r)])) * g in fp16.  `add` is the
+// fp32 output of the projection that feeds the residual stream (O or down):
+// the residual add happens here, and with write_back the sum is stored to
+// x[src(r)].  With rope_cs, also row r of the rotation table at position
+// ctx_len[r / n_max] + r % n_max.
 // gather_gamma = 0: src(r) = r; otherwise the MASK rows:
 // src(r) = (r / (G - 1)) * G + r % (G - 1) + 1.  The row is staged in
 // shared memory (dynamic, 4 d bytes) with 16-byte loads issued together.
 __global__ void __launch_bounds__(kNormThreads)
-    rmsnorm_kernel(const float* __restrict__ x, int d, const float* __restrict__ g, float eps,
+    rmsnorm_kernel(float* x, const float* __restrict__ add, int write_back, int d,
+                   const float* __restrict__ g, float eps,
                    int gather_gamma, __half* __restrict__ out, int* status,
                    const int64_t* __restrict__ ctx_len, int n_max, float2* __restrict__ rope_cs,
                    int half, const RopeInv inv) {
@@ -84,11 +88,20 @@ __global__ void __launch_bounds__(kNormThreads)
     rope_table_row(rope_cs, r, half, (float)(ctx_len[r / n_max] + r % n_max), inv, threadIdx.x);
   int src = r;
   if (gather_gamma > 0) src = (r / (gather_gamma - 1)) * gather_gamma + r % (gather_gamma - 1) + 1;
-  const float4* x4 = reinterpret_cast<const float4*>(x + (size_t)src * d);
+  float4* x4 = reinterpret_cast<float4*>(x + (size_t)src * d);
+  const float4* a4 = add ? reinterpret_cast<const float4*>(add + (size_t)src * d) : nullptr;
   float ss = 0.0f;
 #pragma unroll 4
   for (int c = threadIdx.x; c < d / 4; c += kNormThreads) {
-    const float4 v = __ldcg(x4 + c);
+    float4 v = __ldcg(x4 + c);
+    if (a4) {
+      const float4 y = __ldcg(a4 + c);
+      v.x += y.x;
+      v.y += y.y;
+      v.z += y.z;
+      v.w += y.w;
+      if (write_back) x4[c] = v;
+    }
     reinterpret_cast<float4*>(row_s)[c] = v;
     ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
   }
@@ -314,17 +327,19 @@ int launch_embed_norm(const void* embed, const int32_t* anchor, int B, int gamma
                     x, static_cast<__half*>(h), status, ctx_len, rope_cs, half, inv);
 }
 
-int launch_rmsnorm(const float* x, int rows, int d, const float* g, float eps, int gather_gamma,
-                   void* out, int* status, cudaStream_t s) {
-  return launch_rmsnorm_rope(x, rows, d, g, eps, gather_gamma, out, status, nullptr, 1, nullptr, 0,
-                             RopeInv{}, s);
+int launch_add_rmsnorm(float* x, const float* add, int write_back, int rows, int d, const float* g,
+                       float eps, int gather_gamma, void* out, int* status, cudaStream_t s) {
+  return launch_pdl(rmsnorm_kernel, dim3(rows), dim3(kNormThreads), (size_t)d * 4, s, x, add,
+                    write_back, d, g, eps, gather_gamma, static_cast<__half*>(out), status,
+                    (const int64_t*)nullptr, 1, (float2*)nullptr, 0, RopeInv{});
 }
 
-int launch_rmsnorm_rope(const float* x, int rows, int d, const float* g, float eps, int gather_gamma,
+int launch_rmsnorm_rope(float* x, int rows, int d, const float* g, float eps, int gather_gamma,
                         void* out, int* status, const int64_t* ctx_len, int n_max, float2* rope_cs,
                         int half, const RopeInv& inv, cudaStream_t s) {
-  return launch_pdl(rmsnorm_kernel, dim3(rows), dim3(kNormThreads), (size_t)d * 4, s, x, d, g, eps,
-                    gather_gamma, static_cast<__half*>(out), status, ctx_len, n_max, rope_cs, half, inv);
+  return launch_pdl(rmsnorm_kernel, dim3(rows), dim3(kNormThreads), (size_t)d * 4, s, x,
+                    (const float*)nullptr, 0, d, g, eps, gather_gamma, static_cast<__half*>(out), status,
+                    ctx_len, n_max, rope_cs, half, inv);
 }
 
 int launch_to_f16(const void* src, void* dst, size_t n, int* flag, int grid, cudaStream_t s) {

@@ -15,12 +15,14 @@ int launch_embed_norm(const void* embed, const int32_t* anchor, int B, int gamma
                       int vocab, int d, const float* g, float eps, float* x, void* h, int* status,
                       const int64_t* ctx_len, float2* rope_cs, int half, const RopeInv& inv,
                       cudaStream_t s);
-// out: fp16 [rows, d]; status receives DFLASH_ERR_RANGE for values beyond fp16
-int launch_rmsnorm(const float* x, int rows, int d, const float* g, float eps, int gather_gamma,
-                   void* out, int* status, cudaStream_t s);
-// launch_rmsnorm that also writes rope_cs [rows][half] for the positions
+// out: fp16 [rows, d] = RMSNorm(x + add) * g (rows gathered when
+// gather_gamma > 0); with write_back, x += add in place.  status receives
+// DFLASH_ERR_RANGE for values beyond fp16.
+int launch_add_rmsnorm(float* x, const float* add, int write_back, int rows, int d, const float* g,
+                       float eps, int gather_gamma, void* out, int* status, cudaStream_t s);
+// out = RMSNorm(x) * g, and rope_cs [rows][half] for the positions
 // ctx_len[r / n_max] + r % n_max
-int launch_rmsnorm_rope(const float* x, int rows, int d, const float* g, float eps, int gather_gamma,
+int launch_rmsnorm_rope(float* x, int rows, int d, const float* g, float eps, int gather_gamma,
                         void* out, int* status, const int64_t* ctx_len, int n_max, float2* rope_cs,
                         int half, const RopeInv& inv, cudaStream_t s);
 // dst (fp16) = src (bf16), n elements (a multiple of 8, 16-byte aligned
