@@ -250,6 +250,14 @@ class Cycle:
         self.verify()
 
 
+# DRAM bytes (read + written) of the draft pass's GEMM launches at batch 1,
+# gamma 8, five layers: ncu's dram__bytes_read.sum + dram__bytes_write.sum per
+# launch on a one-layer pass (4 GEMMs per layer + the LM head), scaled to five
+# layers.  Taken with the GEMM kernels as of the fp16-operand, gathered-epilogue
+# version; 4,871,029,248 algorithmic bytes.
+GEMM_TRAFFIC_PER_PASS = 4878.1e6
+
+
 def gpu_launches_per_step(dims, with_append=True):
     per_layer = 7       # QKV, attention, O, RMSNorm, gate|up, down, RMSNorm
     n = 1 + per_layer * dims["n_layers"] + 2          # embed+norm, layers, LM head, top-k
@@ -330,7 +338,9 @@ def run_ours(args, rank, ws):
     achieved = by / (ms * 1e-3) / 1e9
     roof = {"kernel": f"gemm_tc_kernel (all {len(gemm)} GEMM launches of the draft pass)",
             "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-            "frac": round(achieved / hbm, 4), "peak_source": src, "traffic": None,
+            "frac": round(achieved / hbm, 4), "peak_source": src,
+            "traffic": (GEMM_TRAFFIC_PER_PASS if (B, G, args.layers) == (1, 8, 5) else None),
+            "traffic_unit": "DRAM bytes read + written per pass (all GEMM launches)",
             "gemm_ms_per_pass": round(ms, 4), "gemm_bytes_per_pass": by,
             "lm_head_GBps": round(lm[0][1] / (statistics.median(r[0] for r in lm) * 1e-3) / 1e9, 1),
             "kernel_ms_per_pass_by_kind": {k: round(v, 4) for k, v in kinds.items()},
