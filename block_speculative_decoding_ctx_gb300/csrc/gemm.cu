@@ -55,10 +55,15 @@ __device__ __forceinline__ void store_f16(const GemmEpi& e, size_t o, float y) {
   static_cast<__half*>(e.out)[o] = to_f16_checked(y, e.status);
 }
 
+// Floats of one exchange buffer: a chunk of 16 tokens x 128 rows.
+constexpr int kXchg = 16 * 128;
+
 // Epilogue of up to 16 tokens of this thread's row: v[j] is token
 // tok_base + j * tok_step, the first `ntok` are real.  `xchg` holds the
 // chunk as [16][128] floats so that partner rows can be read.  Every thread
-// of the CTA (kNamed: of the four epilogue warps) calls it: it synchronises.
+// of the CTA (kNamed: of the four epilogue warps) calls it: it synchronises
+// once, after writing `xchg`; callers alternate between two buffers so that
+// a chunk's writes never meet the previous chunk's reads.
 __device__ __forceinline__ void epi_sync(bool named) {
   if (named)
     asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -196,7 +201,6 @@ __device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts
       }
     }
   }
-  if (needs_xchg) epi_sync(kNamed);
 }
 
 template <int BN, int STAGES>
@@ -207,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kStage = kABytes + kBBytes;
   constexpr uint32_t kTmemCols = BN < 32 ? 32 : BN;
   static_assert(kStage % 1024 == 0, "stage buffers must keep 1024-byte alignment");
-  static_assert((BN + 16) * 128 * 4 <= STAGES * kStage, "split partials must fit the stage buffers");
+  static_assert((BN + 32) * 128 * 4 <= STAGES * kStage, "split partials must fit the stage buffers");
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
@@ -350,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < n_chunks; ++c) {
         float v[16];
         load_chunk(c, v);
-        epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg);
+        epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg + (c & 1) * kXchg);
       }
     }
   } else if (!args.cluster) {
@@ -385,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] += __ldcg(ps + (c * 16 + j) * 128 + r);
           }
-          epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg);
+          epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg + (c & 1) * kXchg);
         }
       }
       if (threadIdx.x == 0) atomicExch(&args.counters[tile_lin], 0);
@@ -430,7 +434,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const int cnt = mine - g0 < 16 ? mine - g0 : 16;
-        epilogue_chunk(epi, ao, v, tile_m * T + rank + g0 * S, S, cnt, tile_n, r, xchg_s);
+        epilogue_chunk(epi, ao, v, tile_m * T + rank + g0 * S, S, cnt, tile_n, r,
+                       xchg_s + ((g0 >> 4) & 1) * kXchg);
       }
     }
     // no CTA may leave while another still reads its shared memory
@@ -577,6 +582,7 @@ __global__ void __launch_bounds__(192, 1)
     constexpr int ntok = 16;
     constexpr int n_chunks = T / 16;
     int lt = 0;
+    unsigned xc = 0;  // exchange buffer of the next chunk, alternating across tiles
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
       const int tile_m = t % m_tiles, tile_n = t / m_tiles;
       const int buf = lt & 1;
@@ -600,7 +606,8 @@ __global__ void __launch_bounds__(192, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&acce_bar[buf]);
         }
-        epilogue_chunk<true>(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg);
+        epilogue_chunk<true>(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r,
+                             xchg + (xc++ & 1) * kXchg);
       }
     }
   }
@@ -663,7 +670,7 @@ int launch_persistent(const GemmAMaps& A, const CUtensorMap& tmB, const GemmAOpt
                       const GemmArgs& args, const GemmEpi& epi, int n_tiles, int m_tiles,
                       int num_sms, cudaStream_t s, bool pdl) {
   auto kern = gemm_tc_persistent_kernel<BN, STAGES>;
-  constexpr size_t smem = (size_t)STAGES * (kABytes + BN * kBK * 2) + 16 * 128 * 4 + 1024;
+  constexpr size_t smem = (size_t)STAGES * (kABytes + BN * kBK * 2) + 2 * kXchg * 4 + 1024;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
