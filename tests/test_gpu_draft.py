@@ -30,6 +30,9 @@ CASES = [
     ("tiny", 2, 4, [64, 30]),
     ("tiny", 3, 4, [0, 1, 65]),
     ("small", 3, 8, [300, 256, 17]),
+    # batch >= 4 runs attention on tcgen05: head dim 64, ragged, empty and wrapped windows
+    ("tiny", 4, 4, [64, 30, 0, 200]),
+    ("small", 5, 8, [300, 256, 17, 0, 1000]),
     ("small128", 2, 16, [512, 700]),
     ("small128", 4, 8, [100, 513, 1, 2000]),
     ("wide", 16, 8, [256] * 8 + [10, 300, 40, 999, 257, 255, 1, 0]),
