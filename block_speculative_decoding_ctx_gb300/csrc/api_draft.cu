@@ -33,12 +33,6 @@ using namespace dfl;
 constexpr size_t kGemmPartialFloats = 4u << 20;  // ticketed split-K partial tiles (16 MiB)
 constexpr int kGemmCounters = 8192;
 constexpr int kFreeResidTokens = 64;
-// Smallest batch at which block attention runs on tcgen05 (attention_tc.cu);
-// below it the mma.sync kernel with key-split warps (attention.cu).
-#ifndef DFLASH_ATTN_TC_BATCH
-#define DFLASH_ATTN_TC_BATCH 1000000
-#endif
-constexpr int kAttnTcBatch = DFLASH_ATTN_TC_BATCH;
 
 struct LayerMaps {
   CUtensorMap qkv, o, gate, up, down;  // over the fp16 copies
@@ -563,9 +557,8 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
       if (rc) return rc;
     }
     slot = prof_begin(h, s);
-    rc = (B >= kAttnTcBatch ? launch_attention_tc : launch_attention)(
-        static_cast<const char*>(ring_k) + l * ring_layer * 2,
-        static_cast<const char*>(ring_v) + l * ring_layer * 2, aa, B, s);
+    rc = launch_attention(static_cast<const char*>(ring_k) + l * ring_layer * 2,
+                          static_cast<const char*>(ring_v) + l * ring_layer * 2, aa, B, s);
     if (rc) return rc;
     prof_end(h, s, slot, attn_bytes, DFLASH_KIND_ATTENTION);
     {  // O projection (+ residual, here or in the next RMSNorm)

@@ -28,8 +28,5 @@ int attn_row_tiles(int n_q, int n_kv, int gamma);
 // ring_*_layer: the layer's slice of the ring, bf16 [ring_batch, Hkv, W, hd].
 int launch_attention(const void* ring_k_layer, const void* ring_v_layer, const AttnArgs& a, int B,
                      cudaStream_t s);
-// The same on tcgen05 (attention_tc.cu): query group x gamma <= 96 rows.
-int launch_attention_tc(const void* ring_k_layer, const void* ring_v_layer, const AttnArgs& a, int B,
-                        cudaStream_t s);
 
 }  // namespace dfl
