@@ -16,7 +16,9 @@
 // A producer warp streams 64-key K/V tiles of the context ring into shared
 // memory with TMA (128-byte swizzle, evict-first), STAGES deep.  Scores run
 // on mma.sync with fp16 operands (queries are fp16; ring keys, stored bf16,
-// are widened to fp16 in registers — exact in fp16's range) and P.V on bf16
+// are widened to fp16 — exact in fp16's range — either in registers by each
+// consumer or, with many row tiles, once per tile in place by a converter
+// warp) and P.V on bf16
 // operands against the bf16 ring values (fp16 for the block's own values),
 // all with fp32 accumulation; the softmax is online
 // (running max and sum per row, reduced with warp shuffles); the window and
@@ -122,6 +124,15 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Bounded wait taken by a whole warp: the warp goes on only if every lane saw
+// the phase complete, so that the warp-collective instructions after it
+// (ldmatrix, mma.sync) stay convergent even when a wait gives up.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status) {
+  const bool ok = mbar_wait_bounded(bar, parity, abort_flag, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
 template <int HD>
 struct WarpState {
   static constexpr int NT = HD / 8;  // output n-tiles of 8 dims
@@ -131,9 +142,10 @@ struct WarpState {
 };
 
 // Scores, online softmax and P.V of one key tile held in shared memory as
-// HD/64 swizzled halves [NK keys][64 dims] for K and for V: bf16 context-ring
-// tiles (RING) or the block's own fp16 keys and values.
-template <int HD, int NK, bool RING>
+// HD/64 swizzled halves [NK keys][64 dims] for K and for V: bf16 ring values
+// (RING) or the block's own fp16 values.  Keys are fp16, or bf16 ring keys
+// widened in registers here when WIDEN.
+template <int HD, int NK, bool RING, bool WIDEN>
 __device__ __forceinline__ void process_tile(WarpState<HD>& st, uint32_t k_base, uint32_t v_base,
                                              int n_valid, float scale_log2) {
   constexpr int NT_S = NK / 8;
@@ -155,7 +167,7 @@ __device__ __forceinline__ void process_tile(WarpState<HD>& st, uint32_t k_base,
       const int dim = kk * 16 + (((lane >> 3) & 1) << 3);
       ldsm_x4(k_base + (dim >> 6) * kHalf + swz(key, dim & 63), bk[kp][0], bk[kp][1], bk[kp][2],
               bk[kp][3]);
-      if (RING) {
+      if (WIDEN) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) bk[kp][e] = bf16x2_to_f16x2(bk[kp][e]);
       }
@@ -247,9 +259,16 @@ __device__ __forceinline__ void process_tile(WarpState<HD>& st, uint32_t k_base,
 // One CTA per (key split, KV head, request); the S splits of a (request, KV
 // head) form one thread-block cluster and merge their partial softmax states
 // through distributed shared memory.  Warp 0 produces; warp 1 + mt + MT * kw
-// is the consumer of row tile mt taking key tiles kw, kw + KW, ...
+// is the consumer of row tile mt taking key tiles kw, kw + KW, ...  With four
+// or more row tiles one more warp widens each ring key tile to fp16 in place,
+// once for all its consumers (measured: batch 32, gamma 16, 1.16 -> 0.94 ms
+// per pass); with fewer, each consumer widens its fragments in registers (the
+// extra handoff cost more than it saved at gamma 8 and batch 1).
 template <int HD, int MT, int KW>
-__global__ void __launch_bounds__((MT * KW + 1) * 32)
+__host__ __device__ constexpr bool attn_conv_warp() { return MT >= 4; }
+
+template <int HD, int MT, int KW>
+__global__ void __launch_bounds__((MT * KW + 1 + (attn_conv_warp<HD, MT, KW>() ? 1 : 0)) * 32)
     attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 const AttnArgs a) {
   pdl_enter();
@@ -266,7 +285,9 @@ __global__ void __launch_bounds__((MT * KW + 1) * 32)
   auto phase_of = [](int i) { return (uint32_t)((i / KW) / SPG) & 1u; };
   static_assert(kMq * (HD + 2 + 16) * 4 <= kStages * kStageBytes, "partials must fit the stage buffers");
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages];
+  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], kready_bar[kStages];
+  constexpr bool kHasConv = attn_conv_warp<HD, MT, KW>();
+  constexpr int kConv = kHasConv ? MT * KW + 1 : 1 << 20;  // converter warp (if any)
   __shared__ int abort_sh;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -300,6 +321,7 @@ __global__ void __launch_bounds__((MT * KW + 1) * 32)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], MT);
+      mbar_init(&kready_bar[s], 1);
     }
     abort_sh = 0;
     fence_barrier_init();
@@ -337,8 +359,29 @@ __global__ void __launch_bounds__((MT * KW + 1) * 32)
     }
   }
 
+  if (kHasConv && warp == kConv) {
+    // ------------------------------------------------------------- converter
+    // ring keys are bf16: widen each tile's keys to fp16 in place, once
+    for (int i = 0; i < nt; ++i) {
+      const int s = stage_of(i);
+      if (!warp_wait(&full_bar[s], phase_of(i), &abort_sh, a.status)) break;
+      uint4* k4 = reinterpret_cast<uint4*>(smem + s * kStageBytes);
+#pragma unroll 4
+      for (int idx = lane; idx < kTileBytes / 16; idx += 32) {
+        uint4 u = k4[idx];
+        u.x = bf16x2_to_f16x2(u.x);
+        u.y = bf16x2_to_f16x2(u.y);
+        u.z = bf16x2_to_f16x2(u.z);
+        u.w = bf16x2_to_f16x2(u.w);
+        k4[idx] = u;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&kready_bar[s]);
+    }
+  }
+
   WarpState<HD> st;
-  if (warp > 0) {
+  if (warp > 0 && warp < kConv) {
     // ----------------------------------------------------------- consumers
     const int ctid = threadIdx.x - 32;
     // Q rows ri = hh * gamma + i  <-  qkv row b*gamma + i, column (g*group + hh) * hd,
@@ -387,16 +430,17 @@ __global__ void __launch_bounds__((MT * KW + 1) * 32)
 
     // the block's own keys go to the key-split warp with the fewest ring tiles
     if (do_block && kw == (KW - 1 - (nt % KW)) % KW)
-      process_tile<HD, kBlkKeys, false>(st, smem_u32(bk_s), smem_u32(bv_s), a.gamma, a.scale_log2);
+      process_tile<HD, kBlkKeys, false, false>(st, smem_u32(bk_s), smem_u32(bv_s), a.gamma, a.scale_log2);
     for (int i = kw; i < nt; i += KW) {
       const int s = stage_of(i);
       const uint32_t ph = phase_of(i);
-      if (!mbar_wait_bounded(&full_bar[s], ph, &abort_sh, a.status)) break;
+      // K widened (or just landed), V landed
+      if (!warp_wait(kHasConv ? &kready_bar[s] : &full_bar[s], ph, &abort_sh, a.status)) break;
       uint8_t* ks = smem + s * kStageBytes;
       uint8_t* vs = ks + kTileBytes;
       const int slot0 = (t0 + i) * kKeys;
       const int valid = n_valid - slot0 < kKeys ? n_valid - slot0 : kKeys;
-      process_tile<HD, kKeys, true>(st, smem_u32(ks), smem_u32(vs), valid, a.scale_log2);
+      process_tile<HD, kKeys, true, !kHasConv>(st, smem_u32(ks), smem_u32(vs), valid, a.scale_log2);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[s]);
     }
@@ -408,7 +452,7 @@ __global__ void __launch_bounds__((MT * KW + 1) * 32)
     }
   }
 
-  const int cw = warp > 0 ? (warp - 1) % MT : 0;          // row tile of a consumer warp
+  const int cw = (warp > 0 && warp < kConv) ? (warp - 1) % MT : 0;  // row tile of a consumer warp
   const bool lead = warp > 0 && warp <= MT;                // kw == 0: holds the merged state
   if (KW > 1) {
     // Merge the key-split states of each row tile into its kw == 0 warp,
@@ -417,7 +461,7 @@ __global__ void __launch_bounds__((MT * KW + 1) * 32)
     __syncthreads();
     float* kst = reinterpret_cast<float*>(smem);
     constexpr int kRowF = HD + 2;                          // o[HD], m, l
-    if (warp > MT) {
+    if (warp > MT && warp < kConv) {
       const int kw = (warp - 1) / MT;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -569,7 +613,7 @@ constexpr int attn_kw(int MT) {
 template <int HD, int MT>
 int launch_t(const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a, int B, cudaStream_t s) {
   constexpr int KW = attn_kw(MT);
-  constexpr int kThreadsT = (MT * KW + 1) * 32;
+  constexpr int kThreadsT = (MT * KW + 1 + (attn_conv_warp<HD, MT, KW>() ? 1 : 0)) * 32;
   constexpr size_t smem = 1024 + (size_t)attn_stages(KW) * 2 * kKeys * HD * 2 +
                           (size_t)MT * 16 * HD * 2 + 2 * 16 * HD * 2;
   auto kern = attn_kernel<HD, MT, KW>;
