@@ -39,7 +39,6 @@ namespace {
 
 namespace cg = cooperative_groups;
 
-constexpr int kThreads = 128;
 constexpr int kBK = 64;                   // K elements per stage (128 bytes of 16-bit values)
 constexpr int kABytes = 128 * kBK * 2;    // weight box per stage
 
@@ -61,26 +60,27 @@ constexpr int kXchg = 16 * 128;
 // Epilogue of up to 16 tokens of this thread's row: v[j] is token
 // tok_base + j * tok_step, the first `ntok` are real.  `xchg` holds the
 // chunk as [16][128] floats so that partner rows can be read.  Every thread
-// of the CTA (kNamed: of the four epilogue warps) calls it: it synchronises
-// once, after writing `xchg`; callers alternate between two buffers so that
-// a chunk's writes never meet the previous chunk's reads.
-__device__ __forceinline__ void epi_sync(bool named) {
-  if (named)
+// of one epilogue group (four warps, one per TMEM lane quarter, named
+// barrier `bar`) calls it: it synchronises once, after writing `xchg`;
+// callers alternate between two buffers per group so that a chunk's writes
+// never meet the previous chunk's reads.
+__device__ __forceinline__ void epi_sync(int bar) {
+  // immediate barrier ids: a register id would reserve all sixteen
+  if (bar == 1)
     asm volatile("bar.sync 1, 128;" ::: "memory");
   else
-    __syncthreads();
+    asm volatile("bar.sync 2, 128;" ::: "memory");
 }
 
-template <bool kNamed = false>
 __device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const float (&v)[16],
                                int tok_base, int tok_step, int ntok, int tile_n, int r,
-                               float* xchg) {
+                               float* xchg, int bar) {
   const int kind = e.kind;
   const bool needs_xchg = (kind == EPI_QKV || kind == EPI_SWIGLU || kind == EPI_KV_RING);
   if (needs_xchg) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) xchg[j * 128 + r] = v[j];
-    epi_sync(kNamed);
+    epi_sync(bar);
   }
   // Every kind loads what it needs for its 16 tokens into registers first and
   // stores afterwards: loads placed after stores that might alias them would
@@ -203,15 +203,21 @@ __device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts
   }
 }
 
+// Threads of gemm_tc_kernel: four warps, eight (two epilogue groups taking
+// alternate chunks of 16 tokens) for tiles of 128 or more tokens, whose
+// one-tile epilogue would otherwise run serially after the mainloop.
+__host__ __device__ constexpr int gemm_threads(int BN) { return BN >= 128 ? 256 : 128; }
+
 template <int BN, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(gemm_threads(BN), 1)
     gemm_tc_kernel(const __grid_constant__ GemmAMaps A, const __grid_constant__ CUtensorMap tmB,
                         const GemmAOpts ao, const GemmArgs args, const GemmEpi epi) {
   constexpr int kBBytes = BN * kBK * 2;
   constexpr int kStage = kABytes + kBBytes;
   constexpr uint32_t kTmemCols = BN < 32 ? 32 : BN;
+  constexpr int kGroups = gemm_threads(BN) / 128;
   static_assert(kStage % 1024 == 0, "stage buffers must keep 1024-byte alignment");
-  static_assert((BN + 32) * 128 * 4 <= STAGES * kStage, "split partials must fit the stage buffers");
+  static_assert((BN + 64) * 128 * 4 <= STAGES * kStage, "split partials must fit the stage buffers");
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
@@ -333,9 +339,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                               100000000ull);
   }
   __syncthreads();
-  const int r = warp * 32 + lane;
-  const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
-  float* xchg = reinterpret_cast<float*>(smem);
+  const int q = warp & 3, grp = warp >> 2;  // TMEM lane quarter, epilogue group
+  const int r = q * 32 + lane;
+  const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
+  float* xchg = reinterpret_cast<float*>(smem) + grp * 2 * kXchg;  // this group's two buffers
+  const int bar = 1 + grp;
   const bool aborted = abort_sh != 0 || !acc_ok;
 
   constexpr int T = BN;  // tokens per tile
@@ -351,10 +359,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (args.splits == 1) {
     if (!aborted) {
-      for (int c = 0; c < n_chunks; ++c) {
+      for (int c = grp, it = 0; c < n_chunks; c += kGroups, ++it) {
         float v[16];
         load_chunk(c, v);
-        epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg + (c & 1) * kXchg);
+        epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg + (it & 1) * kXchg, bar);
       }
     }
   } else if (!args.cluster) {
@@ -366,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* part = args.partial + (size_t)tile_lin * args.splits * per_split;
     float* mine = part + (size_t)split * per_split;
     if (!aborted) {
-      for (int c = 0; c < n_chunks; ++c) {
+      for (int c = grp; c < n_chunks; c += kGroups) {
         float v[16];
         load_chunk(c, v);
 #pragma unroll
@@ -380,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (last_sh) {
       __threadfence();
       if (!aborted) {
-        for (int c = 0; c < n_chunks; ++c) {
+        for (int c = grp, it = 0; c < n_chunks; c += kGroups, ++it) {
           float v[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = 0.0f;
@@ -389,7 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] += __ldcg(ps + (c * 16 + j) * 128 + r);
           }
-          epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg + (c & 1) * kXchg);
+          epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg + (it & 1) * kXchg,
+                         bar);
         }
       }
       if (threadIdx.x == 0) atomicExch(&args.counters[tile_lin], 0);
@@ -403,8 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // on them.  A CTA whose wait gave up still takes part in both cluster
     // barriers (its siblings would otherwise wait for it) but writes nothing.
     float* part_s = reinterpret_cast<float*>(smem);
-    float* xchg_s = part_s + (size_t)n_chunks * 16 * 128;
-    for (int c = 0; c < n_chunks; ++c) {
+    float* xchg_s = part_s + (size_t)n_chunks * 16 * 128 + grp * 2 * kXchg;
+    for (int c = grp; c < n_chunks; c += kGroups) {
       float v[16];
       if (!aborted) {
         load_chunk(c, v);
@@ -421,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int S = args.splits;
       const int rank = split;  // cluster dims (1, 1, S): rank = blockIdx.z
       const int mine = (T - rank + S - 1) / S;
-      for (int g0 = 0; g0 < mine; g0 += 16) {
+      for (int g0 = grp * 16, it = 0; g0 < mine; g0 += 16 * kGroups, ++it) {
         float v[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] = 0.0f;
@@ -435,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int cnt = mine - g0 < 16 ? mine - g0 : 16;
         epilogue_chunk(epi, ao, v, tile_m * T + rank + g0 * S, S, cnt, tile_n, r,
-                       xchg_s + ((g0 >> 4) & 1) * kXchg);
+                       xchg_s + (it & 1) * kXchg, bar);
       }
     }
     // no CTA may leave while another still reads its shared memory
@@ -449,11 +458,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Persistent, warp-specialised variant for many token columns (no split-K):
 // one CTA per SM walks the tiles t = blockIdx.x, blockIdx.x + gridDim.x, ...
 // (token tiles fastest, so CTAs running at the same time share weight tiles in
-// L2).  Warp 0 lane 0 issues TMA, warp 1 lane 0 issues MMAs, warps 2-5 run
-// the epilogue.  Two TMEM accumulators let the epilogue of one tile overlap
-// the mainloop of the next.
+// L2).  Warp 0 lane 0 issues TMA, warp 1 lane 0 issues MMAs, warps 2-9 run
+// the epilogue as two groups of four (one warp per TMEM lane quarter) taking
+// alternate chunks of 16 tokens.  Two TMEM accumulators let the epilogue of
+// one tile overlap the mainloop of the next.
 template <int BN, int STAGES>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     gemm_tc_persistent_kernel(const __grid_constant__ GemmAMaps A,
                                    const __grid_constant__ CUtensorMap tmB, const GemmAOpts ao,
                                    const GemmArgs args, const GemmEpi epi, int n_tiles, int m_tiles) {
@@ -485,7 +495,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accf_bar[b], 1);
-      mbar_init(&acce_bar[b], 4);
+      mbar_init(&acce_bar[b], 8);
     }
     abort_sh = 0;
     fence_barrier_init();
@@ -579,6 +589,8 @@ __global__ void __launch_bounds__(192, 1)
     // --------------------------------------------------------- epilogue
     const int r = 32 * (warp & 3) + lane;  // TMEM lane quarter of this warp
     const uint32_t t_row = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const int grp = (warp - 2) >> 2, bar = 1 + grp;
+    float* gx = xchg + grp * 2 * kXchg;   // this group's two exchange buffers
     constexpr int ntok = 16;
     constexpr int n_chunks = T / 16;
     int lt = 0;
@@ -588,26 +600,26 @@ __global__ void __launch_bounds__(192, 1)
       const int buf = lt & 1;
       const uint32_t use = (uint32_t)(lt >> 1);
       const bool ok = mbar_wait_bounded(&accf_bar[buf], use & 1u, &abort_sh, args.status);
-      // the four epilogue warps agree before acting on the outcome
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      // the four warps of the group agree before acting on the outcome
+      epi_sync(bar);
       if (!ok || abort_sh) break;
       tc_fence_after();
       const uint32_t base = t_row + (uint32_t)(buf * BN);
-      for (int c = 0; c < n_chunks; ++c) {
+      for (int c = grp; c < n_chunks; c += 2) {
         float v[16];
         uint32_t raw[16];
         tmem_ld_x16(base + c * 16, raw);
         tc_wait_ld();
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]);
-        if (c == n_chunks - 1) {
+        if (c + 2 >= n_chunks) {
           // every column of this accumulator is in registers: hand it back
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acce_bar[buf]);
         }
-        epilogue_chunk<true>(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r,
-                             xchg + (xc++ & 1) * kXchg);
+        epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, gx + (xc++ & 1) * kXchg,
+                       bar);
       }
     }
   }
@@ -640,7 +652,7 @@ int launch_one(const GemmAMaps& A, const CUtensorMap& tmB, const GemmAOpts& ao, 
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(gemm_threads(BN));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -670,7 +682,7 @@ int launch_persistent(const GemmAMaps& A, const CUtensorMap& tmB, const GemmAOpt
                       const GemmArgs& args, const GemmEpi& epi, int n_tiles, int m_tiles,
                       int num_sms, cudaStream_t s, bool pdl) {
   auto kern = gemm_tc_persistent_kernel<BN, STAGES>;
-  constexpr size_t smem = (size_t)STAGES * (kABytes + BN * kBK * 2) + 2 * kXchg * 4 + 1024;
+  constexpr size_t smem = (size_t)STAGES * (kABytes + BN * kBK * 2) + 4 * kXchg * 4 + 1024;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
@@ -681,7 +693,7 @@ int launch_persistent(const GemmAMaps& A, const CUtensorMap& tmB, const GemmAOpt
   const int total = n_tiles * m_tiles;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(total < num_sms ? total : num_sms);
-  cfg.blockDim = dim3(192);
+  cfg.blockDim = dim3(320);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
