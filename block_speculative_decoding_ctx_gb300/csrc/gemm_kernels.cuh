@@ -1,0 +1,703 @@
+// Device code and launch templates of the tcgen05 GEMMs, shared by the
+// translation units that instantiate them (gemm.cu, gemm_tiles_*.cu) so that
+// the many token-tile widths compile in parallel.  See gemm.cu for the design.
+#pragma once
+
+#include <cooperative_groups.h>
+
+#include <cmath>
+
+#include "common.cuh"
+#include "gemm.h"
+
+namespace dfl {
+namespace {
+
+namespace cg = cooperative_groups;
+
+constexpr int kBK = 64;                   // K elements per stage (128 bytes of 16-bit values)
+constexpr int kABytes = 128 * kBK * 2;    // weight box per stage
+
+__device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
+
+// Rotate-half RoPE of dimension d (< hd) of one row: x pairs with the
+// partner dimension d +- hd/2; (cos, sin) come from the token's table row.
+__device__ __forceinline__ float rope_apply(float x, float partner, float2 cs, bool first_half) {
+  return first_half ? fmaf(x, cs.x, -partner * cs.y) : fmaf(x, cs.x, partner * cs.y);
+}
+
+__device__ __forceinline__ void store_f16(const GemmEpi& e, size_t o, float y) {
+  static_cast<__half*>(e.out)[o] = to_f16_checked(y, e.status);
+}
+
+// Floats of one exchange buffer: a chunk of 16 tokens x 128 rows.
+constexpr int kXchg = 16 * 128;
+
+// Epilogue of up to 16 tokens of this thread's row: v[j] is token
+// tok_base + j * tok_step, the first `ntok` are real.  `xchg` holds the
+// chunk as [16][128] floats so that partner rows can be read.  Every thread
+// of one epilogue group (four warps, one per TMEM lane quarter, named
+// barrier `bar`) calls it: it synchronises once, after writing `xchg`;
+// callers alternate between two buffers per group so that a chunk's writes
+// never meet the previous chunk's reads.
+__device__ __forceinline__ void epi_sync(int bar) {
+  // immediate barrier ids: a register id would reserve all sixteen
+  if (bar == 1)
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+  else
+    asm volatile("bar.sync 2, 128;" ::: "memory");
+}
+
+__device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const float (&v)[16],
+                               int tok_base, int tok_step, int ntok, int tile_n, int r,
+                               float* xchg, int bar) {
+  const int kind = e.kind;
+  const bool needs_xchg = (kind == EPI_QKV || kind == EPI_SWIGLU || kind == EPI_KV_RING);
+  if (needs_xchg) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) xchg[j * 128 + r] = v[j];
+    epi_sync(bar);
+  }
+  // Every kind loads what it needs for its 16 tokens into registers first and
+  // stores afterwards: loads placed after stores that might alias them would
+  // each wait for a full memory round trip.
+  if (kind == EPI_F32 || kind == EPI_F16 || kind == EPI_RESID) {
+    const int n = tile_n * 128 + r;
+    if (n < e.N) {
+      if (kind == EPI_RESID) {
+        float* out = static_cast<float*>(e.out);
+        float old[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int tok = tok_base + j * tok_step;
+          old[j] = (j < ntok && tok < e.M) ? __ldcg(out + (size_t)tok * e.ld + n) : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int tok = tok_base + j * tok_step;
+          if (j < ntok && tok < e.M) out[(size_t)tok * e.ld + n] = old[j] + v[j];
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int tok = tok_base + j * tok_step;
+          if (j < ntok && tok < e.M) {
+            const size_t o = (size_t)tok * e.ld + n;
+            if (kind == EPI_F32)
+              static_cast<float*>(e.out)[o] = v[j];
+            else
+              store_f16(e, o, v[j]);
+          }
+        }
+      }
+    }
+  } else if (kind == EPI_QKV) {
+    const int n = tile_n * 128 + r;
+    if (n < e.N) {
+      const bool rot = n < e.rope_rows;
+      const int d = n % e.hd, half = e.hd >> 1;
+      const float2* cs = e.rope_cs + d % half;
+      const int pr = r ^ half;
+      float y[16];
+      if (rot) {
+        float2 c[16];
+        float partner[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int tok = tok_base + j * tok_step;
+          const bool ok = j < ntok && tok < e.M;
+          c[j] = ok ? __ldg(cs + (size_t)tok * half) : make_float2(1.0f, 0.0f);
+          partner[j] = xchg[j * 128 + pr];
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) y[j] = rope_apply(v[j], partner[j], c[j], d < half);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) y[j] = v[j];
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int tok = tok_base + j * tok_step;
+        if (j < ntok && tok < e.M) store_f16(e, (size_t)tok * e.ld + n, y[j]);
+      }
+    }
+  } else if (kind == EPI_SWIGLU) {
+    const int f = tile_n * 64 + r;
+    if (r < 64 && f < e.N) {
+      float u[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) u[j] = xchg[j * 128 + r + 64];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int tok = tok_base + j * tok_step;
+        if (j < ntok && tok < e.M) store_f16(e, (size_t)tok * e.ld + f, silu(v[j]) * u[j]);
+      }
+    }
+  } else if (kind == EPI_KV_RING) {
+    const int local = (tile_n % ao.tiles_per_map) * 128 + r;
+    const int layer = e.layer0 + tile_n / ao.tiles_per_map;
+    const int kv = local / e.kv_dim;            // 0 = K, 1 = V
+    const int g = (local % e.kv_dim) / e.hd;
+    const int d = local % e.hd, half = e.hd >> 1;
+    const float2* cs = e.rope_cs + d % half;
+    const int pr = r ^ half;
+    __nv_bfloat16* ring = static_cast<__nv_bfloat16*>(kv ? e.ring_v : e.ring_k);
+    // gather: position, ring row and rotation of each token
+    long long pos[16];
+    int slot[16];
+    float y[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int tok = tok_base + j * tok_step;
+      pos[j] = -1;
+      slot[j] = -1;
+      y[j] = v[j];
+      if (j < ntok && tok < e.M) {
+        const int b = tok / e.n_max, jr = tok % e.n_max;
+        if (jr < __ldg(e.n_new + b)) {
+          pos[j] = __ldg(e.ctx_len + b) + jr;
+          slot[j] = e.req_slot ? __ldg(e.req_slot + b) : b;
+          if (kv == 0) y[j] = rope_apply(v[j], xchg[j * 128 + pr], __ldg(cs + (size_t)tok * half), d < half);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int tok = tok_base + j * tok_step;
+      if (j < ntok && tok < e.M && slot[j] != -1) {
+        if (pos[j] < 0 || slot[j] < 0 || slot[j] >= e.ring_batch) {
+          report_status(e.status, DFLASH_ERR_ARG);
+          continue;
+        }
+        // the attention kernel reads ring entries as fp16
+        if (!(fabsf(y[j]) <= kF16Max)) report_status(e.status, DFLASH_ERR_RANGE);
+        const size_t o = ((((size_t)layer * e.ring_batch + slot[j]) * e.n_kv + g) * e.window +
+                          (size_t)(pos[j] % e.window)) * e.hd + d;
+        ring[o] = __float2bfloat16_rn(y[j]);
+      }
+    }
+  }
+}
+
+// Threads of gemm_tc_kernel: four warps, eight (two epilogue groups taking
+// alternate chunks of 16 tokens) for tiles of 128 or more tokens, whose
+// one-tile epilogue would otherwise run serially after the mainloop.
+__host__ __device__ constexpr int gemm_threads(int BN) { return BN >= 128 ? 256 : 128; }
+
+// TMEM allocations are powers of two of at least 32 columns.
+__host__ __device__ constexpr uint32_t tmem_cols(int n) {
+  return n <= 32 ? 32u : n <= 64 ? 64u : n <= 128 ? 128u : n <= 256 ? 256u : 512u;
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(gemm_threads(BN), 1)
+    gemm_tc_kernel(const __grid_constant__ GemmAMaps A, const __grid_constant__ CUtensorMap tmB,
+                        const GemmAOpts ao, const GemmArgs args, const GemmEpi epi) {
+  constexpr int kBBytes = BN * kBK * 2;
+  constexpr int kStage = kABytes + kBBytes;
+  constexpr uint32_t kTmemCols = tmem_cols(BN);
+  constexpr int kGroups = gemm_threads(BN) / 128;
+  static_assert(kStage % 1024 == 0, "stage buffers must keep 1024-byte alignment");
+  static_assert((BN + 64) * 128 * 4 <= STAGES * kStage, "split partials must fit the stage buffers");
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t acc_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  __shared__ int last_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile_n = blockIdx.x, tile_m = blockIdx.y, split = blockIdx.z;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int kb_total = (args.K + kBK - 1) / kBK;
+  const int kb0 = (int)((long long)split * kb_total / args.splits);
+  const int kb1 = (int)((long long)(split + 1) * kb_total / args.splits);
+  const int nkb = kb1 - kb0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(&acc_bar, 1);
+    abort_sh = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < ao.n_maps; ++i) tma_prefetch_desc(&A.map[i]);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  // the next kernel may be scheduled now; it waits for our completion before
+  // reading what we write
+  grid_dependents_launch();
+
+  int issued = 0;
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------- producer
+    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_x = policy_evict_last();
+    int map_i = 0, row0;
+    if (ao.dual) {
+      row0 = ao.row_offset + tile_n * 64;
+    } else {
+      map_i = tile_n / ao.tiles_per_map;
+      row0 = ao.row_offset + (tile_n % ao.tiles_per_map) * 128;
+    }
+    const int tok0 = tile_m * BN;
+    // weights do not depend on the previous kernel: start streaming them
+    // before waiting for it (programmatic dependent launch)
+    const int pre = nkb < STAGES ? nkb : STAGES;
+    for (int i = 0; i < pre; ++i) {
+      uint8_t* sa = smem + i * kStage;
+      mbar_arrive_expect_tx(&full_bar[i], kStage);
+      const int kc = (kb0 + i) * kBK;
+      if (ao.dual) {
+        tma_load_2d(sa, &A.map[0], &full_bar[i], kc, row0, pol_w);
+        tma_load_2d(sa + 64 * 128, &A.map[1], &full_bar[i], kc, row0, pol_w);
+      } else {
+        tma_load_2d(sa, &A.map[map_i], &full_bar[i], kc, row0, pol_w);
+      }
+    }
+    grid_dependency_wait();
+    for (int i = 0; i < pre; ++i)
+      tma_load_2d(smem + i * kStage + kABytes, &tmB, &full_bar[i], (kb0 + i) * kBK, tok0, pol_x);
+    issued = pre;
+    for (int i = pre; i < nkb; ++i) {
+      const int s = i % STAGES;
+      const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
+      if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1u, &abort_sh, args.status)) break;
+      uint8_t* sa = smem + s * kStage;
+      mbar_arrive_expect_tx(&full_bar[s], kStage);
+      const int kc = (kb0 + i) * kBK;
+      if (ao.dual) {
+        tma_load_2d(sa, &A.map[0], &full_bar[s], kc, row0, pol_w);
+        tma_load_2d(sa + 64 * 128, &A.map[1], &full_bar[s], kc, row0, pol_w);
+      } else {
+        tma_load_2d(sa, &A.map[map_i], &full_bar[s], kc, row0, pol_w);
+      }
+      tma_load_2d(sa + kABytes, &tmB, &full_bar[s], kc, tok0, pol_x);
+      issued = i + 1;
+    }
+  } else if (warp == 1 && lane == 0) {
+    // --------------------------------------------------------- MMA issuer
+    const uint32_t idesc = idesc_f32acc(128, BN, args.type == OPND_BF16);
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % STAGES;
+      const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
+      if (!mbar_wait_bounded(&full_bar[s], ph, &abort_sh, args.status)) break;
+      tc_fence_after();
+      const uint32_t a_addr = smem_u32(smem + s * kStage);
+      const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+      for (int k = 0; k < kBK / 16; ++k)
+        tc_mma_f16(tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), idesc,
+                   (i | k) ? 1u : 0u);
+      tc_commit(&empty_bar[s]);
+    }
+    tc_commit(&acc_bar);
+  }
+  __syncwarp();
+
+  // ----------------------------------------------------------- epilogue
+  const bool acc_ok = mbar_wait_bounded(&acc_bar, 0, &abort_sh, args.status);
+  tc_fence_after();
+  if (warp == 0 && lane == 0 && abort_sh) {
+    // a wait gave up: let this CTA's copies in flight land before exiting
+    int dummy = 0;
+    for (int i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
+      (void)mbar_wait_bounded(&full_bar[i % STAGES], (uint32_t)(i / STAGES) & 1u, &dummy, nullptr,
+                              100000000ull);
+  }
+  __syncthreads();
+  const int q = warp & 3, grp = warp >> 2;  // TMEM lane quarter, epilogue group
+  const int r = q * 32 + lane;
+  const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
+  float* xchg = reinterpret_cast<float*>(smem) + grp * 2 * kXchg;  // this group's two buffers
+  const int bar = 1 + grp;
+  const bool aborted = abort_sh != 0 || !acc_ok;
+
+  constexpr int T = BN;  // tokens per tile
+  constexpr int ntok = 16;
+  constexpr int n_chunks = T / 16;
+  auto load_chunk = [&](int c, float (&v)[16]) {
+    uint32_t raw[16];
+    tmem_ld_x16(t_row + c * 16, raw);
+    tc_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]);
+  };
+
+  if (args.splits == 1) {
+    if (!aborted) {
+      for (int c = grp, it = 0; c < n_chunks; c += kGroups, ++it) {
+        float v[16];
+        load_chunk(c, v);
+        epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg + (it & 1) * kXchg, bar);
+      }
+    }
+  } else if (!args.cluster) {
+    // Ticketed reduction: every split stores its fp32 partial [T][128] in
+    // global memory; the last split of the tile to arrive (atomic ticket after
+    // a fence) sums them in split order and runs the epilogue.
+    const int tile_lin = tile_m * gridDim.x + tile_n;
+    const size_t per_split = (size_t)n_chunks * 16 * 128;
+    float* part = args.partial + (size_t)tile_lin * args.splits * per_split;
+    float* mine = part + (size_t)split * per_split;
+    if (!aborted) {
+      for (int c = grp; c < n_chunks; c += kGroups) {
+        float v[16];
+        load_chunk(c, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) mine[(c * 16 + j) * 128 + r] = v[j];
+      }
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last_sh = (atomicAdd(&args.counters[tile_lin], 1) == args.splits - 1);
+    __syncthreads();
+    if (last_sh) {
+      __threadfence();
+      if (!aborted) {
+        for (int c = grp, it = 0; c < n_chunks; c += kGroups, ++it) {
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+          for (int s = 0; s < args.splits; ++s) {
+            const float* ps = part + (size_t)s * per_split;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] += __ldcg(ps + (c * 16 + j) * 128 + r);
+          }
+          epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg + (it & 1) * kXchg,
+                         bar);
+        }
+      }
+      if (threadIdx.x == 0) atomicExch(&args.counters[tile_lin], 0);
+    }
+  } else {
+    // The K splits of this tile form a thread-block cluster.  Each leaves its
+    // fp32 partial [T tokens][128 rows] in its own shared memory (the stage
+    // buffers are free: every stage has been consumed); after a cluster
+    // barrier CTA `rank` sums, over distributed shared memory and in split
+    // order, the tokens rank, rank + S, ... of the tile and runs the epilogue
+    // on them.  A CTA whose wait gave up still takes part in both cluster
+    // barriers (its siblings would otherwise wait for it) but writes nothing.
+    float* part_s = reinterpret_cast<float*>(smem);
+    float* xchg_s = part_s + (size_t)n_chunks * 16 * 128 + grp * 2 * kXchg;
+    for (int c = grp; c < n_chunks; c += kGroups) {
+      float v[16];
+      if (!aborted) {
+        load_chunk(c, v);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) part_s[(c * 16 + j) * 128 + r] = v[j];
+    }
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    if (!aborted) {
+      const int S = args.splits;
+      const int rank = split;  // cluster dims (1, 1, S): rank = blockIdx.z
+      const int mine = (T - rank + S - 1) / S;
+      for (int g0 = grp * 16, it = 0; g0 < mine; g0 += 16 * kGroups, ++it) {
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+        for (int s = 0; s < S; ++s) {
+          const float* ps = cluster.map_shared_rank(part_s, s);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int t = rank + (g0 + j) * S;
+            if (g0 + j < mine) v[j] += ps[t * 128 + r];
+          }
+        }
+        const int cnt = mine - g0 < 16 ? mine - g0 : 16;
+        epilogue_chunk(epi, ao, v, tile_m * T + rank + g0 * S, S, cnt, tile_n, r,
+                       xchg_s + (it & 1) * kXchg, bar);
+      }
+    }
+    // no CTA may leave while another still reads its shared memory
+    cluster.sync();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// Persistent, warp-specialised variant for many token columns (no split-K):
+// one CTA per SM walks the tiles t = blockIdx.x, blockIdx.x + gridDim.x, ...
+// (token tiles fastest, so CTAs running at the same time share weight tiles in
+// L2).  Warp 0 lane 0 issues TMA, warp 1 lane 0 issues MMAs, warps 2-9 run
+// the epilogue as two groups of four (one warp per TMEM lane quarter) taking
+// alternate chunks of 16 tokens.  Two TMEM accumulators let the epilogue of
+// one tile overlap the mainloop of the next.
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(320, 1)
+    gemm_tc_persistent_kernel(const __grid_constant__ GemmAMaps A,
+                                   const __grid_constant__ CUtensorMap tmB, const GemmAOpts ao,
+                                   const GemmArgs args, const GemmEpi epi, int n_tiles, int m_tiles) {
+  constexpr int kBBytes = BN * kBK * 2;
+  constexpr int kStage = kABytes + kBBytes;
+  constexpr uint32_t kTmemCols = tmem_cols(2 * BN);  // two accumulators, at columns 0 and BN
+  static_assert(kStage % 1024 == 0, "stage buffers must keep 1024-byte alignment");
+  static_assert(2 * BN <= 512, "two accumulators must fit tensor memory");
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t accf_bar[2];
+  __shared__ __align__(8) uint64_t acce_bar[2];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* xchg = reinterpret_cast<float*>(smem + STAGES * kStage);
+  constexpr int T = BN;
+  const int kb_total = (args.K + kBK - 1) / kBK;
+  const int total = n_tiles * m_tiles;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf_bar[b], 1);
+      mbar_init(&acce_bar[b], 8);
+    }
+    abort_sh = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < ao.n_maps; ++i) tma_prefetch_desc(&A.map[i]);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  grid_dependents_launch();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      bool waited = false;
+      int it = 0;
+      for (int t = blockIdx.x; t < total && !abort_sh; t += gridDim.x) {
+        const int tile_m = t % m_tiles, tile_n = t / m_tiles;
+        int map_i = 0, row0;
+        if (ao.dual) {
+          row0 = ao.row_offset + tile_n * 64;
+        } else {
+          map_i = tile_n / ao.tiles_per_map;
+          row0 = ao.row_offset + (tile_n % ao.tiles_per_map) * 128;
+        }
+        const int tok0 = tile_m * T;
+        for (int kb = 0; kb < kb_total; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1u, &abort_sh, args.status)) break;
+          uint8_t* sa = smem + s * kStage;
+          mbar_arrive_expect_tx(&full_bar[s], kStage);
+          const int kc = kb * kBK;
+          if (ao.dual) {
+            tma_load_2d(sa, &A.map[0], &full_bar[s], kc, row0, pol_w);
+            tma_load_2d(sa + 64 * 128, &A.map[1], &full_bar[s], kc, row0, pol_w);
+          } else {
+            tma_load_2d(sa, &A.map[map_i], &full_bar[s], kc, row0, pol_w);
+          }
+          if (!waited) {  // activations come from the previous kernel
+            grid_dependency_wait();
+            waited = true;
+          }
+          tma_load_2d(sa + kABytes, &tmB, &full_bar[s], kc, tok0, pol_x);
+        }
+      }
+      if (abort_sh) {
+        int dummy = 0;
+        for (int i = (it > STAGES ? it - STAGES : 0); i < it; ++i)
+          (void)mbar_wait_bounded(&full_bar[i % STAGES], (uint32_t)(i / STAGES) & 1u, &dummy, nullptr,
+                                  100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------- MMA issuer
+      const uint32_t idesc = idesc_f32acc(128, BN, args.type == OPND_BF16);
+      int it = 0, lt = 0;
+      for (int t = blockIdx.x; t < total && !abort_sh; t += gridDim.x, ++lt) {
+        const int buf = lt & 1;
+        const uint32_t use = (uint32_t)(lt >> 1);
+        if (!mbar_wait_bounded(&acce_bar[buf], (use & 1u) ^ 1u, &abort_sh, args.status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * BN);
+        for (int kb = 0; kb < kb_total; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          if (!mbar_wait_bounded(&full_bar[s], ph, &abort_sh, args.status)) break;
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + s * kStage);
+          const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            tc_mma_f16(d, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), idesc,
+                       (kb | k) ? 1u : 0u);
+          tc_commit(&empty_bar[s]);
+        }
+        tc_commit(&accf_bar[buf]);
+      }
+    }
+  } else {
+    // --------------------------------------------------------- epilogue
+    const int r = 32 * (warp & 3) + lane;  // TMEM lane quarter of this warp
+    const uint32_t t_row = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const int grp = (warp - 2) >> 2, bar = 1 + grp;
+    float* gx = xchg + grp * 2 * kXchg;   // this group's two exchange buffers
+    constexpr int ntok = 16;
+    constexpr int n_chunks = T / 16;
+    int lt = 0;
+    unsigned xc = 0;  // exchange buffer of the next chunk, alternating across tiles
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
+      const int tile_m = t % m_tiles, tile_n = t / m_tiles;
+      const int buf = lt & 1;
+      const uint32_t use = (uint32_t)(lt >> 1);
+      const bool ok = mbar_wait_bounded(&accf_bar[buf], use & 1u, &abort_sh, args.status);
+      // the four warps of the group agree before acting on the outcome
+      epi_sync(bar);
+      if (!ok || abort_sh) break;
+      tc_fence_after();
+      const uint32_t base = t_row + (uint32_t)(buf * BN);
+      for (int c = grp; c < n_chunks; c += 2) {
+        float v[16];
+        uint32_t raw[16];
+        tmem_ld_x16(base + c * 16, raw);
+        tc_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]);
+        if (c + 2 >= n_chunks) {
+          // every column of this accumulator is in registers: hand it back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acce_bar[buf]);
+        }
+        epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, gx + (xc++ & 1) * kXchg,
+                       bar);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------ launch
+
+
+template <int BN, int STAGES>
+constexpr size_t smem_bytes() {
+  return (size_t)STAGES * (kABytes + BN * kBK * 2) + 1024;
+}
+
+template <int BN, int STAGES>
+int launch_one(const GemmAMaps& A, const CUtensorMap& tmB, const GemmAOpts& ao, const GemmArgs& args,
+               const GemmEpi& epi, dim3 grid, cudaStream_t s, bool pdl) {
+  auto kern = gemm_tc_kernel<BN, STAGES>;
+  constexpr size_t smem = smem_bytes<BN, STAGES>();
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return DFLASH_ERR_LAUNCH;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(gemm_threads(BN));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (args.splits > 1 && args.cluster) {  // the K splits of a tile run as one cluster
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = args.splits;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  if (cudaLaunchKernelEx(&cfg, kern, A, tmB, ao, args, epi) != cudaSuccess) return DFLASH_ERR_LAUNCH;
+  return DFLASH_OK;
+}
+
+
+
+template <int BN, int STAGES>
+int launch_persistent(const GemmAMaps& A, const CUtensorMap& tmB, const GemmAOpts& ao,
+                      const GemmArgs& args, const GemmEpi& epi, int n_tiles, int m_tiles,
+                      int num_sms, cudaStream_t s, bool pdl) {
+  auto kern = gemm_tc_persistent_kernel<BN, STAGES>;
+  constexpr size_t smem = (size_t)STAGES * (kABytes + BN * kBK * 2) + 4 * kXchg * 4 + 1024;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return DFLASH_ERR_LAUNCH;
+    attr_set = true;
+  }
+  const int total = n_tiles * m_tiles;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(total < num_sms ? total : num_sms);
+  cfg.blockDim = dim3(320);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, kern, A, tmB, ao, args, epi, n_tiles, m_tiles) != cudaSuccess)
+    return DFLASH_ERR_LAUNCH;
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+// Launch of one token-tile width: the non-persistent kernel on `grid`, or the
+// persistent one; defined by the translation unit that instantiates it.
+#define DFL_TILE_CASES_ONE(X) X(16, 6) X(32, 5) X(64, 4)
+#define DFL_TILE_CASES_LO(X) X(80, 6) X(96, 6) X(112, 6) X(128, 6) X(144, 5) X(160, 5)
+#define DFL_TILE_CASES_HI(X) X(176, 5) X(192, 4) X(208, 4) X(224, 4) X(240, 4) X(256, 4)
+
+int launch_tile_lo(int BN, bool persistent, const GemmAMaps& A, const CUtensorMap& tmB,
+                   const GemmAOpts& ao, const GemmArgs& args, const GemmEpi& epi, dim3 grid,
+                   int n_tiles, int m_tiles, int num_sms, cudaStream_t s, bool pdl);
+int launch_tile_hi(int BN, bool persistent, const GemmAMaps& A, const CUtensorMap& tmB,
+                   const GemmAOpts& ao, const GemmArgs& args, const GemmEpi& epi, dim3 grid,
+                   int n_tiles, int m_tiles, int num_sms, cudaStream_t s, bool pdl);
+
+}  // namespace dfl
