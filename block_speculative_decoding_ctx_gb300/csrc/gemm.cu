@@ -24,12 +24,21 @@
 // disjoint subset of the tile's tokens over distributed shared memory, in
 // split order — deterministic) or store their partials in global memory, the
 // last to arrive summing them in split order.
+// Many token columns and no split-K: a persistent kernel walks the output
+// tiles (gemm_tc_persistent_kernel), by default over CTA pairs
+// (gemm_tc_pair_kernel: cta_group::2 MMAs of 256 weight rows, the token tile
+// split between the pair's shared memories).
 // All waits are bounded (see mbar_wait_bounded).
 #include <cudaTypedefs.h>
 
 #include <mutex>
 
 #include "gemm_kernels.cuh"
+
+// Persistent GEMMs over CTA pairs (cta_group::2) instead of single CTAs.
+#ifndef DFLASH_GEMM_PAIR
+#define DFLASH_GEMM_PAIR 1
+#endif
 
 namespace dfl {
 namespace {
@@ -118,6 +127,12 @@ int launch_gemm(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void
   // many token columns and no split-K: the persistent kernel
   const bool persistent = splits == 1 && T >= 64 && (size_t)n_tiles * m_tiles >= (size_t)scratch.num_sms;
   dim3 grid(n_tiles, m_tiles, splits);
+  if (persistent && DFLASH_GEMM_PAIR && BN >= 80) {
+    CUtensorMap tmBh;
+    rc = encode_2d(&tmBh, x, type, (uint64_t)K, (uint64_t)M, kBK, (uint32_t)(T / 2));
+    if (rc) return rc;
+    return launch_tile_pair(BN, A, tmBh, ao, args, epi, n_tiles, m_tiles, scratch.num_sms, s, pdl);
+  }
   if (BN >= 176)
     return launch_tile_hi(BN, persistent, A, tmB, ao, args, epi, grid, n_tiles, m_tiles, scratch.num_sms, s, pdl);
   if (BN >= 80)

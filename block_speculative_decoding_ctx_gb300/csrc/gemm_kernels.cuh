@@ -609,6 +609,220 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+// Persistent kernel over CTA pairs (cta_group::2).  A cluster of two CTAs
+// owns a unit of two adjacent weight tiles (256 rows) x one token tile: each
+// CTA loads its own 128 weight rows and half of the token tile, and one
+// thread of the even CTA issues M = 256 MMAs that read both CTAs' shared
+// memory and accumulate each CTA's 128 rows in its own tensor memory.  Per
+// k-block a CTA then moves 16 KiB of weights + BN * 64 bytes of activations
+// through shared memory instead of 16 KiB + BN * 128, which is what bounds
+// the single-CTA kernel's mainloop (TMA fills and MMA operand reads share the
+// SM's shared-memory bandwidth).
+//   Barriers: the even CTA's full[s] takes one expect-tx arrival (its
+// producer's, for both CTAs' bytes) and both CTAs' TMA bytes; the even CTA's MMA commits arrive on empty[s] and
+// accf[b] of both CTAs; the even CTA's acce[b] counts the epilogue warps of
+// both CTAs.  Both CTAs meet at cluster barriers after setup and before exit,
+// so neither leaves while the other may still touch its memory.
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(320, 1)
+    gemm_tc_pair_kernel(const __grid_constant__ GemmAMaps A, const __grid_constant__ CUtensorMap tmB,
+                        const GemmAOpts ao, const GemmArgs args, const GemmEpi epi, int n_tiles,
+                        int m_tiles) {
+  constexpr int kBHalf = BN / 2;                  // token rows of B held by each CTA
+  constexpr int kBBytes = kBHalf * kBK * 2;
+  constexpr int kStage = kABytes + kBBytes;
+  constexpr uint32_t kTmemCols = tmem_cols(2 * BN);  // two accumulators, at columns 0 and BN
+  static_assert(kStage % 1024 == 0, "stage buffers must keep 1024-byte alignment");
+  static_assert(kBHalf % 8 == 0, "half token tiles must hold whole 8-row swizzle atoms");
+  static_assert(2 * BN <= 512, "two accumulators must fit tensor memory");
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t accf_bar[2];
+  __shared__ __align__(8) uint64_t acce_bar[2];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* xchg = reinterpret_cast<float*>(smem + STAGES * kStage);
+  constexpr int T = BN;
+  const int kb_total = (args.K + kBK - 1) / kBK;
+  const int n_pairs_n = (n_tiles + 1) / 2;
+  const int total = n_pairs_n * m_tiles;
+  const int unit0 = (int)(blockIdx.x >> 1), unit_step = (int)(gridDim.x >> 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf_bar[b], 1);
+      mbar_init(&acce_bar[b], 16);
+    }
+    abort_sh = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < ao.n_maps; ++i) tma_prefetch_desc(&A.map[i]);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&tmem_base_sh, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  // the peer's barriers are initialised and its tensor memory allocated
+  cluster_arrive();
+  cluster_wait();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  if (threadIdx.x == 0) {
+    // the pair's MMAs address both CTAs' accumulators by one column address
+    uint32_t peer;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];"
+                 : "=r"(peer)
+                 : "r"(mapa_shared(smem_u32(&tmem_base_sh), rank ^ 1u))
+                 : "memory");
+    if (peer != tmem) {
+      abort_sh = 1;
+      report_status(args.status, DFLASH_ERR_UNSUPPORTED);
+    }
+  }
+  __syncthreads();
+  grid_dependents_launch();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      bool waited = false;
+      int it = 0;
+      for (int t = unit0; t < total && !abort_sh; t += unit_step) {
+        const int tile_m = t % m_tiles;
+        int tile_n = (t / m_tiles) * 2 + (int)rank;
+        // an odd tile count leaves the last unit one tile: the other CTA loads
+        // the live tile's rows again (its results are not stored)
+        if (tile_n >= n_tiles) tile_n = n_tiles - 1;
+        int map_i = 0, row0;
+        if (ao.dual) {
+          row0 = ao.row_offset + tile_n * 64;
+        } else {
+          map_i = tile_n / ao.tiles_per_map;
+          row0 = ao.row_offset + (tile_n % ao.tiles_per_map) * 128;
+        }
+        const int tok0 = tile_m * T + (int)rank * kBHalf;
+        for (int kb = 0; kb < kb_total; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1u, &abort_sh, args.status)) break;
+          uint8_t* sa = smem + s * kStage;
+          const uint32_t fb = mapa_shared(smem_u32(&full_bar[s]), 0);
+          // the even CTA announces both CTAs' bytes; the odd CTA's copies may
+          // land before that (the transaction count runs negative meanwhile)
+          if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * kStage);
+          const int kc = kb * kBK;
+          if (ao.dual) {
+            tma_load_2d_pair(sa, &A.map[0], fb, kc, row0, pol_w);
+            tma_load_2d_pair(sa + 64 * 128, &A.map[1], fb, kc, row0, pol_w);
+          } else {
+            tma_load_2d_pair(sa, &A.map[map_i], fb, kc, row0, pol_w);
+          }
+          if (!waited) {  // activations come from the previous kernel
+            grid_dependency_wait();
+            waited = true;
+          }
+          tma_load_2d_pair(sa + kABytes, &tmB, fb, kc, tok0, pol_x);
+        }
+      }
+      if (abort_sh) {
+        // let this CTA's copies in flight land: wait for the stages it filled
+        // to be consumed or give up after a short bound
+        int dummy = 0;
+        for (int i = (it > STAGES ? it - STAGES : 0); i < it; ++i)
+          (void)mbar_wait_bounded(&empty_bar[i % STAGES], (uint32_t)(i / STAGES) & 1u, &dummy, nullptr,
+                                  100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ------------------------------------------------------- MMA issuer
+      const uint32_t idesc = idesc_f32acc(256, BN, args.type == OPND_BF16);
+      int it = 0, lt = 0;
+      for (int t = unit0; t < total && !abort_sh; t += unit_step, ++lt) {
+        const int buf = lt & 1;
+        const uint32_t use = (uint32_t)(lt >> 1);
+        if (!mbar_wait_bounded(&acce_bar[buf], (use & 1u) ^ 1u, &abort_sh, args.status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * BN);
+        for (int kb = 0; kb < kb_total; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          if (!mbar_wait_bounded(&full_bar[s], ph, &abort_sh, args.status)) break;
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + s * kStage);
+          const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            tc_mma_f16_pair(d, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), idesc,
+                            (kb | k) ? 1u : 0u);
+          tc_commit_pair(&empty_bar[s], (uint16_t)3);
+        }
+        tc_commit_pair(&accf_bar[buf], (uint16_t)3);
+      }
+    }
+  } else {
+    // --------------------------------------------------------- epilogue
+    const int r = 32 * (warp & 3) + lane;  // TMEM lane quarter of this warp
+    const uint32_t t_row = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const int grp = (warp - 2) >> 2, bar = 1 + grp;
+    float* gx = xchg + grp * 2 * kXchg;   // this group's two exchange buffers
+    constexpr int ntok = 16;
+    constexpr int n_chunks = T / 16;
+    int lt = 0;
+    unsigned xc = 0;
+    for (int t = unit0; t < total; t += unit_step, ++lt) {
+      const int tile_m = t % m_tiles, tile_n = (t / m_tiles) * 2 + (int)rank;
+      const int buf = lt & 1;
+      const uint32_t use = (uint32_t)(lt >> 1);
+      const bool ok = mbar_wait_bounded(&accf_bar[buf], use & 1u, &abort_sh, args.status);
+      epi_sync(bar);
+      if (!ok || abort_sh) break;
+      tc_fence_after();
+      const uint32_t base = t_row + (uint32_t)(buf * BN);
+      const bool live = tile_n < n_tiles;  // the last unit may hold one weight tile
+      for (int c = grp; c < n_chunks; c += 2) {
+        float v[16];
+        uint32_t raw[16];
+        tmem_ld_x16(base + c * 16, raw);
+        tc_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]);
+        if (c + 2 >= n_chunks) {
+          // every column of this accumulator is in registers: hand it back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&acce_bar[buf]), 0));
+        }
+        if (live)
+          epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, gx + (xc++ & 1) * kXchg,
+                         bar);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  // the peer may still read this CTA's stages (MMA) or arrive on its barriers
+  cluster_arrive();
+  cluster_wait();
+  if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
+}
+
 // ------------------------------------------------------------------ launch
 
 
@@ -685,6 +899,56 @@ int launch_persistent(const GemmAMaps& A, const CUtensorMap& tmB, const GemmAOpt
   return DFLASH_OK;
 }
 
+template <int BN, int STAGES>
+int launch_pair(const GemmAMaps& A, const CUtensorMap& tmB, const GemmAOpts& ao, const GemmArgs& args,
+                const GemmEpi& epi, int n_tiles, int m_tiles, int num_sms, cudaStream_t s, bool pdl) {
+  auto kern = gemm_tc_pair_kernel<BN, STAGES>;
+  constexpr size_t smem = (size_t)STAGES * (kABytes + BN / 2 * kBK * 2) + 4 * kXchg * 4 + 1024;
+  static int max_pairs = -1;
+  if (max_pairs < 0) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return DFLASH_ERR_LAUNCH;
+    // how many pairs fit at once: a persistent grid must not exceed it
+    cudaLaunchConfig_t q = {};
+    q.gridDim = dim3(2 * (num_sms / 2));
+    q.blockDim = dim3(320);
+    q.dynamicSmemBytes = smem;
+    cudaLaunchAttribute qa[1];
+    qa[0].id = cudaLaunchAttributeClusterDimension;
+    qa[0].val.clusterDim.x = 2;
+    qa[0].val.clusterDim.y = 1;
+    qa[0].val.clusterDim.z = 1;
+    q.attrs = qa;
+    q.numAttrs = 1;
+    int nc = 0;
+    if (cudaOccupancyMaxActiveClusters(&nc, kern, &q) != cudaSuccess || nc < 1) {
+      (void)cudaGetLastError();
+      return DFLASH_ERR_LAUNCH;
+    }
+    max_pairs = nc;
+  }
+  const int units = ((n_tiles + 1) / 2) * m_tiles;
+  const int pairs = units < max_pairs ? units : max_pairs;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(320);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  if (cudaLaunchKernelEx(&cfg, kern, A, tmB, ao, args, epi, n_tiles, m_tiles) != cudaSuccess)
+    return DFLASH_ERR_LAUNCH;
+  return DFLASH_OK;
+}
+
 }  // namespace
 
 // Launch of one token-tile width: the non-persistent kernel on `grid`, or the
@@ -692,6 +956,10 @@ int launch_persistent(const GemmAMaps& A, const CUtensorMap& tmB, const GemmAOpt
 #define DFL_TILE_CASES_ONE(X) X(16, 6) X(32, 5) X(64, 4)
 #define DFL_TILE_CASES_LO(X) X(80, 6) X(96, 6) X(112, 6) X(128, 6) X(144, 5) X(160, 5)
 #define DFL_TILE_CASES_HI(X) X(176, 5) X(192, 4) X(208, 4) X(224, 4) X(240, 4) X(256, 4)
+// pair kernel: stages of 16 KiB + BN * 64 bytes within about 192 KiB
+#define DFL_PAIR_CASES(X)                                                                    \
+  X(80, 8) X(96, 8) X(112, 8) X(128, 8) X(144, 7) X(160, 7) X(176, 7) X(192, 6) X(208, 6) \
+  X(224, 6) X(240, 6) X(256, 6)
 
 int launch_tile_lo(int BN, bool persistent, const GemmAMaps& A, const CUtensorMap& tmB,
                    const GemmAOpts& ao, const GemmArgs& args, const GemmEpi& epi, dim3 grid,
@@ -699,5 +967,10 @@ int launch_tile_lo(int BN, bool persistent, const GemmAMaps& A, const CUtensorMa
 int launch_tile_hi(int BN, bool persistent, const GemmAMaps& A, const CUtensorMap& tmB,
                    const GemmAOpts& ao, const GemmArgs& args, const GemmEpi& epi, dim3 grid,
                    int n_tiles, int m_tiles, int num_sms, cudaStream_t s, bool pdl);
+// The pair kernel of one token-tile width; tmB_half describes boxes of BN / 2
+// token rows.
+int launch_tile_pair(int BN, const GemmAMaps& A, const CUtensorMap& tmB_half, const GemmAOpts& ao,
+                     const GemmArgs& args, const GemmEpi& epi, int n_tiles, int m_tiles, int num_sms,
+                     cudaStream_t s, bool pdl);
 
 }  // namespace dfl
