@@ -258,8 +258,10 @@ class Cycle:
 GEMM_TRAFFIC_PER_PASS = 4878.1e6
 
 
-def gpu_launches_per_step(dims, with_append=True):
-    per_layer = 7       # QKV, attention, O, RMSNorm, gate|up, down, RMSNorm
+def gpu_launches_per_step(dims, tokens, with_append=True):
+    # QKV, attention, O, RMSNorm, gate|up, down, RMSNorm; up to 32 tokens the
+    # RMSNorms run inside the GEMMs that consume them
+    per_layer = 5 if tokens <= 32 else 7
     n = 1 + per_layer * dims["n_layers"] + 2          # embed+norm, layers, LM head, top-k
     n += 1                                            # verify
     if with_append:
@@ -372,7 +374,7 @@ def run_ours(args, rank, ws):
         "stage_ms": {"ctx_append": round(t_app, 4), "draft_block": round(t_draft, 4),
                      "verify": round(t_ver, 4), "target_stand_in_excluded": round(t_stand, 4)},
         "clocks": clk, "e2e": e2e,
-        "gpu_launches": gpu_launches_per_step(dims) * args.steps,
+        "gpu_launches": gpu_launches_per_step(dims, B * G) * args.steps,
         "roofline": roof,
     }
     if extras:

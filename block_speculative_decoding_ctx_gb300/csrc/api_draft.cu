@@ -109,6 +109,7 @@ struct DraftWs {
   void* hf;
   float* logits;
   float2* rope_cs;
+  float* ssq;  // [hidden / 128][M] per-tile sums of squares of the stream
   float* gemm_partial;
   unsigned long long* topk_keys;
   float* topk_ml;
@@ -139,6 +140,7 @@ DraftWs draft_layout(const dflash_handle* h, void* base) {
   w.hf = cv.take<uint16_t>(R * c.hidden);
   w.logits = cv.take<float>(R * c.vocab);
   w.rope_cs = cv.take<float2>(M * (c.head_dim / 2));
+  w.ssq = cv.take<float>((size_t)((c.hidden + 127) / 128) * M);
   w.gemm_partial = cv.take<float>(kGemmPartialFloats);
   w.topk_keys = cv.take<unsigned long long>(R * chunks * 16);
   w.topk_ml = cv.take<float>(R * chunks * 2);
@@ -242,10 +244,11 @@ void prof_end(dflash_handle* h, cudaStream_t s, int slot, double bytes, int kind
 
 // Launch one draft GEMM.  bytes = algorithmic bytes of the launch.
 int draft_gemm(dflash_handle* h, const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void* x,
-               int M, int K, const GemmEpi& e, const GemmScratch& sc, cudaStream_t s, double bytes) {
+               int M, int K, const GemmEpi& e, const GemmScratch& sc, cudaStream_t s, double bytes,
+               const GemmRowScale* rs = nullptr) {
   const int slot = prof_begin(h, s);
   const int rc = launch_gemm(A, ao, n_tiles, x, OPND_F16, M, K, e, sc, splits_for(h, n_tiles, M, K),
-                             s, true);
+                             s, true, rs);
   if (rc) return rc;
   prof_end(h, s, slot, bytes, DFLASH_KIND_GEMM);
   return DFLASH_OK;
@@ -541,6 +544,18 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
   // tokens the epilogue adds it itself and the latency-bound RMSNorm reads
   // one array.
   const bool defer = M > kFreeResidTokens;
+  // With token tiles of at most 32 there is no RMSNorm launch: the O and down
+  // epilogues write the next GEMM's input fp16(x * g) and per-tile sums of
+  // squares of the updated stream, and the next GEMM scales its outputs by the
+  // norm's rstd (GemmRowScale).
+  const bool fuse_norm = !defer && gemm_token_tile(M) <= 32;
+  const int d_tiles = (d + 127) / 128;
+  GemmRowScale rsc;
+  rsc.ssq = ws.ssq;
+  rsc.parts = d_tiles;
+  rsc.n = d;
+  rsc.eps = c.eps;
+  const double ssq_bytes = fuse_norm ? 4.0 * d_tiles * M : 0.0;
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerMaps& lm = h->maps[l];
     const dflash_layer_weights& L = h->layers[l];
@@ -554,8 +569,11 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
       e.rope_rows = (c.n_q_heads + c.n_kv_heads) * hd;
       e.hd = hd;
       const int nt = (qkv_dim + 127) / 128;
+      // layer 0 reads the embedding's RMSNorm; later layers fold theirs in
+      const bool rs_here = fuse_norm && l > 0;
       rc = draft_gemm(h, A, single_map(), nt, ws.h, M, d, e, scratch, s,
-                      2.0 * qkv_dim * d + 2.0 * M * d + 2.0 * M * qkv_dim);
+                      2.0 * qkv_dim * d + 2.0 * M * d + 2.0 * M * qkv_dim + (rs_here ? ssq_bytes : 0.0),
+                      rs_here ? &rsc : nullptr);
       if (rc) return rc;
     }
     slot = prof_begin(h, s);
@@ -568,16 +586,24 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
       A.map[0] = lm.o;
       GemmEpi e = defer ? epi_base(EPI_F32, M, d, ws.y, d, ws.status)
                         : epi_base(EPI_RESID, M, d, ws.x, d, ws.status);
+      if (fuse_norm) {  // the MLP's RMSNorm input and sums of squares
+        e.ssq = ws.ssq;
+        e.xg = static_cast<__half*>(ws.h);
+        e.xg_g = static_cast<const float*>(L.g_mlp);
+      }
       const int nt = (d + 127) / 128;
       rc = draft_gemm(h, A, single_map(), nt, ws.attn, M, qd, e, scratch, s,
-                      2.0 * d * qd + 2.0 * M * qd + (defer ? 4.0 : 8.0) * M * d);
+                      2.0 * d * qd + 2.0 * M * qd + (defer ? 4.0 : 8.0) * M * d +
+                          (fuse_norm ? 2.0 * M * d + ssq_bytes : 0.0));
       if (rc) return rc;
     }
-    slot = prof_begin(h, s);
-    rc = launch_add_rmsnorm(ws.x, defer ? ws.y : nullptr, 1, M, d, static_cast<const float*>(L.g_mlp),
-                            c.eps, 0, ws.h, ws.status, s);
-    if (rc) return rc;
-    prof_end(h, s, slot, (double)M * d * (defer ? 14 : 6), DFLASH_KIND_NORM);
+    if (!fuse_norm) {
+      slot = prof_begin(h, s);
+      rc = launch_add_rmsnorm(ws.x, defer ? ws.y : nullptr, 1, M, d, static_cast<const float*>(L.g_mlp),
+                              c.eps, 0, ws.h, ws.status, s);
+      if (rc) return rc;
+      prof_end(h, s, slot, (double)M * d * (defer ? 14 : 6), DFLASH_KIND_NORM);
+    }
     {  // gate | up + SwiGLU
       GemmAMaps A;
       A.map[0] = lm.gate;
@@ -588,7 +614,8 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
       GemmEpi e = epi_base(EPI_SWIGLU, M, c.ffn, ws.mlp, c.ffn, ws.status);
       const int nt = c.ffn / 64;
       rc = draft_gemm(h, A, ao, nt, ws.h, M, d, e, scratch, s,
-                      4.0 * c.ffn * d + 2.0 * M * d + 2.0 * M * c.ffn);
+                      4.0 * c.ffn * d + 2.0 * M * d + 2.0 * M * c.ffn + ssq_bytes,
+                      fuse_norm ? &rsc : nullptr);
       if (rc) return rc;
     }
     {  // down (+ residual, here or in the next RMSNorm)
@@ -596,11 +623,18 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
       A.map[0] = lm.down;
       GemmEpi e = defer ? epi_base(EPI_F32, M, d, ws.y, d, ws.status)
                         : epi_base(EPI_RESID, M, d, ws.x, d, ws.status);
+      if (fuse_norm) {  // the next layer's (or the final) RMSNorm input and sums of squares
+        e.ssq = ws.ssq;
+        e.xg = static_cast<__half*>(ws.h);
+        e.xg_g = static_cast<const float*>(l + 1 < c.n_layers ? h->layers[l + 1].g_attn : h->w.g_final);
+      }
       const int nt = (d + 127) / 128;
       rc = draft_gemm(h, A, single_map(), nt, ws.mlp, M, c.ffn, e, scratch, s,
-                      2.0 * d * c.ffn + 2.0 * M * c.ffn + (defer ? 4.0 : 8.0) * M * d);
+                      2.0 * d * c.ffn + 2.0 * M * c.ffn + (defer ? 4.0 : 8.0) * M * d +
+                          (fuse_norm ? 2.0 * M * d + ssq_bytes : 0.0));
       if (rc) return rc;
     }
+    if (fuse_norm) continue;
     slot = prof_begin(h, s);
     const float* add = defer ? ws.y : nullptr;
     if (l + 1 < c.n_layers)
@@ -616,10 +650,19 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
   {  // shared LM head on the gamma - 1 MASK rows
     GemmAMaps A;
     A.map[0] = h->lm_head;
-    GemmEpi e = epi_base(EPI_F32, R, c.vocab, logits, c.vocab, ws.status);
     const int nt = (c.vocab + 127) / 128;
-    rc = draft_gemm(h, A, single_map(), nt, ws.hf, R, d, e, scratch, s,
-                    2.0 * c.vocab * d + 2.0 * R * d + 4.0 * R * c.vocab);
+    if (fuse_norm) {
+      // the final RMSNorm folded in: all M rows of the stream in (the anchors
+      // share the token tile), the MASK rows' logits out
+      GemmEpi e = epi_base(EPI_F32, M, c.vocab, logits, c.vocab, ws.status);
+      e.out_gather = gamma;
+      rc = draft_gemm(h, A, single_map(), nt, ws.h, M, d, e, scratch, s,
+                      2.0 * c.vocab * d + 2.0 * M * d + 4.0 * R * c.vocab + ssq_bytes, &rsc);
+    } else {
+      GemmEpi e = epi_base(EPI_F32, R, c.vocab, logits, c.vocab, ws.status);
+      rc = draft_gemm(h, A, single_map(), nt, ws.hf, R, d, e, scratch, s,
+                      2.0 * c.vocab * d + 2.0 * R * d + 4.0 * R * c.vocab);
+    }
     if (rc) return rc;
   }
   const int k_eff = topk > 0 ? topk : 1;

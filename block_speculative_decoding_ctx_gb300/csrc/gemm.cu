@@ -95,9 +95,10 @@ int gemm_plan_splits(int tiles, int K, int target_ctas) {
 
 int launch_gemm(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void* x, int type,
                 int M, int K, const GemmEpi& epi, const GemmScratch& scratch, int splits,
-                cudaStream_t s, bool pdl) {
+                cudaStream_t s, bool pdl, const GemmRowScale* rs) {
   const int BN = gemm_token_tile(M);
   const int T = BN;
+  if (rs && (T > 32 || !rs->ssq || rs->parts < 1 || rs->n < 1)) return DFLASH_ERR_UNSUPPORTED;
   CUtensorMap tmB;
   int rc = encode_2d(&tmB, x, type, (uint64_t)K, (uint64_t)M, kBK, (uint32_t)T);
   if (rc) return rc;
@@ -124,8 +125,12 @@ int launch_gemm(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void
   args.partial = scratch.partial;
   args.counters = scratch.counters;
   args.status = scratch.status;
+  args.rs_ssq = rs ? rs->ssq : nullptr;
+  args.rs_parts = rs ? rs->parts : 0;
+  args.rs_n = rs ? rs->n : 0;
+  args.rs_eps = rs ? rs->eps : 0.0f;
   // many token columns and no split-K: the persistent kernel
-  const bool persistent = splits == 1 && T >= 64 && (size_t)n_tiles * m_tiles >= (size_t)scratch.num_sms;
+  const bool persistent = !rs && splits == 1 && T >= 64 && (size_t)n_tiles * m_tiles >= (size_t)scratch.num_sms;
   dim3 grid(n_tiles, m_tiles, splits);
   if (persistent && DFLASH_GEMM_PAIR && BN >= 80) {
     CUtensorMap tmBh;

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -46,6 +47,26 @@ struct GemmArgs {
   float* partial;   // [tiles][splits][T][128] when cluster == 0
   int* counters;    // [tiles] when cluster == 0, zero between launches
   int* status;
+  // Row scale (see GemmRowScale); rs_ssq == nullptr: none.
+  const float* rs_ssq;
+  int rs_parts;
+  int rs_n;
+  float rs_eps;
+};
+
+// RMSNorm folded into the GEMM that consumes it.  The residual-add epilogue of
+// the GEMM that last updated the fp32 stream x wrote X = fp16(x * g) (the
+// norm's gains, GemmEpi::xg) and, per 128-row tile p, the sums over its rows
+// of x^2 (GemmEpi::ssq: ssq[p][token]).  The consuming GEMM multiplies every
+// accumulator value of token m by rstd(m) = 1 / sqrt(sum_p ssq[p][m] / n +
+// eps), which makes its input RMSNorm(x) * g up to rounding.  Used for token
+// tiles of at most 32, where a separate RMSNorm launch would cost more than
+// the pass's arithmetic.
+struct GemmRowScale {
+  const float* ssq;  // [parts][M]
+  int parts;
+  int n;             // row length of the stream (the norm's mean divides by it)
+  float eps;
 };
 
 struct GemmEpi {
@@ -71,6 +92,16 @@ struct GemmEpi {
   const int32_t* n_new;
   const int32_t* req_slot;
   int layer0;
+  // EPI_RESID: per weight tile, the sums over its rows of the updated stream's
+  // squares, ssq[tile][token], and xg = fp16(stream * xg_g) [M][ld]: the input
+  // of the next GEMM, which applies the RMSNorm's rstd (GemmRowScale); or
+  // nullptr
+  float* ssq;
+  __half* xg;
+  const float* xg_g;
+  // EPI_F32: with out_gather = G > 0 only the MASK rows are written, token t
+  // to row (t / G) * (G - 1) + t % G - 1 (t % G == 0 skipped)
+  int out_gather;
   int* status;      // device status word: argument errors found on the device, and fp16
                     // outputs (or ring entries) beyond the fp16 range (DFLASH_ERR_RANGE)
 };
@@ -101,8 +132,10 @@ int gemm_plan_splits(int tiles, int K, int target_ctas);
 // Y = X W^T through the epilogue.  n_tiles = number of 128-row weight tiles
 // (SwiGLU: F / 64).  x: [M, K] row-major, of the same OperandType `type` as
 // the weights behind A.
+// With rs, every output of token m is scaled by the RMSNorm rstd rs
+// describes (token tiles of at most 32 only).
 int launch_gemm(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void* x, int type,
                 int M, int K, const GemmEpi& epi, const GemmScratch& scratch, int splits,
-                cudaStream_t s, bool pdl);
+                cudaStream_t s, bool pdl, const GemmRowScale* rs = nullptr);
 
 }  // namespace dfl

@@ -48,10 +48,14 @@ __device__ __forceinline__ void epi_sync(int bar) {
     asm volatile("bar.sync 2, 128;" ::: "memory");
 }
 
-__device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const float (&v)[16],
+__device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const float (&v_in)[16],
                                int tok_base, int tok_step, int ntok, int tile_n, int r,
-                               float* xchg, int bar) {
+                               float* xchg, int bar, const float* rs = nullptr) {
   const int kind = e.kind;
+  // row scale of a folded RMSNorm: rs[j * tok_step] is token j's rstd
+  float v[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = (rs && j < ntok) ? v_in[j] * rs[j * tok_step] : v_in[j];
   const bool needs_xchg = (kind == EPI_QKV || kind == EPI_SWIGLU || kind == EPI_KV_RING);
   if (needs_xchg) {
 #pragma unroll
@@ -63,32 +67,71 @@ __device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts
   // each wait for a full memory round trip.
   if (kind == EPI_F32 || kind == EPI_F16 || kind == EPI_RESID) {
     const int n = tile_n * 128 + r;
+    float nw[16];  // EPI_RESID: the updated stream, zero outside the tile
+#pragma unroll
+    for (int j = 0; j < 16; ++j) nw[j] = 0.0f;
     if (n < e.N) {
       if (kind == EPI_RESID) {
         float* out = static_cast<float*>(e.out);
-        float old[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int tok = tok_base + j * tok_step;
-          old[j] = (j < ntok && tok < e.M) ? __ldcg(out + (size_t)tok * e.ld + n) : 0.0f;
+          nw[j] = (j < ntok && tok < e.M) ? __ldcg(out + (size_t)tok * e.ld + n) + v[j] : 0.0f;
         }
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int tok = tok_base + j * tok_step;
-          if (j < ntok && tok < e.M) out[(size_t)tok * e.ld + n] = old[j] + v[j];
+          if (j < ntok && tok < e.M) out[(size_t)tok * e.ld + n] = nw[j];
+        }
+        if (e.xg) {
+          const float gn = __ldg(e.xg_g + n);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tok = tok_base + j * tok_step;
+            if (j < ntok && tok < e.M) e.xg[(size_t)tok * e.ld + n] = to_f16_checked(nw[j] * gn, e.status);
+          }
         }
       } else {
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int tok = tok_base + j * tok_step;
           if (j < ntok && tok < e.M) {
-            const size_t o = (size_t)tok * e.ld + n;
-            if (kind == EPI_F32)
+            int row = tok;
+            if (e.out_gather > 0) {  // MASK rows only
+              const int G = e.out_gather, jj = tok % G;
+              row = jj ? (tok / G) * (G - 1) + jj - 1 : -1;
+            }
+            const size_t o = (size_t)row * e.ld + n;
+            if (row < 0) {
+            } else if (kind == EPI_F32) {
               static_cast<float*>(e.out)[o] = v[j];
-            else
+            } else {
               store_f16(e, o, v[j]);
+            }
           }
         }
+      }
+    }
+    if (kind == EPI_RESID && e.ssq) {
+      // sum over this tile's 128 rows of each token's squared stream values
+      // (warp butterflies, then the group's four warps in order): the next
+      // GEMM's RMSNorm adds these per-tile sums
+      const int q = r >> 5, lane = r & 31;
+      float mine = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        float sq = nw[j] * nw[j];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        if (lane == j) mine = sq;
+      }
+      if (lane < 16) xchg[q * 16 + lane] = mine;
+      epi_sync(bar);
+      if (q == 0 && lane < 16) {
+        const int tok = tok_base + lane * tok_step;
+        if (lane < ntok && tok < e.M)
+          e.ssq[(size_t)tile_n * e.M + tok] =
+              (xchg[lane] + xchg[16 + lane]) + (xchg[32 + lane] + xchg[48 + lane]);
       }
     }
   } else if (kind == EPI_QKV) {
@@ -207,6 +250,7 @@ __global__ void __launch_bounds__(gemm_threads(BN), 1)
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ int last_sh;
+  __shared__ float rs_sh[BN <= 32 ? 32 : 1];  // row scale (RMSNorm rstd) of the tile's tokens
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile_n = blockIdx.x, tile_m = blockIdx.y, split = blockIdx.z;
@@ -307,6 +351,22 @@ __global__ void __launch_bounds__(gemm_threads(BN), 1)
     }
     tc_commit(&acc_bar);
   }
+  if constexpr (BN <= 32) {
+    if (warp == 2 && args.rs_ssq) {
+      // rstd of the tile's tokens for a folded RMSNorm, while the mainloop runs
+      grid_dependency_wait();
+      if (lane < BN) {
+        const int m = tile_m * BN + lane;
+        float rsv = 0.0f;
+        if (m < epi.M) {
+          float ss = 0.0f;
+          for (int p = 0; p < args.rs_parts; ++p) ss += __ldcg(args.rs_ssq + (size_t)p * epi.M + m);
+          rsv = rsqrtf(ss / (float)args.rs_n + args.rs_eps);
+        }
+        rs_sh[lane] = rsv;
+      }
+    }
+  }
   __syncwarp();
 
   // ----------------------------------------------------------- epilogue
@@ -338,12 +398,14 @@ __global__ void __launch_bounds__(gemm_threads(BN), 1)
     for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]);
   };
 
+  const float* rs_tile = (BN <= 32 && args.rs_ssq) ? rs_sh : nullptr;  // by local token
   if (args.splits == 1) {
     if (!aborted) {
       for (int c = grp, it = 0; c < n_chunks; c += kGroups, ++it) {
         float v[16];
         load_chunk(c, v);
-        epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg + (it & 1) * kXchg, bar);
+        epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg + (it & 1) * kXchg, bar,
+                       rs_tile ? rs_tile + c * 16 : nullptr);
       }
     }
   } else if (!args.cluster) {
@@ -379,7 +441,7 @@ __global__ void __launch_bounds__(gemm_threads(BN), 1)
             for (int j = 0; j < 16; ++j) v[j] += __ldcg(ps + (c * 16 + j) * 128 + r);
           }
           epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg + (it & 1) * kXchg,
-                         bar);
+                         bar, rs_tile ? rs_tile + c * 16 : nullptr);
         }
       }
       if (threadIdx.x == 0) atomicExch(&args.counters[tile_lin], 0);
@@ -425,7 +487,7 @@ __global__ void __launch_bounds__(gemm_threads(BN), 1)
         }
         const int cnt = mine - g0 < 16 ? mine - g0 : 16;
         epilogue_chunk(epi, ao, v, tile_m * T + rank + g0 * S, S, cnt, tile_n, r,
-                       xchg_s + (it & 1) * kXchg, bar);
+                       xchg_s + (it & 1) * kXchg, bar, rs_tile ? rs_tile + rank + g0 * S : nullptr);
       }
     }
     // no CTA may leave while another still reads its shared memory
