@@ -253,9 +253,10 @@ class Cycle:
 # DRAM bytes (read + written) of the draft pass's GEMM launches at batch 1,
 # gamma 8, five layers: ncu's dram__bytes_read.sum + dram__bytes_write.sum per
 # launch on a one-layer pass (4 GEMMs per layer + the LM head), scaled to five
-# layers.  Taken with the GEMM kernels as of the fp16-operand, gathered-epilogue
-# version; 4,871,029,248 algorithmic bytes.
-GEMM_TRAFFIC_PER_PASS = 4878.1e6
+# layers.  Taken with the GEMM kernels that fold the RMSNorms in at this
+# batch (residual-add epilogues also write fp16(x * g) and per-tile sums of
+# squares); 4,871,884,288 algorithmic bytes.
+GEMM_TRAFFIC_PER_PASS = 4879.1e6
 
 
 def gpu_launches_per_step(dims, tokens, with_append=True):

@@ -30,11 +30,14 @@ CASES = [
     ("tiny", 2, 4, [64, 30]),
     ("tiny", 3, 4, [0, 1, 65]),
     ("small", 3, 8, [300, 256, 17]),
-    # batch >= 4 runs attention on tcgen05: head dim 64, ragged, empty and wrapped windows
+    # head dim 64 with ragged, empty and wrapped windows
     ("tiny", 4, 4, [64, 30, 0, 200]),
     ("small", 5, 8, [300, 256, 17, 0, 1000]),
     ("small128", 2, 16, [512, 700]),
     ("small128", 4, 8, [100, 513, 1, 2000]),
+    # 17-32 tokens: RMSNorm folded into the GEMMs, split-K through clusters
+    ("small", 4, 8, [300, 17, 256, 1000]),
+    ("small128", 3, 8, [100, 513, 2000]),
     ("wide", 16, 8, [256] * 8 + [10, 300, 40, 999, 257, 255, 1, 0]),
     ("wide", 32, 8, [300] * 32),
     ("wide", 20, 16, [180] * 20),
