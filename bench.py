@@ -270,6 +270,30 @@ def gpu_launches_per_step(dims, tokens, with_append=True):
     return n
 
 
+def acceptance_stats(cyc, g_step, stream, B, G, steps, sigma):
+    """Accepted lengths over untimed replays of the cycle: the distribution of
+    tau (accepted drafts + 1), the rate at which draft position i is accepted
+    (tau >= i + 1), and that rate given position i - 1 was accepted (the decay
+    along the block)."""
+    dev = cyc.n_app.device
+    hist = torch.zeros(G + 1, dtype=torch.int64, device=dev)
+    ones = torch.ones(B, dtype=torch.int64, device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            g_step.replay()
+            hist.scatter_add_(0, cyc.n_app.long(), ones)
+    stream.synchronize()
+    h = hist.cpu().tolist()
+    n = max(sum(h), 1)
+    at_least = [sum(h[t] for t in range(i + 1, G + 1)) / n for i in range(1, G)]
+    given = [at_least[0]] + [at_least[i] / at_least[i - 1] if at_least[i - 1] > 0 else None
+                             for i in range(1, G - 1)]
+    return {"cycles": steps, "requests_per_cycle": B, "sigma": sigma, "tau_hist": h,
+            "tau_mean": round(sum(t * c for t, c in enumerate(h)) / n, 3),
+            "accept_rate_by_position": [round(a, 4) for a in at_least],
+            "accept_rate_given_previous": [None if g is None else round(g, 4) for g in given]}
+
+
 def run_ours(args, rank, ws):
     import block_speculative_decoding_ctx_gb300 as dfl
     dfl.lib()
@@ -314,6 +338,9 @@ def run_ours(args, rank, ws):
     t_ver = time_graph(g_ver, args.steps, stream)
     t_path = max(t_step - t_stand, 1e-6)
     t_path_max = max_over_ranks(t_path, ws)
+
+    # -------------------------- acceptance along the block (untimed replays)
+    acceptance = acceptance_stats(cyc, g_step, stream, B, G, max(64, 256 // B), args.sigma)
 
     # ------------------------------------ dominant kernel (GEMMs of the pass)
     # per-launch device times inside a replayed graph (event nodes around
@@ -377,6 +404,7 @@ def run_ours(args, rank, ws):
         "clocks": clk, "e2e": e2e,
         "gpu_launches": gpu_launches_per_step(dims, B * G) * args.steps,
         "roofline": roof,
+        "acceptance": acceptance,
     }
     if extras:
         res["batches"] = extras

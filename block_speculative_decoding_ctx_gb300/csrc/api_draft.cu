@@ -208,7 +208,7 @@ RopeInv rope_inv(const dflash_config& c) {
 }
 
 int splits_for(const dflash_handle* h, int n_tiles, int M, int K) {
-  const int BN = gemm_token_tile(M);
+  const int BN = gemm_token_tile_for(M, n_tiles, h->num_sms);
   const int m_tiles = (M + BN - 1) / BN;
   const int per_sm = BN <= 64 ? 2 : 1;
   return gemm_plan_splits(n_tiles * m_tiles, K, h->num_sms * per_sm);

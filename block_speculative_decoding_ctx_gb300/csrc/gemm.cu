@@ -82,6 +82,21 @@ int gemm_token_tile(int M) {
   return (per + 15) / 16 * 16;
 }
 
+// A GEMM with fewer weight tiles than SMs whose wide token tile would take
+// exactly two K splits takes two token tiles per weight tile instead: the same
+// CTA count, no partials to reduce.
+#ifndef DFLASH_TOKEN_SPLIT
+#define DFLASH_TOKEN_SPLIT 1
+#endif
+int gemm_token_tile_for(int M, int n_tiles, int num_sms) {
+  const int T0 = gemm_token_tile(M);
+  if (!DFLASH_TOKEN_SPLIT || T0 <= 128 || n_tiles < 1) return T0;
+  const int m0 = (M + T0 - 1) / T0;
+  if (num_sms / (n_tiles * m0) != 2) return T0;
+  const int per = (M + 2 * m0 - 1) / (2 * m0);
+  return (per + 15) / 16 * 16;
+}
+
 int gemm_plan_splits(int tiles, int K, int target_ctas) {
   const int kb = (K + kBK - 1) / kBK;
   // as many splits as fit in one wave of CTA slots: a second, mostly empty
@@ -96,7 +111,7 @@ int gemm_plan_splits(int tiles, int K, int target_ctas) {
 int launch_gemm(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void* x, int type,
                 int M, int K, const GemmEpi& epi, const GemmScratch& scratch, int splits,
                 cudaStream_t s, bool pdl, const GemmRowScale* rs) {
-  const int BN = gemm_token_tile(M);
+  const int BN = gemm_token_tile_for(M, n_tiles, scratch.num_sms);
   const int T = BN;
   if (rs && (T > 32 || !rs->ssq || rs->parts < 1 || rs->n < 1)) return DFLASH_ERR_UNSUPPORTED;
   CUtensorMap tmB;

@@ -127,6 +127,8 @@ int encode_2d(CUtensorMap* map, const void* ptr, int type, uint64_t inner, uint6
               uint32_t box_inner, uint32_t box_outer);
 
 int gemm_token_tile(int M);
+// The token tile launch_gemm takes for n_tiles weight tiles on num_sms SMs.
+int gemm_token_tile_for(int M, int n_tiles, int num_sms);
 int gemm_plan_splits(int tiles, int K, int target_ctas);
 
 // Y = X W^T through the epilogue.  n_tiles = number of 128-row weight tiles

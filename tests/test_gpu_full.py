@@ -8,6 +8,7 @@ the launch configuration the benchmark times (batch 1, gamma 8, top-4).
   are compared with the oracle's H_t and K/V for those positions alone.
 * the batch-16 config: ragged log-uniform contexts; one sampled request's
   draft is recomputed by the oracle.
+* batch 32, gamma 8: two sampled requests (the wide-token-tile GEMM paths).
 Tolerance 1e-2 normwise, as for the small shapes."""
 
 import numpy as np
@@ -89,4 +90,22 @@ def test_batch16_ragged_contexts_sampled_request(full):
     ref = om.draft_pass(tu.oracle_cfg(DIMS), W, rk, rv, lens.numpy(), anchor.numpy(), gamma,
                         requests=[short, long])
     for i, b in enumerate([short, long]):
+        assert tu.rel_err(got["logits"][b], ref["logits"][i]) <= TOL
+
+
+def test_batch32_gamma8_sampled_requests(full):
+    """256 tokens: the QKV GEMM takes two 128-token tiles per weight tile (no
+    K split), gate|up and the LM head the CTA-pair persistent kernel."""
+    W, Wd = full
+    B, gamma = 32, 8
+    lens = torch.full((B,), 8192, dtype=torch.int64)
+    lens[5] = 300                                   # one partly empty window
+    rk, rv = synth.ring(DIMS, B, 91, std=1.4)
+    anchor = synth.token_ids(B, DIMS["vocab"], 92)
+    h = dfl.dflash_create(tu.lib_cfg(DIMS, batch_max=B, gamma_max=gamma), Wd)
+    got = tu.run_draft(h, anchor, lens, rk.cuda(), rv.cuda(), gamma, topk=4)
+    picks = [5, 31]
+    ref = om.draft_pass(tu.oracle_cfg(DIMS), W, rk, rv, lens.numpy(), anchor.numpy(), gamma,
+                        requests=picks)
+    for i, b in enumerate(picks):
         assert tu.rel_err(got["logits"][b], ref["logits"][i]) <= TOL
