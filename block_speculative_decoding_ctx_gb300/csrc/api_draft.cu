@@ -441,11 +441,10 @@ int dflash_ctx_append(dflash_handle* h, int B, int n_max, const void* feats, con
     const int nl = c.n_layers - l0 < kMaxAMaps ? c.n_layers - l0 : kMaxAMaps;
     GemmAMaps A;
     for (int i = 0; i < nl; ++i) A.map[i] = h->maps[l0 + i].qkv;
-    GemmAOpts ao;
+    GemmAOpts ao = single_map();
     ao.n_maps = nl;
     ao.tiles_per_map = tiles_per_layer;
     ao.row_offset = c.n_q_heads * c.head_dim;
-    ao.dual = 0;
     GemmEpi e = epi_base(EPI_KV_RING, M, nl * 2 * kvd, nullptr, 0, ws.status);
     e.ctx_len = ctx_len;
     e.rope_cs = ws.rope_cs;
