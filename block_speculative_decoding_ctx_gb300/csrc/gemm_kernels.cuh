@@ -101,12 +101,12 @@ __device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts
               const int G = e.out_gather, jj = tok % G;
               row = jj ? (tok / G) * (G - 1) + jj - 1 : -1;
             }
-            const size_t o = (size_t)row * e.ld + n;
-            if (row < 0) {
-            } else if (kind == EPI_F32) {
-              static_cast<float*>(e.out)[o] = v[j];
-            } else {
-              store_f16(e, o, v[j]);
+            if (row >= 0) {
+              const size_t o = (size_t)row * e.ld + n;
+              if (kind == EPI_F32)
+                static_cast<float*>(e.out)[o] = v[j];
+              else
+                store_f16(e, o, v[j]);
             }
           }
         }
