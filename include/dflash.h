@@ -2,7 +2,7 @@
  * dflash.h — C ABI of libdflash.so: single-pass block drafting with target
  * context injection, plus lossless verification, on one GB300 (sm_103a).
  *
- * What the library computes (sources are the three pages this build follows):
+ * What the library computes (sources are the three pages it follows):
  *   - "DFlash vs DFlash 2" (blog), section "Conditioning on the target model":
  *       H_t = RMSNorm(W_c [H^(l1); ...; H^(l5)]),
  *       Q_i = W^Q_i H_d,  K_i = [W^K_i H_t ; W^K_i H_d],  V_i = [W^V_i H_t ; W^V_i H_d];

@@ -14,7 +14,7 @@ Sources
   [doc]   "Speculative decoding" product doc, section "How it works" (top
           candidates kept per position; window keeps draft cost flat).
 
-Readings of this build where the pages are silent (parity with the oracle is
+Readings taken here where the pages are silent (parity with the oracle is
 parity with these readings):
   * positions: RoPE (rotate-half pairs (j, j + hd/2), inv_freq_j =
     theta^(-2j/hd)) on queries and keys at absolute positions; context keys

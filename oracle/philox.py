@@ -12,8 +12,8 @@ M0*c0 and M1*c2 and sets
 
 after which the key is bumped by the Weyl constants (W0, W1).  Ten rounds.
 
-How the uniforms of this build are taken from one output block (w0..w3) is a
-convention of this build; the pages name no generator:
+How the uniforms are taken from one output block (w0..w3) is a
+convention of this library and its oracle; the pages name no generator:
 
     counter = (step_lo, step_hi, position, purpose), key = (seed_lo, seed_hi)
     purpose 0: the drafter's draw y ~ q;  1: the accept test;  2: the

@@ -4,8 +4,8 @@ Test infrastructure only (see the package docstring).
 
 * ``probs``: p = top_p(softmax(logits / T)).  The model card
   "Beam-1.0-501B-A23B-DFlash2" (section "Acceptance length") samples at
-  temperature 0.7 and top-p 0.99.  The pages do not define top-p; this build
-  reads it as the usual nucleus rule: order the ids by (probability desc, id
+  temperature 0.7 and top-p 0.99.  The pages do not define top-p; it is
+  read here as the usual nucleus rule: order the ids by (probability desc, id
   asc), keep the shortest prefix whose probability mass reaches top_p, zero
   the rest and renormalise.  The same preparation is applied to the target's
   p and the drafter's q.

@@ -21,7 +21,7 @@ Result: accept_len int32 [B] (n, 0 <= n <= G) and tokens int32 [B, gamma]
 with tokens[:n] = y_1..y_n, tokens[n] = the correction or bonus and the
 rest -1.  tau = n + 1.
 
-Readings of this build where the pages are silent:
+Readings taken here where the pages are silent:
   * greedy ties go to the lowest id;
   * the accept test u < p/q is evaluated as u*q(y) < p(y) in float64 with
     u = u24 * 2^-24, which is exact (24-bit times 24-bit mantissas);

@@ -84,7 +84,7 @@ def test_topk_and_logsumexp_against_brute_force_and_scipy():
 
 def test_drafter_parameter_count_against_model_card():
     """Model card "Beam-1.0-501B-A23B-DFlash2", section "Model": 1.93B
-    parameters.  The matrices this build owns (5 layers + W_c; embedding and
+    parameters.  The matrices the drafter owns (5 layers + W_c; embedding and
     LM head are shared with the target) come to 1,782,579,200, below the
     card's figure by the size of the DFlash 2 modules that are out of scope."""
     n = om.drafter_matrix_params(cfg_of("full"))
