@@ -283,13 +283,20 @@ def acceptance_stats(cyc, g_step, stream, B, G, steps, sigma):
             g_step.replay()
             hist.scatter_add_(0, cyc.n_app.long(), ones)
     stream.synchronize()
-    h = hist.cpu().tolist()
+    out = {"cycles": steps, "requests_per_cycle": B, "sigma": sigma}
+    out.update(acceptance_rates(hist.cpu().tolist(), G))
+    return out
+
+
+def acceptance_rates(h, G):
+    """From a histogram h[tau] (tau = 1..G): the mean, the rate at which draft
+    position i = 1..G-1 is accepted (tau >= i + 1) and that rate given that
+    position i - 1 was accepted."""
     n = max(sum(h), 1)
     at_least = [sum(h[t] for t in range(i + 1, G + 1)) / n for i in range(1, G)]
     given = [at_least[0]] + [at_least[i] / at_least[i - 1] if at_least[i - 1] > 0 else None
                              for i in range(1, G - 1)]
-    return {"cycles": steps, "requests_per_cycle": B, "sigma": sigma, "tau_hist": h,
-            "tau_mean": round(sum(t * c for t, c in enumerate(h)) / n, 3),
+    return {"tau_hist": list(h), "tau_mean": round(sum(t * c for t, c in enumerate(h)) / n, 3),
             "accept_rate_by_position": [round(a, 4) for a in at_least],
             "accept_rate_given_previous": [None if g is None else round(g, 4) for g in given]}
 
