@@ -212,6 +212,10 @@ typedef struct dflash_draft_out {
  *   anchor     int32 [B];  ctx_len int64 [B] (0 allowed: the block alone)
  *   req_slot   int32 [B] or NULL;  ring_k/v as in ctx_append
  *   sampling   host pointer or NULL (greedy drafting)
+ * Device status (dflash_read_status): DFLASH_ERR_RANGE if an fp16 activation
+ * between kernels would exceed +-65504.  With B * gamma <= 32 the layers'
+ * RMSNorms are folded into the GEMMs around them and one of those activations
+ * is the unnormalised residual stream times the norm's gains.
  */
 int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor,
                        const int64_t* ctx_len, const int32_t* req_slot,
