@@ -10,14 +10,18 @@
 // activations rounded to 11 significant bits) or bf16 (W_c with the target's
 // bf16 features); kind::f16 takes both, A and B of one type.
 //
-// Pipeline (one CTA = 4 warps):
+// Pipeline (one CTA = 4 warps, 8 for token tiles of 128 or more):
 //   warp 0 lane 0   TMA producer: 128x64 weight box + BNx64 token box per
 //                   stage, 128-byte swizzle, weights marked evict-first;
 //   warp 1          allocates TMEM; lane 0 issues 4 MMAs (K = 16 each) per
 //                   stage and commits the stage back to the producer;
-//   all 4 warps     epilogue: tcgen05.ld of their 32-lane quarter, then the
-//                   fused epilogue of the layer (RoPE, residual add, SwiGLU,
-//                   fp32 logits, or scatter into the context ring).
+//   warp 2          with a folded RMSNorm, the rstd of the tile's tokens
+//                   while the mainloop runs;
+//   all warps       epilogue, in groups of 4 (one warp per TMEM lane quarter)
+//                   taking alternate 16-token chunks: tcgen05.ld, then the
+//                   fused epilogue of the layer (RoPE, residual add with the
+//                   next norm's input, SwiGLU, fp32 logits, or scatter into
+//                   the context ring).
 // Split-K: the grid's z dimension partitions K.  The splits of one tile
 // either run as a thread-block cluster (each keeps its fp32 partial tile in
 // shared memory and, after a cluster barrier, every CTA of the cluster sums a
