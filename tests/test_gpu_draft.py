@@ -38,6 +38,8 @@ CASES = [
     # 17-32 tokens: RMSNorm folded into the GEMMs, split-K through clusters
     ("small", 4, 8, [300, 17, 256, 1000]),
     ("small128", 3, 8, [100, 513, 2000]),
+    # 64-token tiles with enough weight tiles for the single-CTA persistent kernel
+    ("wide", 8, 8, [300] * 4 + [17, 256, 0, 1000]),
     ("wide", 16, 8, [256] * 8 + [10, 300, 40, 999, 257, 255, 1, 0]),
     ("wide", 32, 8, [300] * 32),
     ("wide", 20, 16, [180] * 20),
