@@ -464,6 +464,13 @@ def run_e2e(args, dfl, cyc, stream, g_step):
                     "API call each step instead"}
 
 
+def attention_ring_bytes(dims, B, context):
+    """Ring K/V bytes the draft pass's attention reads: every layer, request and
+    KV head streams its visible window (min(context, W) keys) of bf16 K and V."""
+    keys = min(context, dims["window"])
+    return dims["n_layers"] * B * dims["n_kv"] * keys * dims["hd"] * 2 * 2
+
+
 def run_extras(args, dfl, dims, W, dev, stream):
     """Draft-pass throughput at batch 16 and 32 (gamma 8) and batch 32 gamma 16
     over a random full ring (context 8192 -> window 4096)."""
@@ -527,8 +534,12 @@ def run_extra(args, dfl, dims, W, dev, stream, B, G, tf_sus, src):
     head = [p for p in prof if p[2] == "gemm"][-1]
     layer0.append(["lm_head", round(head[0] * 1e3, 1),
                    round(2.0 * B * (G - 1) * d * V / (head[0] * 1e-3) / 1e12, 1)])
+    hbm = measured_peaks()[0]
+    attn_gbps = attention_ring_bytes(dims, B, 8192) / (attn_ms * 1e-3) / 1e9
     res = {"draft_blocks_per_s": round(B * 1000.0 / t, 2), "ms_per_pass": round(t, 4),
                 "gemm_ms": round(gemm_ms, 4), "attention_ms": round(attn_ms, 4),
+                "attention_ring_GBps": round(attn_gbps, 1),
+                "attention_frac_of_hbm": round(attn_gbps / hbm, 4),
                 "gemm_tflops": round(gemm_tflops, 1),
                 "gemm_frac_of_tensor_peak": round(gemm_tflops / tf_sus, 4),
                 "first_layer_gemms_us_tflops": layer0,

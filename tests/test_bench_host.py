@@ -26,3 +26,10 @@ def test_acceptance_rates_all_rejected():
     assert r["tau_mean"] == 1.0
     assert r["accept_rate_by_position"] == [0.0, 0.0]
     assert r["accept_rate_given_previous"] == [0.0, None]
+
+
+def test_attention_ring_bytes_counts_the_visible_window():
+    dims = dict(bench.DIMS_FULL)
+    # 5 layers x 32 requests x 8 KV heads x 4096 keys x 128 dims x (K, V) x 2 bytes
+    assert bench.attention_ring_bytes(dims, 32, 8192) == 5 * 32 * 8 * 4096 * 128 * 2 * 2
+    assert bench.attention_ring_bytes(dims, 1, 100) == 5 * 8 * 100 * 128 * 2 * 2
