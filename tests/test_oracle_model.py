@@ -189,31 +189,47 @@ def test_block_attention_is_non_causal_inside_the_block():
 
 # --------------------------------------------------------------- draft pass
 
-def _library_draft_pass(cfg, W, rk, rv, L, anchor, gamma):
+def _rope_c(cfg, t, pos):
+    """Rotate-half RoPE of t [n, heads, hd] at positions pos [n] as a complex
+    product: (x_j + i x_{j+hd/2}) * exp(i pos theta^(-2j/hd))."""
+    dd = torch.float64
+    j = torch.arange(cfg.hd // 2, dtype=dd)
+    pos = torch.as_tensor(np.asarray(pos), dtype=dd)
+    rot = torch.polar(torch.ones(len(pos), cfg.hd // 2, dtype=dd),
+                      pos[:, None] * cfg.rope_theta ** (-2.0 * j / cfg.hd))[:, None, :]
+    z = torch.complex(t[..., :cfg.hd // 2], t[..., cfg.hd // 2:]) * rot
+    return torch.cat([z.real, z.imag], dim=-1)
+
+
+def _library_kv(cfg, lw, h, pos):
+    """K = RoPE(W^K h, pos) and V = W^V h of normalised rows h [n, d], with
+    torch routines: the k and v row blocks of w_qkv (its rows are the q heads,
+    then the k heads, then the v heads), the rotation as a complex product."""
+    dd = torch.float64
+    qd, kd = cfg.n_q * cfg.hd, cfg.n_kv * cfg.hd
+    n = h.shape[0]
+    qkv = torch.as_tensor(np.asarray(h), dtype=dd) @ lw["w_qkv"].to(dd).T
+    k = _rope_c(cfg, qkv[:, qd:qd + kd].reshape(n, cfg.n_kv, cfg.hd), pos)
+    v = qkv[:, qd + kd:].reshape(n, cfg.n_kv, cfg.hd)
+    return k, v
+
+
+def _library_draft_pass(cfg, W, ctx_k, ctx_v, L, anchor, gamma):
     """One request through the layers with torch float64 library routines
-    (rms_norm, SDPA with GQA, silu, complex rotation)."""
+    (rms_norm, SDPA with GQA, silu, complex rotation).  ctx_k[l], ctx_v[l]
+    [n, Hkv, hd] are the visible context keys and values of layer l (any
+    order); the block forms its own keys and values with _library_kv."""
     dd = torch.float64
     ids = [anchor] + [cfg.mask_token] * (gamma - 1)
     x = W["embed"][ids].to(dd)
-    pos = torch.arange(L, L + gamma, dtype=dd)
-    j = torch.arange(cfg.hd // 2, dtype=dd)
-    rot = torch.polar(torch.ones(gamma, cfg.hd // 2, dtype=dd),
-                      pos[:, None] * cfg.rope_theta ** (-2.0 * j / cfg.hd))[:, None, :]
-
-    def rope_c(t):
-        z = torch.complex(t[..., :cfg.hd // 2], t[..., cfg.hd // 2:]) * rot
-        return torch.cat([z.real, z.imag], dim=-1)
-
-    qd, kd = cfg.n_q * cfg.hd, cfg.n_kv * cfg.hd
-    n_valid = min(L, cfg.window)
+    pos = np.arange(L, L + gamma)
+    qd = cfg.n_q * cfg.hd
     for l, lw in enumerate(W["layers"]):
         h = F.rms_norm(x, (cfg.d,), lw["g_attn"].to(dd), eps=cfg.eps)
-        qkv = h @ lw["w_qkv"].to(dd).T
-        q = rope_c(qkv[:, :qd].reshape(gamma, cfg.n_q, cfg.hd))
-        k = rope_c(qkv[:, qd:qd + kd].reshape(gamma, cfg.n_kv, cfg.hd))
-        v = qkv[:, qd + kd:].reshape(gamma, cfg.n_kv, cfg.hd)
-        keys = torch.cat([rk[l, 0].to(dd).permute(1, 0, 2)[:n_valid], k])
-        vals = torch.cat([rv[l, 0].to(dd).permute(1, 0, 2)[:n_valid], v])
+        q = _rope_c(cfg, (h @ lw["w_qkv"][:qd].to(dd).T).reshape(gamma, cfg.n_q, cfg.hd), pos)
+        k, v = _library_kv(cfg, lw, h, pos)
+        keys = torch.cat([torch.as_tensor(ctx_k[l], dtype=dd), k])
+        vals = torch.cat([torch.as_tensor(ctx_v[l], dtype=dd), v])
         o = F.scaled_dot_product_attention(q.permute(1, 0, 2)[None], keys.permute(1, 0, 2)[None],
                                            vals.permute(1, 0, 2)[None], enable_gqa=True)
         x = x + o[0].permute(1, 0, 2).reshape(gamma, qd) @ lw["w_o"].to(dd).T
@@ -221,6 +237,13 @@ def _library_draft_pass(cfg, W, rk, rv, L, anchor, gamma):
         x = x + (F.silu(h @ lw["w_gate"].to(dd).T) * (h @ lw["w_up"].to(dd).T)) @ lw["w_down"].to(dd).T
     hf = F.rms_norm(x, (cfg.d,), W["g_final"].to(dd), eps=cfg.eps)
     return (hf[1:] @ W["lm_head"].to(dd).T).numpy()
+
+
+def _ring_context(cfg, rk, rv, L):
+    """Visible context of request 0 of a ring: slots 0 .. min(L, W) - 1."""
+    n_valid = min(L, cfg.window)
+    return ([rk[l, 0].to(torch.float64).permute(1, 0, 2)[:n_valid] for l in range(cfg.n_layers)],
+            [rv[l, 0].to(torch.float64).permute(1, 0, 2)[:n_valid] for l in range(cfg.n_layers)])
 
 
 @pytest.mark.parametrize("L", [30, 64, 500])
@@ -231,7 +254,7 @@ def test_draft_pass_matches_library_layers(L):
     rk, rv = synth.ring(dims, 1, 4)
     gamma = 4
     got = om.draft_pass(cfg, W, rk, rv, [L], [17], gamma)["logits"][0]
-    want = _library_draft_pass(cfg, W, rk, rv, L, 17, gamma)
+    want = _library_draft_pass(cfg, W, *_ring_context(cfg, rk, rv, L), L, 17, gamma)
     np.testing.assert_allclose(got, want, rtol=1e-9, atol=1e-11)
 
 
@@ -260,3 +283,79 @@ def test_draft_rows_differ_through_positions():
     rk, rv = synth.ring(dims, 1, 8)
     out = om.draft_pass(cfg, W, rk, rv, [64], [3], 4)["logits"][0]
     assert np.abs(out[0] - out[1]).max() > 1e-6
+
+
+# ------------------------------------- context K/V: the injection equation
+#
+# "DFlash vs DFlash 2", section "Conditioning on the target model": the keys
+# and values of layer i are K_i = [W^K_i H_t ; W^K_i H_d] and
+# V_i = [W^V_i H_t ; W^V_i H_d] — the context half is projected by the same
+# W^K_i / W^V_i as the block half.  With rotary positions (a reading the pages
+# leave open) a context key is rotated at its own absolute position exactly
+# like a block key.
+
+@pytest.mark.parametrize("dims_name", ["tiny", "small"])
+def test_context_kv_is_the_blocks_key_value_projection(dims_name):
+    dims = dict(synth.DIMS[dims_name], n_layers=2)
+    cfg = om.Config(**dims)
+    W = synth.weights(dims, 11, random_gains=True)
+    rng = np.random.default_rng(11)
+    H = rng.normal(size=(7, cfg.d))
+    pos = np.array([0, 1, 63, 64, 1000, 65_537, 131_071])
+    Ks, Vs = om.context_kv(cfg, W, H, pos)
+    assert len(Ks) == len(Vs) == cfg.n_layers
+    for l, lw in enumerate(W["layers"]):
+        k, v = _library_kv(cfg, lw, H, pos)
+        np.testing.assert_allclose(Ks[l], k.numpy(), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(Vs[l], v.numpy(), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("L", [5, 64, 100])
+def test_appended_context_drafts_like_a_library_pass_over_projected_features(L):
+    """ctx_append (fusion, projection, rotation, ring slot pos mod W) followed
+    by the draft pass equals a library pass whose context keys and values are
+    the block's own projection routine applied to H_t = RMSNorm(W_c concat(H))
+    at positions 0 .. L-1 (the last W of them visible)."""
+    dims = dict(synth.DIMS["tiny"], n_layers=2)
+    cfg = om.Config(**dims)
+    W = synth.weights(dims, 12, random_gains=True)
+    feats = synth.features(dims, L, 13, torch.float32).numpy()
+    shape = (cfg.n_layers, 1, cfg.n_kv, cfg.window, cfg.hd)
+    rk, rv = np.zeros(shape), np.zeros(shape)
+    for s0 in range(0, L, 29):                         # ragged appends
+        om.ctx_append(cfg, W, rk, rv, 0, feats[s0:s0 + 29], s0)
+    gamma = 4
+    got = om.draft_pass(cfg, W, rk, rv, [L], [17], gamma)["logits"][0]
+
+    dd = torch.float64
+    cat = torch.as_tensor(feats, dtype=dd).reshape(L, cfg.n_feat * cfg.feat_dim)
+    H_t = F.rms_norm(cat @ W["w_c"].to(dd).T, (cfg.d,), W["g_c"].to(dd), eps=cfg.eps)
+    vis = np.arange(max(0, L - cfg.window), L)
+    ctx = [_library_kv(cfg, lw, H_t[vis], vis) for lw in W["layers"]]
+    want = _library_draft_pass(cfg, W, [c[0] for c in ctx], [c[1] for c in ctx], L, 17, gamma)
+    np.testing.assert_allclose(got, want, rtol=1e-9, atol=1e-11)
+
+
+def test_draft_over_appended_context_is_invariant_to_a_common_position_shift():
+    """Rotary scores depend only on query position minus key position: with
+    the same features filling the window at positions s0 .. s0+W-1 and the
+    block at s0+W, the logits cannot depend on s0.  Context keys left
+    unrotated, or rotated by another convention than the block's, break this."""
+    dims = synth.DIMS["tiny"]
+    cfg = om.Config(**dims)
+    W = synth.weights(dims, 14, random_gains=True)
+    n = cfg.window
+    feats = synth.features(dims, n, 15, torch.float32).numpy()
+    shape = (cfg.n_layers, 1, cfg.n_kv, cfg.window, cfg.hd)
+
+    def logits_after(fe, s0):
+        rk, rv = np.zeros(shape), np.zeros(shape)
+        om.ctx_append(cfg, W, rk, rv, 0, fe, s0)
+        return om.draft_pass(cfg, W, rk, rv, [s0 + n], [5], 4)["logits"][0]
+
+    base = logits_after(feats, 0)
+    for s0 in (37, 100_003):
+        np.testing.assert_allclose(logits_after(feats, s0), base, rtol=1e-7, atol=1e-9)
+    # the order of the context matters only through the keys' rotations:
+    # without them a reversed context would give the same logits
+    assert np.abs(logits_after(feats[::-1].copy(), 0) - base).max() > 1e-4
