@@ -29,18 +29,51 @@ static __device__ __align__(256) unsigned char g_verify_scratch[kNoAllocScratchB
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
+void* g_scratch_ctx[kMaxDevices] = {};
+
+// The CUDA context current on this thread (driver entry point, so that the
+// library needs no link to libcuda), or nullptr.
+void* current_context() {
+  using Fn = int (*)(void**);
+  static Fn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<Fn>(f);
+  }();
+  void* ctx = nullptr;
+  if (!fn || fn(&ctx) != 0) return nullptr;
+  return ctx;
+}
 
 // Device address of g_verify_scratch on the current device.  In host code the
-// symbol is only a host-side stand-in, so the address is looked up once per
-// device (with that device current) and cached.
-int scratch_address(void** out) {
+// symbol is only a host-side stand-in.  A call made outside a stream capture
+// looks the address up afresh (cheap once the module is loaded, and right
+// after a device reset has loaded the module again at another address) and
+// remembers it with the context it belongs to.  A call made while `s` is
+// being captured must not trigger a module load, so it uses the remembered
+// address, and only if it belongs to the current context; otherwise it
+// returns DFLASH_ERR_UNSUPPORTED and launches nothing.
+int scratch_address(cudaStream_t s, void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DFLASH_ERR_CUDA;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return DFLASH_ERR_CUDA;
+  }
+  void* ctx = current_context();
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (cs == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess || !p) return DFLASH_ERR_CUDA;
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = ctx;
+  } else if (!g_scratch_ptr[dev] || !ctx || g_scratch_ctx[dev] != ctx) {
+    return DFLASH_ERR_UNSUPPORTED;
   }
   *out = g_scratch_ptr[dev];
   return DFLASH_OK;
@@ -75,8 +108,9 @@ int dflash_verify_noalloc(int mode, int B, int gamma, int vocab, const float* ta
   measure.take<unsigned long long>((size_t)B * row_chunks(vocab) * 2);
   if (measure.off > kNoAllocScratchBytes) return DFLASH_ERR_SHAPE;  // beyond the fixed scratch
 
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   void* base = nullptr;
-  int rc = scratch_address(&base);
+  int rc = scratch_address(s, &base);
   if (rc) return rc;
   Carve c(base, kWsHeader);
   int* counters = c.take<int>(B);
@@ -84,7 +118,6 @@ int dflash_verify_noalloc(int mode, int B, int gamma, int vocab, const float* ta
   unsigned long long* zsum = c.take<unsigned long long>((size_t)B * row_chunks(vocab) * 2);
   int* status = static_cast<int*>(base);
 
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(base, 0, zero_end, s) != cudaSuccess) return DFLASH_ERR_CUDA;
   if (mode == DFLASH_VERIFY_GREEDY)
     return launch_verify_greedy(B, gamma, vocab, target, draft, accept_len, tokens, next_anchor,

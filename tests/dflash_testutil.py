@@ -68,3 +68,63 @@ def run_draft(h, anchor, ctx_len, rk, rv, gamma, topk, sampling=None, req_slot=N
     assert dfl.dflash_read_status(ws) == 0
     assert R > 0
     return {k: (v.cpu().numpy() if v is not None else None) for k, v in out.items()}
+
+
+def widen(W):
+    """Float64 numpy copies of CPU weight tensors (exact: bf16 and float32
+    values are float64 values).  The oracle reads them without re-widening
+    per call, which keeps full-size oracle passes to seconds."""
+    if isinstance(W, dict):
+        return {k: widen(v) for k, v in W.items()}
+    if isinstance(W, list):
+        return [widen(v) for v in W]
+    return W.double().numpy()
+
+
+def check_probs(got, want, tol=1e-5):
+    """A float32 sampling distribution against the oracle's float64 one, row
+    by row: the kept sets may differ only in a few ids at the nucleus boundary
+    whose mass is below tol; on the ids both keep, max abs error over max abs
+    value <= tol."""
+    got = got.reshape(-1, got.shape[-1])
+    want = want.reshape(-1, want.shape[-1])
+    np.testing.assert_allclose(got.sum(-1), 1.0, rtol=1e-4)
+    for r in range(got.shape[0]):
+        kg, kw = got[r] > 0, want[r] > 0
+        diff = kg ^ kw
+        assert want[r][diff].sum() <= tol and diff.sum() <= 3
+        both = kg & kw
+        assert np.abs(got[r][both] - want[r][both]).max() / np.abs(want[r]).max() <= tol
+
+
+def check_q_against_oracle_logits(q_gpu, z_gpu, z_ref, T, top_p):
+    """q = top_p(softmax(z / T)) from the drafter's logits, judged through the
+    logits it came from.
+
+    With eps = max |z_gpu - z_ref| over a row, every log-probability of
+    softmax(z / T) moves by at most 2 eps / T (eps / T for the id itself, as
+    much again for the log-sum-exp), and renormalising a nucleus that keeps
+    the same ids moves it by at most as much again: 4 eps / T in all.  So,
+    per row and per id kept on both sides,
+        |q_gpu - q_ref| <= (exp(4 eps / T) - 1) * max(q_gpu, q_ref),
+    and an id kept on one side only lies at the nucleus boundary: it is no
+    more likely than exp(4 eps / T) times the least likely id both keep.
+    Returns the largest eps seen (the logits themselves are checked by the
+    caller against the 1e-2 normwise bar)."""
+    from oracle import sampling as osamp
+    V = q_gpu.shape[-1]
+    qg = q_gpu.reshape(-1, V).astype(np.float64)
+    zg = z_gpu.reshape(-1, V).astype(np.float64)
+    zr = z_ref.reshape(-1, V)
+    worst = 0.0
+    for r in range(qg.shape[0]):
+        eps = float(np.abs(zg[r] - zr[r]).max())
+        worst = max(worst, eps)
+        qr = osamp.probs(zr[r:r + 1], T, top_p)[0]
+        f = np.exp(4.0 * eps / T)
+        kg, kr = qg[r] > 0, qr > 0
+        both = kg & kr
+        assert (np.abs(qg[r][both] - qr[both]) <= (f - 1.0) * np.maximum(qg[r][both], qr[both]) + 1e-12).all()
+        floor = min(qg[r][both].min(), qr[both].min())
+        assert (qg[r][kg & ~kr] <= f * floor).all() and (qr[kr & ~kg] <= f * floor).all()
+    return worst

@@ -93,6 +93,123 @@ def test_captured_cycle_replays_like_eager_calls():
     assert (graphed["anchor"].cpu().numpy() == tok[np.arange(B), n]).all()
 
 
+def test_captured_cycle_matches_oracle_cycle():
+    """Three replays of one captured cycle (ctx_append of the positions the
+    last verification committed, draft_block, greedy verify writing the next
+    anchor and append count on the device) against the oracle running the
+    same cycle: its own ring, context lengths and anchors.
+
+    Before each replay the test writes the stand-in target logits (outside
+    the graph), designed from the oracle's drafts for that cycle so that each
+    request accepts a chosen number of drafts (all of them, with the bonus, in
+    one case).  Draft tokens are compared with the oracle's top-1 wherever its
+    margin exceeds twice the logit tolerance, and tolerance-aware elsewhere;
+    the oracle then verifies the GPU's drafts, so accept lengths, committed
+    tokens, next anchors, append counts and context lengths are compared bit
+    for bit, and the ring entries appended each cycle within 1e-2."""
+    from oracle import model as om
+    dims, h, rk0, rv0 = _setup()
+    B, gamma, V = 2, 8, dims["vocab"]
+    G = gamma - 1
+    TOL = 1e-2
+    dev = torch.device("cuda")
+    W = synth.weights(dims, 91, random_gains=True)          # the weights _setup loaded
+    cfg = tu.oracle_cfg(dims)
+    feats = synth.features(dims, B * gamma, 93).reshape(B, gamma, dims["n_feat"], dims["feat_dim"])
+    ctx0, anchor0, napp0 = [300, 40], [5, 7], [3, 1]
+    design = [(3, 0), (G, 2), (1, 5)]                       # drafts each request should accept
+
+    def state():
+        return dict(ctx=torch.tensor(ctx0, dtype=torch.int64, device=dev),
+                    anchor=torch.tensor(anchor0, dtype=torch.int32, device=dev),
+                    n_app=torch.tensor(napp0, dtype=torch.int32, device=dev),
+                    rk=rk0.clone(), rv=rv0.clone(),
+                    logits=torch.empty((B, G, V), device=dev),
+                    draft=torch.empty((B, G), dtype=torch.int32, device=dev),
+                    target=torch.zeros((B, gamma, V), device=dev),
+                    acc=torch.empty(B, dtype=torch.int32, device=dev),
+                    tok=torch.empty((B, gamma), dtype=torch.int32, device=dev),
+                    ws_a=dfl.workspace(dfl.dflash_append_workspace_bytes(h)),
+                    ws_d=dfl.workspace(dfl.dflash_draft_workspace_bytes(h)),
+                    ws_v=dfl.workspace(dfl.dflash_verify_workspace_bytes(B, gamma, V)))
+
+    fd = feats.cuda()
+
+    def cycle(st):
+        dfl.dflash_ctx_append(h, fd, st["n_app"], st["ctx"], st["rk"], st["rv"], st["ws_a"])
+        dfl.dflash_draft_block(h, st["anchor"], st["ctx"], st["rk"], st["rv"], gamma, st["ws_d"],
+                               out=dict(logits=st["logits"], draft=st["draft"]))
+        dfl.dflash_verify(dfl.DFLASH_VERIFY_GREEDY, st["target"], st["draft"], st["acc"], st["tok"],
+                          st["ws_v"], next_anchor=st["anchor"], n_append=st["n_app"])
+
+    s = torch.cuda.Stream()
+    warm = state()
+    with torch.cuda.stream(s):
+        cycle(warm)                      # first calls outside the capture
+    torch.cuda.synchronize()
+    st = state()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        cycle(st)
+    fresh = state()                      # capture recorded work without running it
+    for k in ("ctx", "anchor", "n_app", "rk", "rv"):
+        st[k].copy_(fresh[k])
+    for ws in ("ws_a", "ws_d", "ws_v"):
+        st[ws].zero_()
+    torch.cuda.synchronize()
+
+    ork, orv = rk0.double().cpu().numpy(), rv0.double().cpu().numpy()
+    octx, oanc, oapp = np.array(ctx0), np.array(anchor0), np.array(napp0)
+    rng = np.random.default_rng(95)
+    for cyc_i, ks in enumerate(design):
+        # the oracle's cycle up to its drafts
+        appended = []
+        for b in range(B):
+            om.ctx_append(cfg, W, ork, orv, b, feats[b, :oapp[b]], int(octx[b]))
+            appended.append((int(octx[b]), int(oapp[b])))
+        octx = octx + oapp
+        z = om.draft_pass(cfg, W, ork, orv, octx, oanc, gamma)["logits"]
+        top = z.argmax(-1)
+        # stand-in target designed from the oracle's drafts
+        t = rng.normal(size=(B, gamma, V)).astype(np.float32)
+        for b, k in enumerate(ks):
+            for i in range(k):
+                t[b, i, top[b, i]] = 20.0
+            c = (int(top[b, k]) + 17 if k < G else 3 * cyc_i + 11) % V
+            t[b, k, c] = 20.0
+        st["target"].copy_(torch.from_numpy(t))
+        with torch.cuda.stream(s):
+            g.replay()
+        torch.cuda.synchronize()
+        zg = st["logits"].cpu().numpy()
+        assert tu.rel_err(zg, z) <= TOL
+        scale = np.abs(z).max()
+        yg = st["draft"].cpu().numpy()
+        srt = np.sort(z, axis=-1)
+        for b in range(B):
+            for i in range(G):
+                if srt[b, i, -1] - srt[b, i, -2] > 2 * TOL * scale:
+                    assert yg[b, i] == top[b, i]
+                else:
+                    assert z[b, i, yg[b, i]] >= srt[b, i, -1] - TOL * scale
+        n_o, tok_o = over.greedy(t, yg)
+        np.testing.assert_array_equal(st["acc"].cpu().numpy(), n_o)
+        np.testing.assert_array_equal(st["tok"].cpu().numpy(), tok_o)
+        oanc = tok_o[np.arange(B), n_o].astype(np.int64)
+        oapp = n_o + 1
+        np.testing.assert_array_equal(st["anchor"].cpu().numpy(), oanc)
+        np.testing.assert_array_equal(st["n_app"].cpu().numpy(), oapp)
+        np.testing.assert_array_equal(st["ctx"].cpu().numpy(), octx)
+        gk, gv = st["rk"].double().cpu().numpy(), st["rv"].double().cpu().numpy()
+        for b, (p0, n) in enumerate(appended):
+            slots = (p0 + np.arange(n)) % dims["window"]
+            assert tu.rel_err(gk[:, b][:, :, slots], ork[:, b][:, :, slots]) <= TOL
+            assert tu.rel_err(gv[:, b][:, :, slots], orv[:, b][:, :, slots]) <= TOL
+    assert dfl.dflash_read_status(st["ws_a"]) == 0
+    assert dfl.dflash_read_status(st["ws_d"]) == 0
+    assert dfl.dflash_read_status(st["ws_v"]) == 0
+
+
 def test_verify_commit_outputs_sampled():
     B, gamma, V = 5, 6, 300
     rng = np.random.default_rng(3)

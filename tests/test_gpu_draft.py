@@ -83,26 +83,53 @@ def test_draft_block_with_request_slots_and_topk16():
                   want.reshape(-1, want.shape[-1]), TOL)
 
 
-def test_draft_block_sampled_q_and_draw():
-    dims = synth.DIMS["small"]
-    B, gamma = 3, 8
-    W = synth.weights(dims, 31)
+@pytest.mark.parametrize("name,B,gamma,lens", [("small", 3, 8, [256, 40, 999]),
+                                                ("small128", 4, 16, [512, 0, 7, 2000])])
+def test_sampled_draft_then_sampled_verify_chain(name, B, gamma, lens):
+    """draft_block with T = 0.7, top-p 0.99 gives q and y ~ q; stand-in
+    target logits (draft logits + N(0, 1)) give p through dflash_probs; the
+    sampled verification of y is bit-exact against the oracle fed the same
+    float32 p, q and y.  q is checked against the sampling preparation of the
+    drafter's own logits (1e-5) and against the oracle's logits within the
+    bound those logits' error implies."""
+    from oracle import verify as over
+    dims = synth.DIMS[name]
+    T, top_p, step = 0.7, 0.99, 5
+    G, V = gamma - 1, dims["vocab"]
+    W = synth.weights(dims, 31, random_gains=True)
     rk, rv = synth.ring(dims, B, 32)
-    anchor = synth.token_ids(B, dims["vocab"], 33)
-    L = torch.tensor([256, 40, 999], dtype=torch.int64)
+    anchor = synth.token_ids(B, V, 33)
+    L = torch.tensor(lens, dtype=torch.int64)
     seeds = synth.seeds(B, 34)
     h = dfl.dflash_create(tu.lib_cfg(dims, batch_max=B, gamma_max=gamma), tu.to_dev(W))
-    sp = dict(temperature=0.7, top_p=0.99, seeds=seeds.cuda(), step=5)
+    sp = dict(temperature=T, top_p=top_p, seeds=seeds.cuda(), step=step)
     got = tu.run_draft(h, anchor, L, rk.cuda(), rv.cuda(), gamma, topk=4, sampling=sp)
     ref = om.draft_pass(tu.oracle_cfg(dims), W, rk, rv, L.numpy(), anchor.numpy(), gamma)
-    q_ref = osamp.probs(ref["logits"], 0.7, 0.99)
-    # q follows the oracle within the logit tolerance propagated through softmax
-    assert tu.rel_err(got["q"], q_ref) <= 5e-2
-    np.testing.assert_allclose(got["q"].sum(-1), 1.0, rtol=1e-4)
-    # every proposed token lies in the support of the GPU's own q
-    q = got["q"]
-    y = got["draft"]
-    assert all(q[b, i, y[b, i]] > 0 for b in range(B) for i in range(gamma - 1))
+    z = got["logits"]
+    assert tu.rel_err(z, ref["logits"]) <= TOL
+    tu.check_probs(got["q"], osamp.probs(z, T, top_p))
+    tu.check_q_against_oracle_logits(got["q"], z, ref["logits"], T, top_p)
+    seeds_u = seeds.numpy().view(np.uint64)
+    np.testing.assert_array_equal(got["draft"], osamp.draft_draw(got["q"], seeds_u, step))
+
+    t = (np.concatenate([z, z[:, G - 1:]], axis=1) +
+         synth.normal((B, gamma, V), 1.0, 35).numpy()).astype(np.float32)
+    dev = torch.device("cuda")
+    tt = torch.from_numpy(t).to(dev)
+    p = torch.empty_like(tt)
+    dfl.dflash_probs(tt, T, top_p, p, dfl.workspace(dfl.dflash_probs_workspace_bytes(B * gamma, V)))
+    n = torch.full((B,), -7, dtype=torch.int32, device=dev)
+    tok = torch.full((B, gamma), -7, dtype=torch.int32, device=dev)
+    ws_v = dfl.workspace(dfl.dflash_verify_workspace_bytes(B, gamma, V))
+    dfl.dflash_verify(dfl.DFLASH_VERIFY_SAMPLED, p, torch.from_numpy(got["draft"]).to(dev), n, tok,
+                      ws_v, q=torch.from_numpy(got["q"]).to(dev), seeds=seeds.cuda(), step=step)
+    torch.cuda.synchronize()
+    assert dfl.dflash_read_status(ws_v) == 0
+    p_np = p.cpu().numpy()
+    tu.check_probs(p_np, osamp.probs(t, T, top_p))
+    want_n, want_tok = over.sampled(p_np, got["q"], got["draft"], seeds_u, step)
+    np.testing.assert_array_equal(n.cpu().numpy(), want_n)
+    np.testing.assert_array_equal(tok.cpu().numpy(), want_tok)
 
 
 @pytest.mark.parametrize("B,G,V", [(1, 7, 1024), (5, 3, 5003), (4, 15, 151936)])
