@@ -18,6 +18,10 @@ What it computes, and where each step comes from:
                 ("DFlash vs DFlash 2" blog, section "The problem: one expensive
                 token at a time": accept with min(1, p/q), resample from the
                 normalised [p - q]+, bonus token when every draft survives).
+* ``quant``     FP8 (E4M3) drafter weights with one float32 scale per output
+                row, and their exact dequantization (product doc "Speculative
+                decoding", introduction, and model card section "Serve": the
+                models are served in FP8; format and scaling are readings).
 * ``model``     the drafter: target-feature fusion H_t = RMSNorm(W_c[...]),
                 context K/V injection, the non-causal block pass over
                 [anchor, MASK, ...] with a sliding-window context, the shared
@@ -35,4 +39,4 @@ parity with these readings): RoPE placement and base, the pre-norm layer
 layout, the RMSNorm epsilon, the MASK token id, and the Philox counter layout.
 """
 
-from . import philox, fixedpoint, sampling, verify, model  # noqa: F401
+from . import philox, fixedpoint, sampling, verify, model, quant  # noqa: F401
