@@ -39,18 +39,26 @@ class dflash_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "hidden", "n_q_heads", "n_kv_heads", "head_dim", "ffn", "vocab", "n_layers", "n_feat",
         "feat_dim", "window", "gamma_max", "topk_max", "batch_max", "append_max")] + [
-        ("rope_theta", ctypes.c_float), ("eps", ctypes.c_float), ("mask_id", ctypes.c_int)]
+        ("rope_theta", ctypes.c_float), ("eps", ctypes.c_float), ("mask_id", ctypes.c_int),
+        ("weight_format", ctypes.c_int)]
+
+
+DFLASH_WEIGHTS_BF16 = 0
+DFLASH_WEIGHTS_E4M3 = 1
+
+LAYER_MATRICES = ("w_qkv", "w_o", "w_gate", "w_up", "w_down")
 
 
 class dflash_layer_weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
-        "g_attn", "w_qkv", "w_o", "g_mlp", "w_gate", "w_up", "w_down")]
+        "g_attn", "w_qkv", "w_o", "g_mlp", "w_gate", "w_up", "w_down",
+        "s_qkv", "s_o", "s_gate", "s_up", "s_down")]
 
 
 class dflash_weights(ctypes.Structure):
     _fields_ = [("embed", ctypes.c_void_p), ("lm_head", ctypes.c_void_p), ("w_c", ctypes.c_void_p),
                 ("g_c", ctypes.c_void_p), ("g_final", ctypes.c_void_p),
-                ("layers", ctypes.POINTER(dflash_layer_weights))]
+                ("layers", ctypes.POINTER(dflash_layer_weights)), ("s_lm_head", ctypes.c_void_p)]
 
 
 class dflash_sampling(ctypes.Structure):
@@ -99,6 +107,7 @@ def lib():
         "dflash_sample_draft": (_I, [_I, _I, _I, _P, _P, ctypes.c_uint64, _P, _P, _SZ, _P]),
         "dflash_sample_workspace_bytes": (_SZ, [_I, _I]),
         "dflash_profile_enable": (_I, [_P, _I]),
+        "dflash_quantize_e4m3": (_I, [_P, _I, _I, _P, _P, _P]),
         "dflash_verify_noalloc": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, ctypes.c_uint64, _P, _P, _P,
                                        _P, _P]),
         "dflash_profile_read": (_I, [_P, ctypes.POINTER(ctypes.c_float),
@@ -169,17 +178,26 @@ class Handle:
 
 
 def dflash_create(cfg, weights):
-    """cfg: dict with the dflash_config fields; weights: dict of CUDA tensors
-    (matrices bf16, gains float32) with keys embed, lm_head, w_c, g_c, g_final
-    and layers = [dict(g_attn, w_qkv, w_o, g_mlp, w_gate, w_up, w_down)]."""
+    """cfg: dict with the dflash_config fields (weight_format defaults to
+    DFLASH_WEIGHTS_BF16); weights: dict of CUDA tensors (matrices bf16, gains
+    float32) with keys embed, lm_head, w_c, g_c, g_final and layers =
+    [dict(g_attn, w_qkv, w_o, g_mlp, w_gate, w_up, w_down)].  With
+    DFLASH_WEIGHTS_E4M3 the layer matrices and lm_head are uint8 E4M3 codes
+    and s_qkv, s_o, s_gate, s_up, s_down (per layer) and s_lm_head their
+    float32 row scales."""
+    cfg = dict(cfg)
+    cfg.setdefault("weight_format", DFLASH_WEIGHTS_BF16)
     c = dflash_config(**{k: cfg[k] for k, _ in dflash_config._fields_})
     layers = (dflash_layer_weights * len(weights["layers"]))()
     for i, lw in enumerate(weights["layers"]):
         for k, _ in dflash_layer_weights._fields_:
-            setattr(layers[i], k, lw[k].data_ptr())
+            t = lw.get(k)
+            setattr(layers[i], k, t.data_ptr() if t is not None else None)
+    s_head = weights.get("s_lm_head")
     w = dflash_weights(weights["embed"].data_ptr(), weights["lm_head"].data_ptr(),
                        weights["w_c"].data_ptr(), weights["g_c"].data_ptr(),
-                       weights["g_final"].data_ptr(), layers)
+                       weights["g_final"].data_ptr(), layers,
+                       s_head.data_ptr() if s_head is not None else None)
     out = ctypes.c_void_p()
     _check(lib().dflash_create(ctypes.byref(c), ctypes.byref(w), ctypes.byref(out)), "dflash_create")
     return Handle(out, (weights, layers), dict(cfg))
@@ -302,3 +320,31 @@ def dflash_verify_noalloc(mode, target, draft, accept_len, tokens, q=None, seeds
                                        _ptr(seeds), ctypes.c_uint64(int(step) & (2 ** 64 - 1)),
                                        _ptr(accept_len), _ptr(tokens), _ptr(next_anchor),
                                        _ptr(n_append), _stream(stream)), "dflash_verify_noalloc")
+
+
+def dflash_quantize_e4m3(w, codes, scales, stream=None):
+    """w bf16 [rows, cols] -> codes uint8 [rows, cols], scales float32 [rows]."""
+    rows, cols = w.shape
+    _check(lib().dflash_quantize_e4m3(_ptr(w), rows, cols, _ptr(codes), _ptr(scales), _stream(stream)),
+           "dflash_quantize_e4m3")
+
+
+def quantize_weights_e4m3(weights, stream=None):
+    """A copy of a bf16 weight dict (see dflash_create) whose layer matrices
+    and lm_head are E4M3 codes with their row scales, made on the device by
+    dflash_quantize_e4m3; embed, w_c and the gains are shared."""
+    def q(t):
+        codes = torch.empty(t.shape, dtype=torch.uint8, device=t.device)
+        scales = torch.empty(t.shape[0], dtype=torch.float32, device=t.device)
+        dflash_quantize_e4m3(t, codes, scales, stream)
+        return codes, scales
+
+    out = {k: v for k, v in weights.items() if k != "layers"}
+    out["lm_head"], out["s_lm_head"] = q(weights["lm_head"])
+    out["layers"] = []
+    for lw in weights["layers"]:
+        nl = dict(lw)
+        for k in LAYER_MATRICES:
+            nl[k], nl["s_" + k[2:]] = q(lw[k])
+        out["layers"].append(nl)
+    return out

@@ -3,9 +3,9 @@
 //
 // ctx_append  ("DFlash vs DFlash 2" blog, section "Conditioning on the target
 //              model", H_t equation and K/V injection equation):
-//   W_c GEMM (bf16 features, fp32 out) -> RMSNorm(g_c) (fp16) -> per-layer
-//   K/V GEMM whose epilogue rotates K and scatters K and V into ring slot
-//   pos mod W -> ctx_len += n.
+//   W_c GEMM (bf16 features) -> RMSNorm(g_c) (fp16) -> per-layer K/V GEMM
+//   whose epilogue rotates K and scatters K and V into ring slot pos mod W ->
+//   ctx_len += n; up to 32 tokens the RMSNorm is folded into the two GEMMs.
 // draft_block ("DFlash: generate the block all at once"):
 //   embed [anchor, MASK...] + RMSNorm (+RoPE table) -> for each layer: QKV
 //   GEMM (+RoPE) -> block attention over [ring window ; block] -> O GEMM ->
@@ -45,11 +45,13 @@ struct dflash_handle {
   std::vector<LayerMaps> maps;
   CUtensorMap lm_head, w_c;  // lm_head: fp16 copy; w_c: the caller's bf16 matrix
   RopeInv rope;              // inverse rotary frequencies (double -> float pairs)
-  void* f16 = nullptr;       // fp16 copies of every layer's matrices and the LM head
+  void* f16 = nullptr;       // fp16 copies of every layer's matrices and the LM head (bf16 weights)
+  int wtype = OPND_F16;      // operand type of those matrices in the GEMMs (OPND_E4M3: in place)
   int num_sms;
   int mask_id;
-  // benchmark hook: event pairs around the GEMM launches of draft_block
-  std::vector<cudaEvent_t> prof_events;
+  // benchmark hook: device completion timestamps of draft_block's launches
+  unsigned long long* prof_ts = nullptr;  // [prof_cap + 1], device
+  int prof_cap = 0;
   std::vector<double> prof_bytes;
   std::vector<int> prof_kinds;
   int prof_used = 0;
@@ -76,6 +78,7 @@ int validate_config(const dflash_config& c) {
   if (c.append_max < 1 || c.append_max > 8192) return DFLASH_ERR_UNSUPPORTED;
   if (!(c.eps > 0.0f) || !(c.rope_theta > 0.0f)) return DFLASH_ERR_ARG;
   if (c.mask_id < -1 || c.mask_id >= c.vocab) return DFLASH_ERR_ARG;
+  if (c.weight_format != DFLASH_WEIGHTS_BF16 && c.weight_format != DFLASH_WEIGHTS_E4M3) return DFLASH_ERR_ARG;
   // query-group rows of one KV head must fit the attention kernel's tiles
   if (attn_row_tiles(c.n_q_heads, c.n_kv_heads, c.gamma_max) > 6) return DFLASH_ERR_UNSUPPORTED;
   return DFLASH_OK;
@@ -156,6 +159,7 @@ struct AppendWs {
   float* gemm_partial;
   void* ht;
   float2* rope_cs;
+  float* ssq;  // [hidden / 128][M] per-tile sums of squares of W_c's output (folded RMSNorm)
   size_t bytes;
 };
 
@@ -169,17 +173,20 @@ AppendWs append_layout(const dflash_handle* h, void* base) {
   w.fused = cv.take<float>(M * c.hidden);
   w.ht = cv.take<uint16_t>(M * c.hidden);
   w.rope_cs = cv.take<float2>(M * (c.head_dim / 2));
+  w.ssq = cv.take<float>((size_t)((c.hidden + 127) / 128) * (M < 32 ? 32 : M));
   w.gemm_partial = cv.take<float>(kGemmPartialFloats);
   w.bytes = cv.off;
   return w;
 }
 
-GemmAOpts single_map() {
+GemmAOpts single_map(const float* scale = nullptr) {
   GemmAOpts o;
   o.n_maps = 1;
   o.tiles_per_map = 1 << 30;
   o.row_offset = 0;
   o.dual = 0;
+  for (int i = 0; i < kMaxAMaps; ++i) o.scale[i] = nullptr;
+  o.scale[0] = scale;
   return o;
 }
 
@@ -214,29 +221,32 @@ int splits_for(const dflash_handle* h, int n_tiles, int M, int K) {
   return gemm_plan_splits(n_tiles * m_tiles, K, h->num_sms * per_sm);
 }
 
-// Profiling brackets around one launch of the pass (no-ops unless enabled).
-// While the stream is captured, external records become event nodes (with
-// timestamps) of the graph; otherwise they are plain records.
-bool prof_record(cudaEvent_t e, cudaStream_t s) {
-  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return false;
-  }
-  const cudaError_t rc = cs == cudaStreamCaptureStatusActive
-                             ? cudaEventRecordWithFlags(e, s, cudaEventRecordExternal)
-                             : cudaEventRecord(e, s);
-  if (rc != cudaSuccess) (void)cudaGetLastError();
-  return rc == cudaSuccess;
+// Profiling marks (no-ops unless enabled).  A mark is a one-warp kernel
+// launched with programmatic dependent launch right after a launch of the
+// pass: it lets the next kernel be scheduled at once (so that kernel's early
+// start overlaps the profiled one exactly as without the mark), waits for the
+// profiled kernel to complete and writes %globaltimer into its slot.  Slot 0
+// is written by a mark before the first launch.  Launch i is then charged the
+// interval between completions i and i + 1: the intervals add up to the
+// whole pass, overlap included, where an event pair around every launch
+// would serialise neighbouring kernels and charge each its full latency.
+__global__ void profile_mark_kernel(unsigned long long* ts, int slot) {
+  pdl_enter();
+  if (threadIdx.x == 0) ts[slot] = globaltimer_ns();
+}
+
+bool prof_mark(dflash_handle* h, cudaStream_t s, int slot) {
+  return launch_pdl(profile_mark_kernel, dim3(1), dim3(32), 0, s, h->prof_ts, slot) == DFLASH_OK;
 }
 int prof_begin(dflash_handle* h, cudaStream_t s) {
   const int i = h->prof_used;
-  if (2 * (i + 1) > (int)h->prof_events.size()) return -1;
-  return prof_record(h->prof_events[2 * i], s) ? i : -1;
+  if (i >= h->prof_cap) return -1;
+  if (i == 0 && !prof_mark(h, s, 0)) return -1;
+  return i;
 }
 void prof_end(dflash_handle* h, cudaStream_t s, int slot, double bytes, int kind) {
   if (slot < 0) return;
-  if (!prof_record(h->prof_events[2 * slot + 1], s)) return;
+  if (!prof_mark(h, s, slot + 1)) return;
   h->prof_bytes[slot] = bytes;
   h->prof_kinds[slot] = kind;
   h->prof_used = slot + 1;
@@ -247,40 +257,114 @@ int draft_gemm(dflash_handle* h, const GemmAMaps& A, const GemmAOpts& ao, int n_
                int M, int K, const GemmEpi& e, const GemmScratch& sc, cudaStream_t s, double bytes,
                const GemmRowScale* rs = nullptr) {
   const int slot = prof_begin(h, s);
-  const int rc = launch_gemm(A, ao, n_tiles, x, OPND_F16, M, K, e, sc, splits_for(h, n_tiles, M, K),
+  const int rc = launch_gemm(A, ao, n_tiles, x, h->wtype, M, K, e, sc, splits_for(h, n_tiles, M, K),
                              s, true, rs);
   if (rc) return rc;
   prof_end(h, s, slot, bytes, DFLASH_KIND_GEMM);
   return DFLASH_OK;
 }
 
+// E4M3 weights: check the caller's codes and scales, then encode the TMA
+// descriptors over them in place (no copy).
+int create_e4m3(dflash_handle* h, const dflash_weights& w) {
+  const dflash_config& c = h->cfg;
+  const uint64_t d = c.hidden, F = c.ffn, qd = (uint64_t)c.n_q_heads * c.head_dim;
+  const uint64_t qkv_rows = (uint64_t)(c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
+  h->wtype = OPND_E4M3;
+  struct Mat {
+    const void* codes;
+    const float* scale;
+    uint64_t rows, cols;
+  };
+  std::vector<Mat> mats;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const dflash_layer_weights& L = h->layers[l];
+    mats.push_back({L.w_qkv, L.s_qkv, qkv_rows, d});
+    mats.push_back({L.w_o, L.s_o, d, qd});
+    mats.push_back({L.w_gate, L.s_gate, F, d});
+    mats.push_back({L.w_up, L.s_up, F, d});
+    mats.push_back({L.w_down, L.s_down, d, F});
+  }
+  mats.push_back({w.lm_head, w.s_lm_head, (uint64_t)c.vocab, d});
+  for (const Mat& m : mats) {
+    if (!m.scale) return DFLASH_ERR_ARG;
+    if (!aligned(m.scale, 4)) return DFLASH_ERR_ALIGN;
+  }
+  int* flag = nullptr;
+  if (cudaMalloc(&flag, sizeof(int)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return DFLASH_ERR_CUDA;
+  }
+  // the weights may have been written on any stream: wait for all of it
+  int rc = cudaDeviceSynchronize() == cudaSuccess && cudaMemset(flag, 0, sizeof(int)) == cudaSuccess
+               ? DFLASH_OK
+               : DFLASH_ERR_CUDA;
+  for (size_t i = 0; i < mats.size() && !rc; ++i)
+    rc = launch_check_e4m3(mats[i].codes, mats[i].rows * mats[i].cols, mats[i].scale, mats[i].rows, flag,
+                           4 * h->num_sms, 0);
+  int bad = 0;
+  if (!rc && cudaMemcpy(&bad, flag, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) rc = DFLASH_ERR_CUDA;
+  cudaFree(flag);
+  if (rc) return rc;
+  if (bad) return DFLASH_ERR_RANGE;
+  h->maps.resize(c.n_layers);
+  rc = encode_2d_u8(&h->lm_head, w.lm_head, d, c.vocab, 128, 128);
+  if (!rc) rc = encode_2d(&h->w_c, w.w_c, OPND_BF16, (uint64_t)c.n_feat * c.feat_dim, d, 64, 128);
+  for (int l = 0; l < c.n_layers && !rc; ++l) {
+    const dflash_layer_weights& L = h->layers[l];
+    LayerMaps& m = h->maps[l];
+    rc = encode_2d_u8(&m.qkv, L.w_qkv, d, qkv_rows, 128, 128);
+    if (!rc) rc = encode_2d_u8(&m.o, L.w_o, qd, d, 128, 128);
+    if (!rc) rc = encode_2d_u8(&m.gate, L.w_gate, d, F, 128, 64);
+    if (!rc) rc = encode_2d_u8(&m.up, L.w_up, d, F, 128, 64);
+    if (!rc) rc = encode_2d_u8(&m.down, L.w_down, F, d, 128, 128);
+  }
+  return rc;
+}
+
 }  // namespace
 
 extern "C" {
 
+int dflash_quantize_e4m3(const void* w, int rows, int cols, void* codes, float* scales,
+                         dflash_stream_t stream) {
+  if (!w || !codes || !scales) return DFLASH_ERR_ARG;
+  if (rows < 1 || cols < 16 || cols % 16) return DFLASH_ERR_SHAPE;
+  if (!aligned(w, 16) || !aligned(codes, 16) || !aligned(scales, 4)) return DFLASH_ERR_ALIGN;
+  return launch_quantize_e4m3(w, rows, cols, codes, scales, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int dflash_profile_enable(dflash_handle* h, int n_pairs) {
   if (!h || n_pairs < 0 || n_pairs > 4096) return DFLASH_ERR_ARG;
-  for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
-  h->prof_events.clear();
+  if (h->prof_ts) cudaFree(h->prof_ts);
+  h->prof_ts = nullptr;
+  h->prof_cap = 0;
   h->prof_bytes.assign(n_pairs, 0.0);
   h->prof_kinds.assign(n_pairs, 0);
   h->prof_used = 0;
-  for (int i = 0; i < 2 * n_pairs; ++i) {
-    cudaEvent_t e;
-    if (cudaEventCreate(&e) != cudaSuccess) return DFLASH_ERR_CUDA;
-    h->prof_events.push_back(e);
+  if (n_pairs == 0) return DFLASH_OK;
+  void* p = nullptr;
+  if (cudaMalloc(&p, sizeof(unsigned long long) * (n_pairs + 1)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return DFLASH_ERR_CUDA;
   }
+  h->prof_ts = static_cast<unsigned long long*>(p);
+  h->prof_cap = n_pairs;
   return DFLASH_OK;
 }
 
 int dflash_profile_read(dflash_handle* h, float* ms, double* bytes, int* kinds, int cap, int* count) {
   if (!h || !count || cap < 0 || (cap > 0 && (!ms || !bytes || !kinds))) return DFLASH_ERR_ARG;
   const int n = h->prof_used < cap ? h->prof_used : cap;
-  if (n > 0 && cudaEventSynchronize(h->prof_events[2 * h->prof_used - 1]) != cudaSuccess)
+  *count = 0;
+  if (n == 0) return DFLASH_OK;
+  std::vector<unsigned long long> ts(h->prof_used + 1);
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(ts.data(), h->prof_ts, sizeof(unsigned long long) * ts.size(),
+                 cudaMemcpyDeviceToHost) != cudaSuccess)
     return DFLASH_ERR_CUDA;
   for (int i = 0; i < n; ++i) {
-    if (cudaEventElapsedTime(&ms[i], h->prof_events[2 * i], h->prof_events[2 * i + 1]) != cudaSuccess)
-      return DFLASH_ERR_CUDA;
+    ms[i] = (float)((double)(long long)(ts[i + 1] - ts[i]) * 1e-6);
     bytes[i] = h->prof_bytes[i];
     kinds[i] = h->prof_kinds[i];
   }
@@ -320,6 +404,15 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
   const dflash_config& c = *cfg;
   const uint64_t d = c.hidden, F = c.ffn, qd = (uint64_t)c.n_q_heads * c.head_dim;
   const uint64_t qkv_rows = (uint64_t)(c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
+  if (c.weight_format == DFLASH_WEIGHTS_E4M3) {
+    rc = create_e4m3(h, *w);
+    if (rc) {
+      dflash_destroy(h);
+      return rc;
+    }
+    *out = h;
+    return DFLASH_OK;
+  }
 
   // fp16 copies: per layer qkv, o, gate, up, down, then the LM head; a flag word last
   struct Mat {
@@ -384,7 +477,7 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
 
 int dflash_destroy(dflash_handle* h) {
   if (h) {
-    for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
+    if (h->prof_ts) cudaFree(h->prof_ts);
     if (h->f16) cudaFree(h->f16);
   }
   delete h;
@@ -421,19 +514,37 @@ int dflash_ctx_append(dflash_handle* h, int B, int n_max, const void* feats, con
   const int Kc = c.n_feat * c.feat_dim;
   int rc;
 
-  // H_t before normalisation: fused = concat(features) W_c^T (fp32)
+  // With token tiles of at most 32 the RMSNorm that forms H_t is folded into
+  // the two GEMMs: W_c's epilogue writes fp16(H * g_c) and per-tile sums of
+  // squares of H, the K/V GEMM scales by rstd (GemmRowScale) and rotates keys
+  // at their positions itself.  Otherwise W_c writes fp32 H and a separate
+  // RMSNorm (which also tabulates the rotations) normalises it.
+  const bool fold = gemm_token_tile(M) <= 32;
+  const int d_tiles = (d + 127) / 128;
   {
     GemmAMaps A;
     A.map[0] = h->w_c;
-    GemmEpi e = epi_base(EPI_F32, M, d, ws.fused, d, ws.status);
-    const int nt = (d + 127) / 128;
+    GemmEpi e = epi_base(fold ? EPI_NORM_IN : EPI_F32, M, d, fold ? nullptr : ws.fused, d, ws.status);
+    if (fold) {
+      e.xg = static_cast<__half*>(ws.ht);
+      e.xg_g = static_cast<const float*>(h->w.g_c);
+      e.ssq = ws.ssq;
+    }
+    const int nt = d_tiles;
     rc = launch_gemm(A, single_map(), nt, feats, OPND_BF16, M, Kc, e, scratch, splits_for(h, nt, M, Kc),
                      s, true);
     if (rc) return rc;
   }
-  rc = launch_rmsnorm_rope(ws.fused, M, d, static_cast<const float*>(h->w.g_c), c.eps, 0, ws.ht,
-                           ws.status, ctx_len, n_max, ws.rope_cs, c.head_dim / 2, h->rope, s);
-  if (rc) return rc;
+  if (!fold) {
+    rc = launch_rmsnorm_rope(ws.fused, M, d, static_cast<const float*>(h->w.g_c), c.eps, 0, ws.ht,
+                             ws.status, ctx_len, n_max, ws.rope_cs, c.head_dim / 2, h->rope, s);
+    if (rc) return rc;
+  }
+  GemmRowScale rsc;
+  rsc.ssq = ws.ssq;
+  rsc.parts = d_tiles;
+  rsc.n = d;
+  rsc.eps = c.eps;
   // K/V of every layer into the ring, up to kMaxAMaps layers per launch
   const int kvd = c.n_kv_heads * c.head_dim;
   const int tiles_per_layer = 2 * kvd / 128;
@@ -442,12 +553,14 @@ int dflash_ctx_append(dflash_handle* h, int B, int n_max, const void* feats, con
     GemmAMaps A;
     for (int i = 0; i < nl; ++i) A.map[i] = h->maps[l0 + i].qkv;
     GemmAOpts ao = single_map();
+    for (int i = 0; i < nl; ++i) ao.scale[i] = h->layers[l0 + i].s_qkv;
     ao.n_maps = nl;
     ao.tiles_per_map = tiles_per_layer;
     ao.row_offset = c.n_q_heads * c.head_dim;
     GemmEpi e = epi_base(EPI_KV_RING, M, nl * 2 * kvd, nullptr, 0, ws.status);
     e.ctx_len = ctx_len;
-    e.rope_cs = ws.rope_cs;
+    e.rope_cs = fold ? nullptr : ws.rope_cs;
+    e.rope_inv = h->rope;
     e.hd = c.head_dim;
     e.ring_k = ring_k;
     e.ring_v = ring_v;
@@ -460,7 +573,8 @@ int dflash_ctx_append(dflash_handle* h, int B, int n_max, const void* feats, con
     e.req_slot = req_slot;
     e.layer0 = l0;
     const int nt = nl * tiles_per_layer;
-    rc = launch_gemm(A, ao, nt, ws.ht, OPND_F16, M, d, e, scratch, splits_for(h, nt, M, d), s, true);
+    rc = launch_gemm(A, ao, nt, ws.ht, h->wtype, M, d, e, scratch, splits_for(h, nt, M, d), s, true,
+                     fold ? &rsc : nullptr);
     if (rc) return rc;
   }
   return launch_add_lengths(B, n_new, ctx_len, s);
@@ -555,12 +669,15 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
   rsc.n = d;
   rsc.eps = c.eps;
   const double ssq_bytes = fuse_norm ? 4.0 * d_tiles * M : 0.0;
+  // bytes per weight element streamed (E4M3 codes: 1, plus a 4-byte scale per row)
+  const double wb = h->wtype == OPND_E4M3 ? 1.0 : 2.0;
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerMaps& lm = h->maps[l];
     const dflash_layer_weights& L = h->layers[l];
     {  // QKV (+RoPE on q and k)
       GemmAMaps A;
       A.map[0] = lm.qkv;
+      const GemmAOpts ao = single_map(L.s_qkv);
       GemmEpi e = epi_base(EPI_QKV, M, qkv_dim, ws.qkv, qkv_dim, ws.status);
       e.ctx_len = ctx_len;
       e.gamma = gamma;
@@ -570,8 +687,8 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
       const int nt = (qkv_dim + 127) / 128;
       // layer 0 reads the embedding's RMSNorm; later layers fold theirs in
       const bool rs_here = fuse_norm && l > 0;
-      rc = draft_gemm(h, A, single_map(), nt, ws.h, M, d, e, scratch, s,
-                      2.0 * qkv_dim * d + 2.0 * M * d + 2.0 * M * qkv_dim + (rs_here ? ssq_bytes : 0.0),
+      rc = draft_gemm(h, A, ao, nt, ws.h, M, d, e, scratch, s,
+                      wb * qkv_dim * d + 2.0 * M * d + 2.0 * M * qkv_dim + (rs_here ? ssq_bytes : 0.0),
                       rs_here ? &rsc : nullptr);
       if (rc) return rc;
     }
@@ -591,8 +708,8 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
         e.xg_g = static_cast<const float*>(L.g_mlp);
       }
       const int nt = (d + 127) / 128;
-      rc = draft_gemm(h, A, single_map(), nt, ws.attn, M, qd, e, scratch, s,
-                      2.0 * d * qd + 2.0 * M * qd + (defer ? 4.0 : 8.0) * M * d +
+      rc = draft_gemm(h, A, single_map(L.s_o), nt, ws.attn, M, qd, e, scratch, s,
+                      wb * d * qd + 2.0 * M * qd + (defer ? 4.0 : 8.0) * M * d +
                           (fuse_norm ? 2.0 * M * d + ssq_bytes : 0.0));
       if (rc) return rc;
     }
@@ -607,13 +724,14 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
       GemmAMaps A;
       A.map[0] = lm.gate;
       A.map[1] = lm.up;
-      GemmAOpts ao = single_map();
+      GemmAOpts ao = single_map(L.s_gate);
       ao.n_maps = 2;
       ao.dual = 1;
+      ao.scale[1] = L.s_up;
       GemmEpi e = epi_base(EPI_SWIGLU, M, c.ffn, ws.mlp, c.ffn, ws.status);
       const int nt = c.ffn / 64;
       rc = draft_gemm(h, A, ao, nt, ws.h, M, d, e, scratch, s,
-                      4.0 * c.ffn * d + 2.0 * M * d + 2.0 * M * c.ffn + ssq_bytes,
+                      2.0 * wb * c.ffn * d + 2.0 * M * d + 2.0 * M * c.ffn + ssq_bytes,
                       fuse_norm ? &rsc : nullptr);
       if (rc) return rc;
     }
@@ -628,8 +746,8 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
         e.xg_g = static_cast<const float*>(l + 1 < c.n_layers ? h->layers[l + 1].g_attn : h->w.g_final);
       }
       const int nt = (d + 127) / 128;
-      rc = draft_gemm(h, A, single_map(), nt, ws.mlp, M, c.ffn, e, scratch, s,
-                      2.0 * d * c.ffn + 2.0 * M * c.ffn + (defer ? 4.0 : 8.0) * M * d +
+      rc = draft_gemm(h, A, single_map(L.s_down), nt, ws.mlp, M, c.ffn, e, scratch, s,
+                      wb * d * c.ffn + 2.0 * M * c.ffn + (defer ? 4.0 : 8.0) * M * d +
                           (fuse_norm ? 2.0 * M * d + ssq_bytes : 0.0));
       if (rc) return rc;
     }
@@ -655,12 +773,12 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
       // share the token tile), the MASK rows' logits out
       GemmEpi e = epi_base(EPI_F32, M, c.vocab, logits, c.vocab, ws.status);
       e.out_gather = gamma;
-      rc = draft_gemm(h, A, single_map(), nt, ws.h, M, d, e, scratch, s,
-                      2.0 * c.vocab * d + 2.0 * M * d + 4.0 * R * c.vocab + ssq_bytes, &rsc);
+      rc = draft_gemm(h, A, single_map(h->w.s_lm_head), nt, ws.h, M, d, e, scratch, s,
+                      wb * c.vocab * d + 2.0 * M * d + 4.0 * R * c.vocab + ssq_bytes, &rsc);
     } else {
       GemmEpi e = epi_base(EPI_F32, R, c.vocab, logits, c.vocab, ws.status);
-      rc = draft_gemm(h, A, single_map(), nt, ws.hf, R, d, e, scratch, s,
-                      2.0 * c.vocab * d + 2.0 * R * d + 4.0 * R * c.vocab);
+      rc = draft_gemm(h, A, single_map(h->w.s_lm_head), nt, ws.hf, R, d, e, scratch, s,
+                      wb * c.vocab * d + 2.0 * R * d + 4.0 * R * c.vocab);
     }
     if (rc) return rc;
   }

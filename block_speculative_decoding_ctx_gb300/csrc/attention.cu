@@ -106,6 +106,13 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return r;
 }
 
+// Either bf16 half of w is beyond the fp16 range (exponent field of 2^16 or
+// more, infinities and NaN included); bf16 values below 2^16 are at most
+// 65280, inside it.
+__device__ __forceinline__ bool bf16x2_beyond_f16(uint32_t w) {
+  return ((w >> 23) & 0xFFu) >= 143u || ((w >> 7) & 0xFFu) >= 143u;
+}
+
 __device__ __forceinline__ void store_h2(__half* out, size_t o, float y0, float y1) {
   *reinterpret_cast<__half2*>(out + o) = __floats2half2_rn(y0, y1);
 }
@@ -139,6 +146,9 @@ struct WarpState {
   float o[NT][4];
   float m[2], l[2];
   uint32_t qa[HD / 16][4];           // fp16 Q fragments (A operand), k-steps of 16 dims
+  uint32_t key_exp;                  // per-half maximum of the exponent bits of the ring keys
+                                     // widened here (bf16x2_beyond_f16 of it flags a key
+                                     // beyond the fp16 range)
 };
 
 // Scores, online softmax and P.V of one key tile held in shared memory as
@@ -169,7 +179,10 @@ __device__ __forceinline__ void process_tile(WarpState<HD>& st, uint32_t k_base,
               bk[kp][3]);
       if (WIDEN) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) bk[kp][e] = bf16x2_to_f16x2(bk[kp][e]);
+        for (int e = 0; e < 4; ++e) {
+          st.key_exp = __vmaxu2(st.key_exp, bk[kp][e] & 0x7F807F80u);
+          bk[kp][e] = bf16x2_to_f16x2(bk[kp][e]);
+        }
       }
     }
 #pragma unroll
@@ -362,6 +375,7 @@ __global__ void __launch_bounds__((MT * KW + 1 + (attn_conv_warp<HD, MT, KW>() ?
   if (kHasConv && warp == kConv) {
     // ------------------------------------------------------------- converter
     // ring keys are bf16: widen each tile's keys to fp16 in place, once
+    bool bad = false;
     for (int i = 0; i < nt; ++i) {
       const int s = stage_of(i);
       if (!warp_wait(&full_bar[s], phase_of(i), &abort_sh, a.status)) break;
@@ -369,15 +383,21 @@ __global__ void __launch_bounds__((MT * KW + 1 + (attn_conv_warp<HD, MT, KW>() ?
 #pragma unroll 4
       for (int idx = lane; idx < kTileBytes / 16; idx += 32) {
         uint4 u = k4[idx];
+        bad |= bf16x2_beyond_f16(u.x) | bf16x2_beyond_f16(u.y) | bf16x2_beyond_f16(u.z) |
+               bf16x2_beyond_f16(u.w);
         u.x = bf16x2_to_f16x2(u.x);
         u.y = bf16x2_to_f16x2(u.y);
         u.z = bf16x2_to_f16x2(u.z);
         u.w = bf16x2_to_f16x2(u.w);
         k4[idx] = u;
       }
+      // these generic-proxy writes must be ordered before the TMA copy that
+      // later refills the stage (an async-proxy write to the same bytes)
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&kready_bar[s]);
     }
+    if (bad) report_status(a.status, DFLASH_ERR_RANGE);
   }
 
   WarpState<HD> st;
@@ -427,6 +447,7 @@ __global__ void __launch_bounds__((MT * KW + 1 + (attn_conv_warp<HD, MT, KW>() ?
     for (int t = 0; t < WarpState<HD>::NT; ++t) st.o[t][0] = st.o[t][1] = st.o[t][2] = st.o[t][3] = 0.f;
     st.m[0] = st.m[1] = -INFINITY;
     st.l[0] = st.l[1] = 0.0f;
+    st.key_exp = 0u;
 
     // the block's own keys go to the key-split warp with the fewest ring tiles
     if (do_block && kw == (KW - 1 - (nt % KW)) % KW)
@@ -450,6 +471,8 @@ __global__ void __launch_bounds__((MT * KW + 1 + (attn_conv_warp<HD, MT, KW>() ?
       st.l[h] += __shfl_xor_sync(0xffffffffu, st.l[h], 1);
       st.l[h] += __shfl_xor_sync(0xffffffffu, st.l[h], 2);
     }
+    // ring keys are read as fp16: one beyond its range is reported, not saturated silently
+    if (bf16x2_beyond_f16(st.key_exp)) report_status(a.status, DFLASH_ERR_RANGE);
   }
 
   const int cw = (warp > 0 && warp < kConv) ? (warp - 1) % MT : 0;  // row tile of a consumer warp

@@ -75,6 +75,28 @@ int encode_2d(CUtensorMap* map, const void* ptr, int type, uint64_t inner, uint6
   return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_ERR_CUDA;
 }
 
+int encode_2d_u8(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                 uint32_t box_outer) {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return DFLASH_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) || inner % 16) return DFLASH_ERR_ALIGN;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_ERR_CUDA;
+}
+
 int gemm_token_tile(int M) {
   if (M <= 16) return 16;
   if (M <= 32) return 32;
@@ -115,6 +137,7 @@ int gemm_plan_splits(int tiles, int K, int target_ctas) {
 int launch_gemm(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void* x, int type,
                 int M, int K, const GemmEpi& epi, const GemmScratch& scratch, int splits,
                 cudaStream_t s, bool pdl, const GemmRowScale* rs) {
+  if (type == OPND_E4M3) return launch_gemm_f8(A, ao, n_tiles, x, M, K, epi, scratch, s, pdl, rs);
   const int BN = gemm_token_tile_for(M, n_tiles, scratch.num_sms);
   const int T = BN;
   if (rs && (T > 32 || !rs->ssq || rs->parts < 1 || rs->n < 1)) return DFLASH_ERR_UNSUPPORTED;

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "common.cuh"
 #include "dflash.h"
 
 namespace dfl {
@@ -18,11 +19,15 @@ enum EpiKind : int {
   EPI_QKV = 2,     // out fp16 [M, ld]; rows < rope_rows rotated (table row m)
   EPI_RESID = 3,   // out fp32 [M, ld] += acc
   EPI_SWIGLU = 4,  // A tile = 64 gate rows + 64 up rows; out fp16 [M, ld] = silu(g) * u
-  EPI_KV_RING = 5  // scatter K (rotated) / V rows into the bf16 context ring
+  EPI_KV_RING = 5,  // scatter K (rotated) / V rows into the bf16 context ring
+  EPI_NORM_IN = 6   // a folded RMSNorm's input: xg = fp16(acc * xg_g) and per-tile sums of
+                    // squares ssq (GemmEpi); nothing else is written
 };
 
-// Element type of both MMA operands (tcgen05 kind::f16 takes A and B of one type).
-enum OperandType : int { OPND_F16 = 0, OPND_BF16 = 1 };
+// Element type of both MMA operands (tcgen05 kind::f16 takes A and B of one
+// type).  OPND_E4M3: E4M3 weights (one float32 scale per row, GemmAOpts::
+// scale) widened to fp16 in shared memory, fp16 tokens (gemm_f8.cu).
+enum OperandType : int { OPND_F16 = 0, OPND_BF16 = 1, OPND_E4M3 = 2 };
 
 // TMA descriptors of the weight operand (rows = output features, K inner).
 struct GemmAMaps {
@@ -34,6 +39,9 @@ struct GemmAOpts {
   int tiles_per_map;  // 128-row tiles served by each descriptor (multi-map mode)
   int row_offset;     // first weight row inside each descriptor
   int dual;           // SwiGLU: map[0] gate rows, map[1] up rows, 64-row boxes
+  // E4M3 weights: float32 scale of every row of each descriptor's matrix
+  // (indexed like its rows, row_offset included); nullptr for fp16 weights
+  const float* scale[kMaxAMaps];
 };
 
 struct GemmArgs {
@@ -78,7 +86,9 @@ struct GemmEpi {
   // rotary positions
   const int64_t* ctx_len;
   int gamma;
-  const float2* rope_cs;  // [M][hd/2] (cos, sin) of token m's position x inv_freq_j
+  const float2* rope_cs;  // [M][hd/2] (cos, sin) of token m's position x inv_freq_j; for
+                          // EPI_KV_RING nullptr means: computed here from rope_inv
+  RopeInv rope_inv;
   int rope_rows;
   int hd;
   // context ring scatter
@@ -92,10 +102,10 @@ struct GemmEpi {
   const int32_t* n_new;
   const int32_t* req_slot;
   int layer0;
-  // EPI_RESID: per weight tile, the sums over its rows of the updated stream's
-  // squares, ssq[tile][token], and xg = fp16(stream * xg_g) [M][ld]: the input
-  // of the next GEMM, which applies the RMSNorm's rstd (GemmRowScale); or
-  // nullptr
+  // EPI_RESID (and EPI_NORM_IN, where the "stream" is the accumulator): per
+  // weight tile, the sums over its rows of the updated stream's squares,
+  // ssq[tile][token], and xg = fp16(stream * xg_g) [M][ld]: the input of the
+  // next GEMM, which applies the RMSNorm's rstd (GemmRowScale); or nullptr
   float* ssq;
   __half* xg;
   const float* xg_g;
@@ -125,6 +135,9 @@ struct GemmScratch {
 // [outer, inner] with a (box_outer x box_inner) box and the 128-byte swizzle.
 int encode_2d(CUtensorMap* map, const void* ptr, int type, uint64_t inner, uint64_t outer,
               uint32_t box_inner, uint32_t box_outer);
+// The same for a matrix of bytes (E4M3 codes): box_inner bytes (<= 128).
+int encode_2d_u8(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                 uint32_t box_outer);
 
 int gemm_token_tile(int M);
 // The token tile launch_gemm takes for n_tiles weight tiles on num_sms SMs.
@@ -136,8 +149,15 @@ int gemm_plan_splits(int tiles, int K, int target_ctas);
 // the weights behind A.
 // With rs, every output of token m is scaled by the RMSNorm rstd rs
 // describes (token tiles of at most 32 only).
+// type OPND_E4M3: the weights behind A are E4M3 codes with ao.scale set, x
+// is fp16; the split count is planned by launch_gemm_f8 (`splits` ignored).
 int launch_gemm(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void* x, int type,
                 int M, int K, const GemmEpi& epi, const GemmScratch& scratch, int splits,
                 cudaStream_t s, bool pdl, const GemmRowScale* rs = nullptr);
+// E4M3 weights x fp16 tokens (gemm_f8.cu); token tiles of 16, 32, 64 or 128.
+int launch_gemm_f8(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void* x, int M, int K,
+                   const GemmEpi& epi, const GemmScratch& scratch, cudaStream_t s, bool pdl,
+                   const GemmRowScale* rs);
+int f8_token_tile(int M);
 
 }  // namespace dfl

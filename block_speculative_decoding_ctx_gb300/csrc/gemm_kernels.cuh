@@ -50,12 +50,18 @@ __device__ __forceinline__ void epi_sync(int bar) {
 
 __device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const float (&v_in)[16],
                                int tok_base, int tok_step, int ntok, int tile_n, int r,
-                               float* xchg, int bar, const float* rs = nullptr) {
+                               float* xchg, int bar, const float* rs = nullptr,
+                               float wscale = 1.0f) {
   const int kind = e.kind;
-  // row scale of a folded RMSNorm: rs[j * tok_step] is token j's rstd
+  // row scale of a folded RMSNorm: rs[j * tok_step] is token j's rstd; the
+  // weight row's dequantization scale (E4M3 weights) multiplies every token
   float v[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) v[j] = (rs && j < ntok) ? v_in[j] * rs[j * tok_step] : v_in[j];
+  if (wscale != 1.0f) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] *= wscale;
+  }
   const bool needs_xchg = (kind == EPI_QKV || kind == EPI_SWIGLU || kind == EPI_KV_RING);
   if (needs_xchg) {
 #pragma unroll
@@ -65,13 +71,22 @@ __device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts
   // Every kind loads what it needs for its 16 tokens into registers first and
   // stores afterwards: loads placed after stores that might alias them would
   // each wait for a full memory round trip.
-  if (kind == EPI_F32 || kind == EPI_F16 || kind == EPI_RESID) {
+  if (kind == EPI_F32 || kind == EPI_F16 || kind == EPI_RESID || kind == EPI_NORM_IN) {
     const int n = tile_n * 128 + r;
     float nw[16];  // EPI_RESID: the updated stream, zero outside the tile
 #pragma unroll
     for (int j = 0; j < 16; ++j) nw[j] = 0.0f;
     if (n < e.N) {
-      if (kind == EPI_RESID) {
+      if (kind == EPI_NORM_IN) {
+        // the accumulator is the norm's input: its gained fp16 copy only
+        const float gn = __ldg(e.xg_g + n);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int tok = tok_base + j * tok_step;
+          nw[j] = (j < ntok && tok < e.M) ? v[j] : 0.0f;
+          if (j < ntok && tok < e.M) e.xg[(size_t)tok * e.ld + n] = to_f16_checked(v[j] * gn, e.status);
+        }
+      } else if (kind == EPI_RESID) {
         float* out = static_cast<float*>(e.out);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -112,7 +127,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts
         }
       }
     }
-    if (kind == EPI_RESID && e.ssq) {
+    if ((kind == EPI_RESID || kind == EPI_NORM_IN) && e.ssq) {
       // sum over this tile's 128 rows of each token's squared stream values
       // (warp butterflies, then the group's four warps in order): the next
       // GEMM's RMSNorm adds these per-tile sums
@@ -182,6 +197,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts
     const int kv = local / e.kv_dim;            // 0 = K, 1 = V
     const int g = (local % e.kv_dim) / e.hd;
     const int d = local % e.hd, half = e.hd >> 1;
+    const bool cs_table = e.rope_cs != nullptr;
     const float2* cs = e.rope_cs + d % half;
     const int pr = r ^ half;
     __nv_bfloat16* ring = static_cast<__nv_bfloat16*>(kv ? e.ring_v : e.ring_k);
@@ -200,7 +216,15 @@ __device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts
         if (jr < __ldg(e.n_new + b)) {
           pos[j] = __ldg(e.ctx_len + b) + jr;
           slot[j] = e.req_slot ? __ldg(e.req_slot + b) : b;
-          if (kv == 0) y[j] = rope_apply(v[j], xchg[j * 128 + pr], __ldg(cs + (size_t)tok * half), d < half);
+          if (kv == 0) {
+            float2 c;
+            if (cs_table) {
+              c = __ldg(cs + (size_t)tok * half);
+            } else {  // no table: the rotation of this position and frequency here
+              rope_sincos((float)pos[j], e.rope_inv.f[d % half].x, e.rope_inv.f[d % half].y, &c.y, &c.x);
+            }
+            y[j] = rope_apply(v[j], xchg[j * 128 + pr], c, d < half);
+          }
         }
       }
     }
@@ -219,6 +243,134 @@ __device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts
         ring[o] = __float2bfloat16_rn(y[j]);
       }
     }
+  }
+}
+
+// Epilogue of a one-tile GEMM CTA once its accumulator is complete (or its
+// mainloop gave up: `aborted`): every thread of the CTA calls it.  Warps form
+// groups of four (one warp per TMEM lane quarter) taking alternate 16-token
+// chunks.  With split-K the tile's splits are reduced first: through global
+// memory and a ticket, or inside the thread-block cluster the splits form.
+// The stage buffers at `smem` are free by now and serve as scratch.  rs_tile:
+// the folded RMSNorm's rstd per local token, or nullptr; wscale: this thread's
+// weight-row dequantization scale (1 for fp16 weights).
+template <int BN, int kGroups>
+__device__ __forceinline__ void one_tile_epilogue(uint8_t* smem, uint32_t tmem, bool aborted,
+                                                  const GemmAOpts& ao, const GemmArgs& args,
+                                                  const GemmEpi& epi, int tile_n, int tile_m, int split,
+                                                  const float* rs_tile, int* last_sh, float wscale) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp & 3, grp = warp >> 2;  // TMEM lane quarter, epilogue group
+  const int r = q * 32 + lane;
+  const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
+  float* xchg = reinterpret_cast<float*>(smem) + grp * 2 * kXchg;  // this group's two buffers
+  const int bar = 1 + grp;
+
+  constexpr int T = BN;  // tokens per tile
+  constexpr int ntok = 16;
+  constexpr int n_chunks = T / 16;
+  auto load_chunk = [&](int c, float (&v)[16]) {
+    uint32_t raw[16];
+    tmem_ld_x16(t_row + c * 16, raw);
+    tc_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]);
+  };
+
+  if (args.splits == 1) {
+    if (!aborted) {
+      for (int c = grp, it = 0; c < n_chunks; c += kGroups, ++it) {
+        float v[16];
+        load_chunk(c, v);
+        epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg + (it & 1) * kXchg, bar,
+                       rs_tile ? rs_tile + c * 16 : nullptr, wscale);
+      }
+    }
+  } else if (!args.cluster) {
+    // Ticketed reduction: every split stores its fp32 partial [T][128] in
+    // global memory; the last split of the tile to arrive (atomic ticket after
+    // a fence) sums them in split order and runs the epilogue.
+    const int tile_lin = tile_m * gridDim.x + tile_n;
+    const size_t per_split = (size_t)n_chunks * 16 * 128;
+    float* part = args.partial + (size_t)tile_lin * args.splits * per_split;
+    float* mine = part + (size_t)split * per_split;
+    if (!aborted) {
+      for (int c = grp; c < n_chunks; c += kGroups) {
+        float v[16];
+        load_chunk(c, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) mine[(c * 16 + j) * 128 + r] = v[j];
+      }
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) *last_sh = (atomicAdd(&args.counters[tile_lin], 1) == args.splits - 1);
+    __syncthreads();
+    if (*last_sh) {
+      __threadfence();
+      if (!aborted) {
+        for (int c = grp, it = 0; c < n_chunks; c += kGroups, ++it) {
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+          for (int s = 0; s < args.splits; ++s) {
+            const float* ps = part + (size_t)s * per_split;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] += __ldcg(ps + (c * 16 + j) * 128 + r);
+          }
+          epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg + (it & 1) * kXchg,
+                         bar, rs_tile ? rs_tile + c * 16 : nullptr, wscale);
+        }
+      }
+      if (threadIdx.x == 0) atomicExch(&args.counters[tile_lin], 0);
+    }
+  } else {
+    // The K splits of this tile form a thread-block cluster.  Each leaves its
+    // fp32 partial [T tokens][128 rows] in its own shared memory (the stage
+    // buffers are free: every stage has been consumed); after a cluster
+    // barrier CTA `rank` sums, over distributed shared memory and in split
+    // order, the tokens rank, rank + S, ... of the tile and runs the epilogue
+    // on them.  A CTA whose wait gave up still takes part in both cluster
+    // barriers (its siblings would otherwise wait for it) but writes nothing.
+    float* part_s = reinterpret_cast<float*>(smem);
+    float* xchg_s = part_s + (size_t)n_chunks * 16 * 128 + grp * 2 * kXchg;
+    for (int c = grp; c < n_chunks; c += kGroups) {
+      float v[16];
+      if (!aborted) {
+        load_chunk(c, v);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) part_s[(c * 16 + j) * 128 + r] = v[j];
+    }
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    if (!aborted) {
+      const int S = args.splits;
+      const int rank = split;  // cluster dims (1, 1, S): rank = blockIdx.z
+      const int mine = (T - rank + S - 1) / S;
+      for (int g0 = grp * 16, it = 0; g0 < mine; g0 += 16 * kGroups, ++it) {
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+        for (int s = 0; s < S; ++s) {
+          const float* ps = cluster.map_shared_rank(part_s, s);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int t = rank + (g0 + j) * S;
+            if (g0 + j < mine) v[j] += ps[t * 128 + r];
+          }
+        }
+        const int cnt = mine - g0 < 16 ? mine - g0 : 16;
+        epilogue_chunk(epi, ao, v, tile_m * T + rank + g0 * S, S, cnt, tile_n, r,
+                       xchg_s + (it & 1) * kXchg, bar, rs_tile ? rs_tile + rank + g0 * S : nullptr,
+                       wscale);
+      }
+    }
+    // no CTA may leave while another still reads its shared memory
+    cluster.sync();
   }
 }
 
@@ -380,119 +532,8 @@ __global__ void __launch_bounds__(gemm_threads(BN), 1)
                               100000000ull);
   }
   __syncthreads();
-  const int q = warp & 3, grp = warp >> 2;  // TMEM lane quarter, epilogue group
-  const int r = q * 32 + lane;
-  const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
-  float* xchg = reinterpret_cast<float*>(smem) + grp * 2 * kXchg;  // this group's two buffers
-  const int bar = 1 + grp;
-  const bool aborted = abort_sh != 0 || !acc_ok;
-
-  constexpr int T = BN;  // tokens per tile
-  constexpr int ntok = 16;
-  constexpr int n_chunks = T / 16;
-  auto load_chunk = [&](int c, float (&v)[16]) {
-    uint32_t raw[16];
-    tmem_ld_x16(t_row + c * 16, raw);
-    tc_wait_ld();
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]);
-  };
-
-  const float* rs_tile = (BN <= 32 && args.rs_ssq) ? rs_sh : nullptr;  // by local token
-  if (args.splits == 1) {
-    if (!aborted) {
-      for (int c = grp, it = 0; c < n_chunks; c += kGroups, ++it) {
-        float v[16];
-        load_chunk(c, v);
-        epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg + (it & 1) * kXchg, bar,
-                       rs_tile ? rs_tile + c * 16 : nullptr);
-      }
-    }
-  } else if (!args.cluster) {
-    // Ticketed reduction: every split stores its fp32 partial [T][128] in
-    // global memory; the last split of the tile to arrive (atomic ticket after
-    // a fence) sums them in split order and runs the epilogue.
-    const int tile_lin = tile_m * gridDim.x + tile_n;
-    const size_t per_split = (size_t)n_chunks * 16 * 128;
-    float* part = args.partial + (size_t)tile_lin * args.splits * per_split;
-    float* mine = part + (size_t)split * per_split;
-    if (!aborted) {
-      for (int c = grp; c < n_chunks; c += kGroups) {
-        float v[16];
-        load_chunk(c, v);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) mine[(c * 16 + j) * 128 + r] = v[j];
-      }
-    }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) last_sh = (atomicAdd(&args.counters[tile_lin], 1) == args.splits - 1);
-    __syncthreads();
-    if (last_sh) {
-      __threadfence();
-      if (!aborted) {
-        for (int c = grp, it = 0; c < n_chunks; c += kGroups, ++it) {
-          float v[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = 0.0f;
-          for (int s = 0; s < args.splits; ++s) {
-            const float* ps = part + (size_t)s * per_split;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] += __ldcg(ps + (c * 16 + j) * 128 + r);
-          }
-          epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg + (it & 1) * kXchg,
-                         bar, rs_tile ? rs_tile + c * 16 : nullptr);
-        }
-      }
-      if (threadIdx.x == 0) atomicExch(&args.counters[tile_lin], 0);
-    }
-  } else {
-    // The K splits of this tile form a thread-block cluster.  Each leaves its
-    // fp32 partial [T tokens][128 rows] in its own shared memory (the stage
-    // buffers are free: every stage has been consumed); after a cluster
-    // barrier CTA `rank` sums, over distributed shared memory and in split
-    // order, the tokens rank, rank + S, ... of the tile and runs the epilogue
-    // on them.  A CTA whose wait gave up still takes part in both cluster
-    // barriers (its siblings would otherwise wait for it) but writes nothing.
-    float* part_s = reinterpret_cast<float*>(smem);
-    float* xchg_s = part_s + (size_t)n_chunks * 16 * 128 + grp * 2 * kXchg;
-    for (int c = grp; c < n_chunks; c += kGroups) {
-      float v[16];
-      if (!aborted) {
-        load_chunk(c, v);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = 0.0f;
-      }
-#pragma unroll
-      for (int j = 0; j < 16; ++j) part_s[(c * 16 + j) * 128 + r] = v[j];
-    }
-    cg::cluster_group cluster = cg::this_cluster();
-    cluster.sync();
-    if (!aborted) {
-      const int S = args.splits;
-      const int rank = split;  // cluster dims (1, 1, S): rank = blockIdx.z
-      const int mine = (T - rank + S - 1) / S;
-      for (int g0 = grp * 16, it = 0; g0 < mine; g0 += 16 * kGroups, ++it) {
-        float v[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = 0.0f;
-        for (int s = 0; s < S; ++s) {
-          const float* ps = cluster.map_shared_rank(part_s, s);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int t = rank + (g0 + j) * S;
-            if (g0 + j < mine) v[j] += ps[t * 128 + r];
-          }
-        }
-        const int cnt = mine - g0 < 16 ? mine - g0 : 16;
-        epilogue_chunk(epi, ao, v, tile_m * T + rank + g0 * S, S, cnt, tile_n, r,
-                       xchg_s + (it & 1) * kXchg, bar, rs_tile ? rs_tile + rank + g0 * S : nullptr);
-      }
-    }
-    // no CTA may leave while another still reads its shared memory
-    cluster.sync();
-  }
+  one_tile_epilogue<BN, kGroups>(smem, tmem, abort_sh != 0 || !acc_ok, ao, args, epi, tile_n, tile_m,
+                                 split, (BN <= 32 && args.rs_ssq) ? rs_sh : nullptr, &last_sh, 1.0f);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);

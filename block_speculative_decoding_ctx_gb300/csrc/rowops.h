@@ -34,5 +34,11 @@ int launch_topk_lse(const float* logits, int rows, int V, int k, unsigned long l
                     float* part_ml, int* counters, int32_t* ids, float* vals, float* lse,
                     int32_t* draft, cudaStream_t s);
 int launch_add_lengths(int B, const int32_t* n_new, int64_t* ctx_len, cudaStream_t s);
+// quant.cu: E4M3 codes and per-row scales from bf16 weights [rows, cols]
+// (cols even), and the check of given codes (n bytes, a multiple of 16) and
+// scales (*flag = 1 on a NaN code or a scale that is not finite and positive).
+int launch_quantize_e4m3(const void* w, int rows, int cols, void* codes, float* scales, cudaStream_t s);
+int launch_check_e4m3(const void* codes, size_t n, const float* scales, size_t rows, int* flag, int grid,
+                      cudaStream_t s);
 
 }  // namespace dfl

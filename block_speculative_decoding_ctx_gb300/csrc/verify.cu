@@ -16,7 +16,8 @@
 // draw, which re-reads only the one chunk that holds the sampled index.  The
 // tickets are reset by that last CTA, so the scratch needs no clearing
 // between calls.  All draws are integer arithmetic on floor(w * 2^45), which
-// makes them independent of summation order.
+// makes them independent of summation order.  The temperature / top-p
+// preparation of a row is in probs.cu.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -315,157 +316,6 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// -------------------------------------------------- temperature and top-p
-
-constexpr int kProbThreads = 1024;
-
-struct SoftmaxRow {
-  const float* row;
-  float invT, M, S;
-  // z = l / T - M (one fused rounding), e = exp(z), p = e / S: the same
-  // instruction sequence wherever a probability is needed.
-  __device__ __forceinline__ float operator()(int v) const {
-    return __fdiv_rn(expf(__fmaf_rn(__ldg(row + v), invT, -M)), S);
-  }
-};
-
-// Warp-aggregated add of (mass, count) into a 256-bin shared histogram.
-__device__ __forceinline__ void hist_add(unsigned long long* hist, unsigned* histc, bool active,
-                                         uint32_t digit, unsigned long long mass) {
-  const unsigned act = __ballot_sync(0xffffffffu, active);
-  if (!active) return;
-  const unsigned grp = __match_any_sync(act, digit);
-  const unsigned lo = __reduce_add_sync(grp, (unsigned)(mass & 0x7FFFFFu));
-  const unsigned hi = __reduce_add_sync(grp, (unsigned)(mass >> 23));
-  const int lane = threadIdx.x & 31;
-  if (lane == __ffs(grp) - 1) {
-    atomicAdd(&hist[digit], ((unsigned long long)hi << 23) + lo);
-    atomicAdd(&histc[digit], (unsigned)__popc(grp));
-  }
-}
-
-__global__ void __launch_bounds__(kProbThreads)
-    probs_kernel(const float* __restrict__ logits, int V, float invT, float top_p,
-                 float* __restrict__ probs) {
-  pdl_enter();
-  __shared__ float redf[33];
-  __shared__ unsigned long long redu[33];
-  __shared__ unsigned long long hist[256];
-  __shared__ unsigned histc[256];
-  __shared__ unsigned long long s_above, s_thr;
-  __shared__ uint32_t s_prefix, s_mask, s_ntie;
-  const int r = blockIdx.x;
-  const float* row = logits + (size_t)r * V;
-  float* out = probs + (size_t)r * V;
-
-  // max of l / T, then the normaliser
-  float m = -INFINITY;
-  for (int v = threadIdx.x; v < V; v += kProbThreads) m = fmaxf(m, __ldg(row + v) * invT);
-  m = warp_max_f(m);
-  if ((threadIdx.x & 31) == 0) redf[threadIdx.x >> 5] = m;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    float t = redf[threadIdx.x];
-    t = warp_max_f(t);
-    if (threadIdx.x == 0) redf[32] = t;
-  }
-  __syncthreads();
-  const float M = redf[32];
-  float s = 0.0f;
-  for (int v = threadIdx.x; v < V; v += kProbThreads)
-    s += expf(__fmaf_rn(__ldg(row + v), invT, -M));
-  s = block_sum(s, redf);
-  const SoftmaxRow P{row, invT, M, s};
-
-  if (!(top_p < 1.0f)) {
-    for (int v = threadIdx.x; v < V; v += kProbThreads) out[v] = P(v);
-    return;
-  }
-
-  // Fixed-point total and the nucleus threshold thr = ceil(top_p * Z).
-  unsigned long long Z = 0;
-  for (int v = threadIdx.x; v < V; v += kProbThreads) Z += to_fixed45(P(v));
-  Z = block_sum(Z, redu);
-  if (threadIdx.x == 0) {
-    unsigned long long thr = (unsigned long long)ceil((double)top_p * (double)Z);
-    if (thr == 0) thr = 1;
-    if (thr > Z) thr = Z;
-    s_thr = thr;
-    s_above = 0;
-    s_prefix = 0;
-    s_mask = 0;
-  }
-  __syncthreads();
-
-  // Radix select, 8 bits per pass, on the bit pattern of p (p >= 0, so the
-  // pattern orders like the value): find the largest key t* whose mass of
-  // {key >= t*} reaches thr.  s_above ends as the mass of {key > t*}.
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += kProbThreads) {
-      hist[i] = 0;
-      histc[i] = 0;
-    }
-    __syncthreads();
-    const uint32_t prefix = s_prefix, mask = s_mask;
-    for (int v0 = 0; v0 < V; v0 += kProbThreads) {
-      const int v = v0 + threadIdx.x;
-      float pv = 0.0f;
-      if (v < V) pv = P(v);
-      const uint32_t key = __float_as_uint(pv);
-      const bool act = (v < V) && ((key & mask) == prefix);
-      hist_add(hist, histc, act, (key >> shift) & 255u, to_fixed45(pv));
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      unsigned long long cum = s_above;
-      int sel = 0;
-      for (int d = 255; d >= 0; --d) {
-        if (cum + hist[d] >= s_thr) {
-          sel = d;
-          break;
-        }
-        cum += hist[d];
-      }
-      s_above = cum;
-      s_prefix = prefix | ((uint32_t)sel << shift);
-      s_mask = mask | (255u << shift);
-      s_ntie = histc[sel];
-    }
-    __syncthreads();
-  }
-  const uint32_t tstar = s_prefix;
-  const unsigned long long above = s_above;
-  const unsigned long long pstar = to_fixed45(__uint_as_float(tstar));
-  const unsigned n_tie = s_ntie;
-  unsigned long long k_tie = (s_thr - above + pstar - 1) / pstar;  // pstar > 0 by construction
-  if (k_tie > n_tie) k_tie = n_tie;
-  const unsigned long long kept = above + k_tie * pstar;
-  const float Sk = (float)((double)kept * 0x1p-45);
-
-  if (k_tie == n_tie) {
-    for (int v = threadIdx.x; v < V; v += kProbThreads) {
-      const float pv = P(v);
-      out[v] = (__float_as_uint(pv) >= tstar) ? __fdiv_rn(pv, Sk) : 0.0f;
-    }
-    return;
-  }
-  // Some ties at t* are dropped: keep the lowest ids.  Contiguous segments
-  // per thread give an id-ordered rank through one block scan.
-  const int seg = (V + kProbThreads - 1) / kProbThreads;
-  const int s0 = min(V, (int)threadIdx.x * seg), s1 = min(V, s0 + seg);
-  unsigned long long nt = 0;
-  for (int v = s0; v < s1; ++v) nt += (__float_as_uint(P(v)) == tstar);
-  unsigned long long tot;
-  unsigned long long rank = block_exclusive_scan(nt, redu, &tot);
-  for (int v = s0; v < s1; ++v) {
-    const float pv = P(v);
-    const uint32_t key = __float_as_uint(pv);
-    bool keep = key > tstar;
-    if (key == tstar) keep = (rank++ < k_tie);
-    out[v] = keep ? __fdiv_rn(pv, Sk) : 0.0f;
-  }
-}
-
 }  // namespace
 
 int launch_verify_greedy(int B, int gamma, int V, const float* target, const int32_t* draft,
@@ -497,12 +347,6 @@ int launch_sample_rows(int rows, int V, const float* w, long long row_stride, in
   dim3 grid(chunks, rows);
   return launch_pdl(sample_rows_kernel, grid, dim3(kThreads), 0, s, w, row_stride, V, chunks,
                     rows_per_req, seeds, step, purpose, out, out_stride, counters, zsum, status);
-}
-
-int launch_probs(int rows, int V, const float* logits, float temperature, float top_p,
-                 float* probs, cudaStream_t s) {
-  return launch_pdl(probs_kernel, dim3(rows), dim3(kProbThreads), 0, s, logits, V, 1.0f / temperature,
-                    top_p, probs);
 }
 
 }  // namespace dfl

@@ -50,9 +50,11 @@
  * bf16 as given), and so does the context K/V ring.
  *
  * Memory and ownership.  Every pointer argument, unless it says "host", is
- * device memory owned by the caller.  dflash_create allocates the handle's
- * fp16 matrix copy (2 bytes per element of those matrices; dflash_destroy
- * frees it); no other call allocates device memory.  Calls other than
+ * device memory owned by the caller.  With bf16 weights dflash_create
+ * allocates the handle's fp16 matrix copy (2 bytes per element of those
+ * matrices; dflash_destroy frees it); with E4M3 weights the handle holds no
+ * device memory.  No other call allocates device memory, except the
+ * benchmark hook dflash_profile_enable.  Calls other than
  * create/destroy are asynchronous on the given stream, never synchronise the
  * host, and may be captured into a CUDA graph.
  *
@@ -119,7 +121,19 @@ typedef struct dflash_config {
   float rope_theta;
   float eps;
   int mask_id;     /* MASK token id; -1 selects vocab - 1 */
+  int weight_format; /* DFLASH_WEIGHTS_BF16 (0) or DFLASH_WEIGHTS_E4M3 (1) */
 } dflash_config;
+
+/* Storage of the drafter's matrices (w_qkv, w_o, w_gate, w_up, w_down of
+ * every layer, and lm_head).  BF16: bf16 values, copied by dflash_create into
+ * an fp16 buffer of the handle.  E4M3: FP8 codes (1 sign, 4 exponent bits
+ * with bias 7, 3 mantissa bits, no infinities, largest finite 448) with one
+ * float32 scale per output row, weight[r][c] = code[r][c] * scale[r]; used in
+ * place (the handle holds no copy), half the bytes a draft pass streams.  The
+ * pages serve their models in bf16, FP8 and NVFP4 ("Speculative decoding"
+ * product doc, introduction; model card, section "Serve") without fixing the
+ * FP8 format; dflash_quantize_e4m3 makes such weights from bf16 ones. */
+enum { DFLASH_WEIGHTS_BF16 = 0, DFLASH_WEIGHTS_E4M3 = 1 };
 
 /* One drafter layer.  Matrices are bf16 row-major [out, in] (the torch Linear
  * layout), gains are float32.  All device pointers, 16-byte aligned. */
@@ -131,6 +145,13 @@ typedef struct dflash_layer_weights {
   const void* w_gate; /* bf16 [F, d] */
   const void* w_up;   /* bf16 [F, d] */
   const void* w_down; /* bf16 [d, F] */
+  /* E4M3 weights only: float32 scale of every output row of the matrix above
+   * of the same name ([(Hq + 2 Hkv) hd], [d], [F], [F], [d]); else NULL */
+  const float* s_qkv;
+  const float* s_o;
+  const float* s_gate;
+  const float* s_up;
+  const float* s_down;
 } dflash_layer_weights;
 
 typedef struct dflash_weights {
@@ -140,19 +161,24 @@ typedef struct dflash_weights {
   const void* g_c;     /* float32 [d], gain of the RMSNorm that forms H_t */
   const void* g_final; /* float32 [d] */
   const dflash_layer_weights* layers; /* HOST array of n_layers entries */
+  const float* s_lm_head; /* E4M3 weights only: float32 [V] row scales of lm_head */
 } dflash_weights;
 
 typedef struct dflash_handle dflash_handle;
 
-/* Validate cfg, copy w_qkv, w_o, w_gate, w_up, w_down of every layer and
- * lm_head into the handle's fp16 buffer (allocated here; synchronises the
- * device), record the other weight pointers and encode the TMA descriptors.
- * embed, w_c and the gains are read from the caller's memory later: they
- * must stay alive and unchanged while the handle is used; the copied
- * matrices need not.  Must be called with the weights' device current.
- * Returns DFLASH_OK and *out, or an error (then *out is NULL):
- * DFLASH_ERR_RANGE if a copied matrix holds a value beyond +-65504 (or a
- * NaN), DFLASH_ERR_CUDA if the buffer cannot be allocated. */
+/* Validate cfg, record the weight pointers and encode the TMA descriptors.
+ * BF16 weights: copy w_qkv, w_o, w_gate, w_up, w_down of every layer and
+ * lm_head into the handle's fp16 buffer (allocated here), which the draft
+ * pass then reads; the copied matrices need not stay alive.  E4M3 weights:
+ * nothing is copied; the codes and scales are read in place and must stay
+ * alive and unchanged while the handle is used, like embed, w_c and the
+ * gains in both formats.  Synchronises the device (the weights may have
+ * been written on any stream).  Must be called with the weights' device
+ * current.  Returns DFLASH_OK and *out, or an error (then *out is NULL):
+ * DFLASH_ERR_RANGE if a copied bf16 matrix holds a value beyond +-65504 (or a
+ * NaN), or an E4M3 matrix a NaN code or a scale that is not finite and
+ * positive; DFLASH_ERR_ARG if an E4M3 scale pointer is missing;
+ * DFLASH_ERR_CUDA if a buffer cannot be allocated. */
 int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_handle** out);
 int dflash_destroy(dflash_handle* h);
 
@@ -269,15 +295,20 @@ int dflash_verify(int mode, int B, int gamma, int vocab, const float* target, co
                   int32_t* accept_len, int32_t* tokens, int32_t* next_anchor, int32_t* n_append,
                   void* workspace, size_t ws_bytes, dflash_stream_t stream);
 
-/* Benchmark hook.  dflash_profile_enable(h, n) creates n pairs of CUDA
- * events (n = 0 destroys them); afterwards every draft_block call on h
- * records a pair around each of its first n kernel launches, on the call's
- * stream.  dflash_profile_read synchronises on the last recorded event and
- * returns, for each launch of the last call, its duration in ms, its
- * algorithmic bytes (operands read + results written, each counted once) and
- * its kind (DFLASH_KIND_*); *count receives the number of launches (<= cap).
- * A draft_block call captured into a CUDA graph records the events as event
- * nodes, so a replayed graph can be profiled too (read after the replay). */
+/* Benchmark hook.  dflash_profile_enable(h, n) allocates a device buffer of
+ * n + 1 timestamps (n = 0 frees it); afterwards every draft_block call on h
+ * launches, on the call's stream, a one-warp mark kernel before its first
+ * launch and after each of its first n launches.  A mark lets the next kernel
+ * start early (programmatic dependent launch) as it would without it, waits
+ * for the launch before it to complete and writes the device clock
+ * (%globaltimer).  dflash_profile_read synchronises the device and returns,
+ * for each launch of the last call, the time from the previous launch's
+ * completion to its own in ms (these add up to the whole pass, overlap
+ * between neighbouring kernels included), its algorithmic bytes (operands
+ * read + results written, each counted once) and its kind (DFLASH_KIND_*);
+ * *count receives the number of launches (<= cap).  A draft_block call
+ * captured into a CUDA graph captures its marks too, so a replayed graph can
+ * be profiled (read after the replay). */
 enum { DFLASH_KIND_GEMM = 0, DFLASH_KIND_ATTENTION = 1, DFLASH_KIND_NORM = 2,
        DFLASH_KIND_TOPK = 3, DFLASH_KIND_SAMPLING = 4 };
 int dflash_profile_enable(dflash_handle* h, int n_pairs);
@@ -300,11 +331,15 @@ int dflash_profile_read(dflash_handle* h, float* ms, double* bytes, int* kinds, 
  * asynchronous memset on the given stream.
  *   Limit: 256 + 256*ceil(4B/256) + 256*ceil(8*B*gamma/256)
  *          + 16*B*ceil(vocab/8192) bytes (rounded up to 256) must not exceed
- *          256 KiB — e.g. B <= 256 at gamma 16 and vocabulary 151,936;
- *          larger calls return DFLASH_ERR_SHAPE and launch nothing.
- *   The first call on a device looks up the array's device address with that
- *   device current (cudaGetSymbolAddress) and caches it; make that first call
- *   before any stream capture.
+ *          256 KiB: at gamma 16 and vocabulary 151,936 the largest B is 600
+ *          (B = 601 needs 262,656 bytes); larger calls return
+ *          DFLASH_ERR_SHAPE, launch nothing and leave the outputs untouched.
+ *   A call made outside any stream capture looks up the array's device
+ *   address with the current device (cudaGetSymbolAddress) and remembers it
+ *   with the current context.  A call made while its stream is captured uses
+ *   that remembered address, so the first call on a device, and the first
+ *   after a device reset, must be made before any capture; a captured call
+ *   without one returns DFLASH_ERR_UNSUPPORTED and launches nothing.
  *   Every call on a device shares the one array and the array keeps the last
  *   call's contents: calls whose work overlaps on the GPU (two streams, or
  *   graphs replayed concurrently) race on it and must be serialised by the
@@ -314,6 +349,20 @@ int dflash_verify_noalloc(int mode, int B, int gamma, int vocab, const float* ta
                           const float* q, const int32_t* draft, const uint64_t* seeds,
                           uint64_t step, int32_t* accept_len, int32_t* tokens,
                           int32_t* next_anchor, int32_t* n_append, dflash_stream_t stream);
+
+/* E4M3 weights from bf16 ones (the format of DFLASH_WEIGHTS_E4M3), one CTA
+ * per row: scale[r] = max_c |w[r][c]| / 448 in float32 (1 for a row of
+ * zeros); code[r][c] = w[r][c] / scale[r] (float32 division, round to
+ * nearest) rounded to the nearest E4M3 value, ties to an even mantissa,
+ * saturating at +-448.  A NaN or infinite weight makes NaN codes, which
+ * dflash_create refuses.  The pages fix no FP8 scheme; this is the
+ * library's reading (see DFLASH_WEIGHTS_E4M3).
+ *   w       bf16 [rows, cols], cols a multiple of 16, 16-byte aligned
+ *   codes   uint8 [rows, cols] out, 16-byte aligned
+ *   scales  float32 [rows] out
+ * Asynchronous on the stream; allocates nothing. */
+int dflash_quantize_e4m3(const void* w, int rows, int cols, void* codes, float* scales,
+                         dflash_stream_t stream);
 
 /* Copy the workspace status word to the host (synchronises the stream). */
 int dflash_read_status(const void* workspace, int32_t* status_host, dflash_stream_t stream);

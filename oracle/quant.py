@@ -36,26 +36,26 @@ def e4m3_value(code):
     return sign * mag
 
 
-# the 127 non-negative finite values in code order (codes 0x00 .. 0x7E are
-# increasing in value)
-_POS = e4m3_value(np.arange(127, dtype=np.uint8))
-
-
 def e4m3_round(x):
     """Codes (uint8) of float32 values x: nearest E4M3 value, ties to an even
-    mantissa, magnitudes beyond 448 saturate.  x must not be NaN."""
+    mantissa, magnitudes beyond 448 saturate.  x must not be NaN.
+
+    Below 2^-6 the E4M3 values are the multiples of 2^-9; in the binade
+    [2^e, 2^(e+1)) they are the multiples of 2^(e-3).  Rounding |x| to that
+    grid with round-half-even gives the mantissa count m (the scaling by a
+    power of two is exact in float32, so only the rounding to an integer
+    rounds); the codes 0x00 .. 0x7E enumerate the
+    non-negative values in increasing order, so the code is m for the
+    subnormal grid (m = 8 is 2^-6, code 0x08) and 8 (e + 7) + (m - 8) in
+    binade e (m = 16 is the next binade's first value, same formula)."""
     x = np.asarray(x, dtype=np.float32)
-    a = np.minimum(np.abs(x).astype(np.float64), E4M3_MAX)
-    hi = np.searchsorted(_POS, a, side="left")          # first value >= a
-    hi = np.minimum(hi, 126)
-    lo = np.maximum(hi - 1, 0)
-    d_lo = a - _POS[lo]
-    d_hi = _POS[hi] - a
-    # pick the nearer; on a tie the code with the even last mantissa bit
-    take_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
-    idx = np.where(a == _POS[hi], hi, np.where(take_hi, hi, lo)).astype(np.uint8)
+    a = np.minimum(np.abs(x), np.float32(E4M3_MAX))
+    _, k = np.frexp(a)                                  # a = f 2^k, f in [0.5, 1)
+    e = np.maximum(k - 1, -6).astype(np.int32)          # binade; subnormals share -6's grid
+    m = np.rint(np.ldexp(a, 3 - e)).astype(np.int32)    # round half to even
+    code = np.where(a < np.float32(2.0 ** -6), m, 8 * (e + 7) + (m - 8)).astype(np.uint8)
     # the sign bit follows x, also where it rounds to zero
-    return np.where(np.signbit(x), idx | np.uint8(0x80), idx).astype(np.uint8)
+    return np.where(np.signbit(x), code | np.uint8(0x80), code).astype(np.uint8)
 
 
 def quantize_rows(w):
@@ -68,6 +68,10 @@ def quantize_rows(w):
     return e4m3_round(x), scale
 
 
+# value of every code (the formula of e4m3_value, tabulated once)
+_VALUE = e4m3_value(np.arange(256, dtype=np.uint8))
+
+
 def dequantize_rows(codes, scales):
     """float64 weights code value * s_r."""
-    return e4m3_value(codes) * np.asarray(scales, dtype=np.float64)[:, None]
+    return _VALUE[np.asarray(codes, dtype=np.uint8)] * np.asarray(scales, dtype=np.float64)[:, None]

@@ -128,3 +128,38 @@ def check_q_against_oracle_logits(q_gpu, z_gpu, z_ref, T, top_p):
         floor = min(qg[r][both].min(), qr[both].min())
         assert (qg[r][kg & ~kr] <= f * floor).all() and (qr[kr & ~kg] <= f * floor).all()
     return worst
+
+
+def oracle_e4m3_weights(W, chunk_rows=1024):
+    """Float64 weights the oracle reads for an E4M3 drafter: every layer
+    matrix and the LM head quantized by the oracle's own E4M3 rule from the
+    same bf16 values and dequantized exactly (code value times row scale);
+    embed, w_c and the gains widened as they are.  Also returns the oracle's
+    codes and scales of layer 0's w_qkv for a bit-exact check."""
+    from oracle import quant
+
+    import concurrent.futures
+    import os
+
+    def deq(t):
+        out = np.empty(t.shape, dtype=np.float64)
+
+        def one(r0):
+            codes, s = quant.quantize_rows(t[r0:r0 + chunk_rows].float().numpy())
+            out[r0:r0 + chunk_rows] = quant.dequantize_rows(codes, s)
+
+        # rows are independent; numpy releases the interpreter lock in its loops
+        with concurrent.futures.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
+            list(ex.map(one, range(0, t.shape[0], chunk_rows)))
+        return out
+
+    W64 = {k: (widen(v) if k != "layers" else None) for k, v in W.items()}
+    W64["lm_head"] = deq(W["lm_head"])
+    W64["layers"] = []
+    for lw in W["layers"]:
+        d = {k: widen(v) for k, v in lw.items()}
+        for k in ("w_qkv", "w_o", "w_gate", "w_up", "w_down"):
+            d[k] = deq(lw[k])
+        W64["layers"].append(d)
+    ref_codes = quant.quantize_rows(W["layers"][0]["w_qkv"].float().numpy())
+    return W64, ref_codes

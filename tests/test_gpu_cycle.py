@@ -301,3 +301,29 @@ def test_activation_beyond_fp16_range_is_reported():
                            ws, out=dict(draft=torch.empty((1, 3), dtype=torch.int32, device=dev)))
     torch.cuda.synchronize()
     assert dfl.dflash_read_status(ws) == -9
+
+
+@pytest.mark.parametrize("gamma", [4, 16])
+def test_ring_key_beyond_fp16_range_is_reported(gamma):
+    """Attention reads ring keys as fp16: a bf16 key beyond +-65504 written
+    into the ring by the caller is reported (DFLASH_ERR_RANGE), on the path
+    that widens keys in each consumer's registers (gamma 4: two row tiles) and
+    on the one where a converter warp widens them in shared memory (gamma 16:
+    five row tiles)."""
+    dims = synth.DIMS["small"]
+    W = synth.weights(dims, 98)
+    h = dfl.dflash_create(tu.lib_cfg(dims, batch_max=1, gamma_max=16), tu.to_dev(W))
+    rk, rv = synth.ring(dims, 1, 99)
+    dev = torch.device("cuda")
+    out = dict(draft=torch.empty((1, gamma - 1), dtype=torch.int32, device=dev))
+    anchor = torch.tensor([3], dtype=torch.int32, device=dev)
+    L = torch.tensor([200], dtype=torch.int64, device=dev)
+    ws = dfl.workspace(dfl.dflash_draft_workspace_bytes(h))
+    dfl.dflash_draft_block(h, anchor, L, rk.cuda(), rv.cuda(), gamma, ws, out=out)
+    torch.cuda.synchronize()
+    assert dfl.dflash_read_status(ws) == 0
+    rk[1, 0, 1, 150, 17] = 1.0e5                 # layer 1, KV head 1, a visible slot
+    ws2 = dfl.workspace(dfl.dflash_draft_workspace_bytes(h))
+    dfl.dflash_draft_block(h, anchor, L, rk.cuda(), rv.cuda(), gamma, ws2, out=out)
+    torch.cuda.synchronize()
+    assert dfl.dflash_read_status(ws2) == -9

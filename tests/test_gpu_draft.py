@@ -163,6 +163,9 @@ def _oracle_ring(dims, W, B, feats, starts, n_new):
     ("tiny", 2, 8, [0, 61], [8, 5]),          # second request wraps the window
     ("small", 3, 40, [5, 250, 1000], [40, 17, 0]),
     ("small128", 2, 20, [511, 3], [20, 1]),
+    # up to 32 tokens the RMSNorm is folded into the W_c and K/V GEMMs
+    ("small128", 2, 16, [511, 3], [16, 9]),
+    ("small", 4, 8, [0, 255, 1000, 7], [8, 1, 0, 5]),
 ])
 def test_ctx_append_matches_oracle(name, B, n_max, starts, n_new):
     dims = synth.DIMS[name]
