@@ -64,6 +64,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=5, help="drafter layers (profiling cases only)")
     ap.add_argument("--weights", default="bf16", choices=["bf16", "e4m3"],
                     help="drafter weight format of the profiling case (--profile-cycles)")
+    ap.add_argument("--sampled", action="store_true",
+                    help="sampled drafting and verification in the profiling case (--profile-cycles)")
     ap.add_argument("--cpu-probe", default=None, choices=["tiny", "verify16"],
                     help=argparse.SUPPRESS)  # one oracle timing, run in a child process
     return ap.parse_args()
@@ -88,6 +90,14 @@ def spawn_replicas(args):
 
 
 # ----------------------------------------------------------------- helpers
+
+_T0 = time.perf_counter()
+
+
+def progress(what):
+    """Elapsed wall time of the bench's phases, on stderr (the JSON line is stdout)."""
+    print(f"[bench {time.perf_counter() - _T0:7.1f} s] {what}", file=sys.stderr, flush=True)
+
 
 def dist_setup(backend=None):
     """Rank, world size; initialises the process group for world size > 1
@@ -229,6 +239,8 @@ def time_graph(g, steps, stream):
 
 def capture(fn, stream):
     g = torch.cuda.CUDAGraph()
+    # work queued on other streams (workspace fills, a prefill) must land first
+    torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         fn()                    # eager warm-up outside the capture
     torch.cuda.synchronize()
@@ -295,6 +307,7 @@ class Cycle:
         self.out = dict(topk_ids=self.ids, topk_vals=self.vals, lse=self.lse, logits=self.logits,
                         draft=self.draft)
         self.sampling = None
+        torch.cuda.synchronize()   # the prefill and workspace fills ran on the current stream
         if sampled:
             from block_speculative_decoding_ctx_gb300 import synth
             self.seeds = synth.seeds(B + req0, seed)[req0:].to(dev)   # Philox key per request
@@ -303,6 +316,7 @@ class Cycle:
             self.ws_p = dfl.workspace(dfl.dflash_probs_workspace_bytes(B * gamma, V), dev)
             self.out["q"] = self.q
             self.sampling = dict(temperature=SAMPLING_T, top_p=SAMPLING_TOP_P, seeds=self.seeds, step=1)
+            torch.cuda.synchronize()
 
     def append(self):
         self.dfl.dflash_ctx_append(self.h, self.feats, self.n_app, self.ctx, self.rk, self.rv, self.ws_a)
@@ -341,12 +355,12 @@ class Cycle:
 
 
 # DRAM bytes (read + written) of the draft pass's GEMM launches at batch 1,
-# gamma 8, five layers: ncu's dram__bytes_read.sum + dram__bytes_write.sum per
-# launch on a one-layer pass (4 GEMMs per layer + the LM head), scaled to five
-# layers.  Taken with the GEMM kernels that fold the RMSNorms in at this
-# batch (residual-add epilogues also write fp16(x * g) and per-tile sums of
-# squares); 4,871,884,288 algorithmic bytes.
-GEMM_TRAFFIC_PER_PASS = 4879.1e6
+# gamma 8, five layers: ncu's dram__bytes_read.sum + dram__bytes_write.sum of
+# the QKV, O, gate|up, down and LM-head launches of a one-layer pass (the
+# layer's four scaled to five layers), with the GEMM kernels as they stand
+# (folded RMSNorms, the LM head writing fp32 logits); 4,871,884,288
+# algorithmic bytes.
+GEMM_TRAFFIC_PER_PASS = 4882.1e6
 
 
 def gpu_launches_per_step(dims, tokens, with_append=True, sampled=False):
@@ -370,6 +384,7 @@ def acceptance_stats(cyc, g_step, stream, B, G, steps, sigma):
     dev = cyc.n_app.device
     hist = torch.zeros(G + 1, dtype=torch.int64, device=dev)
     ones = torch.ones(B, dtype=torch.int64, device=dev)
+    torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for _ in range(steps):
             g_step.replay()
@@ -442,7 +457,8 @@ def run_ours(args, rank, ws):
     else:
         h = dfl.dflash_create(cfg, W)
     r0, _ = replica_requests(B, rank, ws)
-    cyc = Cycle(dfl, h, dims, B, G, [args.context] * B, args.sigma, dev, 99 + r0)
+    cyc = Cycle(dfl, h, dims, B, G, [args.context] * B, args.sigma, dev, 99 + r0,
+                sampled=bool(args.profile_cycles and args.sampled))
     stream = torch.cuda.Stream(device=dev)
     if args.profile_cycles:
         with torch.cuda.stream(stream):
@@ -479,6 +495,7 @@ def run_ours(args, rank, ws):
     t_path_max = max_over_ranks(t_path, ws)
 
     # -------------------------- acceptance along the block (untimed replays)
+    progress("headline timed")
     acceptance = acceptance_stats(cyc, g_step, stream, B, G, max(64, 256 // B), args.sigma)
 
     # ------------------------------------ dominant kernel (GEMMs of the pass)
@@ -506,18 +523,23 @@ def run_ours(args, rank, ws):
                                      for r in rows[-1][:9]]}
 
     # ------------------------------------------------- end to end (host buffers)
+    progress("acceptance and launch profile")
     e2e = run_e2e(args, dfl, cyc, stream, g_step)
+    progress("end to end")
 
     extras, sweep, fp8 = {}, None, None
     if not args.no_extras and ws == 1:
         del cyc, g_step, g_stand, g_draft, g_app, g_ver, h
         torch.cuda.empty_cache()
         fp8 = run_fp8_line(args, dfl, dims, W, dev, stream)
+        progress("E4M3 line")
         torch.cuda.empty_cache()
         extras = run_batch_lines(args, dfl, dims, W, dev, stream)
+        progress("batch lines")
         del W
         torch.cuda.empty_cache()
         sweep = verify_sweep(args, dfl, dev, stream)
+        progress("verify sweep")
 
     value = job_value(B, ws, t_path_max)
     res = {
@@ -584,6 +606,10 @@ def run_fp8_line(args, dfl, dims, W, dev, stream):
                "gemm_GBps": round(by / (gemm_ms * 1e-3) / 1e9, 1),
                "gemm_frac_of_hbm": round(by / (gemm_ms * 1e-3) / 1e9 / hbm, 4),
                "kernel_ms_per_pass_by_kind": {k: round(v, 4) for k, v in kinds.items()},
+               "first_layer_launches_us_GBps": [[r[2], round(r[0] * 1e3, 1), round(r[1] / (r[0] * 1e-3) / 1e9, 1)]
+                                                for r in rows[-1][:9]] +
+                                               [["lm_head", round(gemm[-1][0] * 1e3, 1),
+                                                 round(gemm[-1][1] / (gemm[-1][0] * 1e-3) / 1e9, 1)]],
                "status": dfl.dflash_read_status(cyc.ws_d)}
         del h, cyc, g_step, g_stand, g_draft, Wq
         return res
@@ -777,12 +803,13 @@ def verify_sweep(args, dfl, dev, stream):
     hbm = measured_peaks()[0]
     V = DIMS_FULL["vocab"]
     flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)
-    reps = 10
+    reps = 5
     rows = []
 
     def time_calls(fn):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(reps)]
+        torch.cuda.synchronize()        # inputs were made on the current stream
         with torch.cuda.stream(stream):
             fn()
             for e0, e1 in ev:
@@ -805,8 +832,10 @@ def verify_sweep(args, dfl, dev, stream):
             ws_v = dfl.workspace(dfl.dflash_verify_workspace_bytes(B, gamma, V), dev)
             n = torch.empty(B, dtype=torch.int32, device=dev)
             tok = torch.empty((B, gamma), dtype=torch.int32, device=dev)
+            torch.cuda.synchronize()
             with torch.cuda.stream(stream):
                 dfl.dflash_sample_draft(q, seeds, 3, y, ws_s)
+            torch.cuda.synchronize()
             for sigma in SWEEP_SIGMA:
                 t = d + torch.randn((B, gamma, V), generator=gen, device=dev) * sigma
                 p = torch.softmax(t, dim=-1)
@@ -1004,6 +1033,7 @@ def main():
     if rank == 0:
         if not args.no_cpu and ws == 1 and not args.profile_cycles:
             res["cpu_baseline"] = cpu_baseline()
+            progress("CPU baseline")
         print(json.dumps(res), flush=True)
     if ws > 1:
         import torch.distributed as dist

@@ -10,9 +10,11 @@
 //   embed [anchor, MASK...] + RMSNorm (+RoPE table) -> for each layer: QKV
 //   GEMM (+RoPE) -> block attention over [ring window ; block] -> O GEMM ->
 //   residual add + RMSNorm -> gate|up GEMM (+SwiGLU) -> down GEMM -> residual
-//   add + RMSNorm (final RMSNorm gathers the gamma-1 MASK rows) -> LM head GEMM (fp32
-//   logits) -> top-k + log-sum-exp [-> q = top_p(softmax(logits / T)) ->
-//   y ~ q].
+//   add + RMSNorm (final RMSNorm gathers the gamma-1 MASK rows) -> LM head GEMM
+//   (fp32 logits, then a chunked top-k + log-sum-exp kernel; or, when no
+//   logits are wanted, an epilogue that keeps each vocabulary tile's top keys
+//   and (max, sum of exp), then a merge kernel) [-> q = top_p(softmax(logits
+//   / T)) -> y ~ q].
 // Every drafter contraction runs on fp16 operands: the handle holds an fp16
 // copy of the matrices (exact re-encoding of the bf16 values) and every
 // activation between kernels is stored as fp16.
@@ -114,8 +116,10 @@ struct DraftWs {
   float2* rope_cs;
   float* ssq;  // [hidden / 128][M] per-tile sums of squares of the stream
   float* gemm_partial;
-  unsigned long long* topk_keys;
+  unsigned long long* topk_keys;  // chunked top-k partials over the fp32 logits
   float* topk_ml;
+  unsigned long long* tk_keys;  // LM-head epilogue top-k partials [R][vocab tiles][slots]
+  float2* tk_ml;                // [R][vocab tiles]
   unsigned long long* samp_zsum;
   size_t bytes;
 };
@@ -147,6 +151,9 @@ DraftWs draft_layout(const dflash_handle* h, void* base) {
   w.gemm_partial = cv.take<float>(kGemmPartialFloats);
   w.topk_keys = cv.take<unsigned long long>(R * chunks * 16);
   w.topk_ml = cv.take<float>(R * chunks * 2);
+  const size_t vtiles = (size_t)((c.vocab + 127) / 128);
+  w.tk_keys = cv.take<unsigned long long>(R * vtiles * topk_slots(c.topk_max));
+  w.tk_ml = cv.take<float2>(R * vtiles);
   w.samp_zsum = cv.take<unsigned long long>(R * chunks);
   w.bytes = cv.off;
   return w;
@@ -763,32 +770,56 @@ int dflash_draft_block(dflash_handle* h, int B, int gamma, const int32_t* anchor
     if (rc) return rc;
     prof_end(h, s, slot, (double)(l + 1 < c.n_layers ? M : R) * d * (defer ? 14 : 6), DFLASH_KIND_NORM);
   }
-  float* logits = out->logits ? out->logits : ws.logits;
+  // Top-k, log-sum-exp and the top-1 draft.  When the caller wants fp32
+  // logits or sampling needs them, the LM head writes them and a chunked
+  // top-k kernel reads them back.  Otherwise the logits are never written:
+  // the LM head's epilogue keeps each vocabulary tile's top keys and (max,
+  // sum of exp) per MASK row and a merge kernel finishes.  Measured on
+  // GB300 with logits written in both: the epilogue's top-k costs the LM head
+  // more than the separate kernel takes (batch 1: +22 us against 15 us;
+  // batch 32, gamma 8: +83 us against 98 us).
+  float* logits = out->logits ? out->logits : (sampling ? ws.logits : nullptr);
+  const bool fused_topk = logits == nullptr;
+  const int k_eff = topk > 0 ? topk : 1;
+  const int vtiles = (c.vocab + 127) / 128;
+  const int slots = topk_slots(c.topk_max);
+  const double part_bytes = (double)R * vtiles * (8.0 * k_eff + 8.0);
   {  // shared LM head on the gamma - 1 MASK rows
     GemmAMaps A;
     A.map[0] = h->lm_head;
-    const int nt = (c.vocab + 127) / 128;
+    const double logit_bytes = logits ? 4.0 * R * c.vocab : part_bytes;
+    GemmEpi e = epi_base(EPI_F32, fuse_norm ? M : R, c.vocab, logits, c.vocab, ws.status);
+    if (fused_topk) {
+      e.tk_keys = ws.tk_keys;
+      e.tk_ml = ws.tk_ml;
+      e.tk_slots = slots;
+      e.tk_k = k_eff;
+      e.tk_tiles = vtiles;
+    }
     if (fuse_norm) {
       // the final RMSNorm folded in: all M rows of the stream in (the anchors
-      // share the token tile), the MASK rows' logits out
-      GemmEpi e = epi_base(EPI_F32, M, c.vocab, logits, c.vocab, ws.status);
+      // share the token tile), the MASK rows out
       e.out_gather = gamma;
-      rc = draft_gemm(h, A, single_map(h->w.s_lm_head), nt, ws.h, M, d, e, scratch, s,
-                      wb * c.vocab * d + 2.0 * M * d + 4.0 * R * c.vocab + ssq_bytes, &rsc);
+      rc = draft_gemm(h, A, single_map(h->w.s_lm_head), vtiles, ws.h, M, d, e, scratch, s,
+                      wb * c.vocab * d + 2.0 * M * d + logit_bytes + ssq_bytes, &rsc);
     } else {
-      GemmEpi e = epi_base(EPI_F32, R, c.vocab, logits, c.vocab, ws.status);
-      rc = draft_gemm(h, A, single_map(h->w.s_lm_head), nt, ws.hf, R, d, e, scratch, s,
-                      wb * c.vocab * d + 2.0 * R * d + 4.0 * R * c.vocab);
+      rc = draft_gemm(h, A, single_map(h->w.s_lm_head), vtiles, ws.hf, R, d, e, scratch, s,
+                      wb * c.vocab * d + 2.0 * R * d + logit_bytes);
     }
     if (rc) return rc;
   }
-  const int k_eff = topk > 0 ? topk : 1;
   slot = prof_begin(h, s);
-  rc = launch_topk_lse(logits, R, c.vocab, k_eff, ws.topk_keys, ws.topk_ml, ws.topk_counters,
-                       topk > 0 ? out->topk_ids : nullptr, topk > 0 ? out->topk_vals : nullptr,
-                       out->lse, sampling ? nullptr : out->draft, s);
+  int32_t* ids_out = topk > 0 ? out->topk_ids : nullptr;
+  float* vals_out = topk > 0 ? out->topk_vals : nullptr;
+  int32_t* draft_out = sampling ? nullptr : out->draft;
+  if (fused_topk)
+    rc = launch_topk_merge(R, vtiles, slots, k_eff, ws.tk_keys, ws.tk_ml, ids_out, vals_out, out->lse,
+                           draft_out, s);
+  else
+    rc = launch_topk_lse(logits, R, c.vocab, k_eff, ws.topk_keys, ws.topk_ml, ws.topk_counters, ids_out,
+                         vals_out, out->lse, draft_out, s);
   if (rc) return rc;
-  prof_end(h, s, slot, 4.0 * R * c.vocab, DFLASH_KIND_TOPK);
+  prof_end(h, s, slot, fused_topk ? part_bytes : 4.0 * R * c.vocab, DFLASH_KIND_TOPK);
   if (sampling) {
     slot = prof_begin(h, s);
     rc = launch_probs(R, c.vocab, logits, sampling->temperature, sampling->top_p, out->q, s);

@@ -192,6 +192,66 @@ __device__ __forceinline__ T block_exclusive_scan(T v, T* scratch, T* total) {
   return r;
 }
 
+// ------------------------------------------------- top-k keys and (max, sum)
+
+// (value, id) packed so that a larger key is a larger value, ties to the lower id.
+__device__ __forceinline__ unsigned long long vkey(float v, int id) {
+  return ((unsigned long long)ordered_key(v) << 32) | (uint32_t)(~(uint32_t)id);
+}
+
+template <int KT>
+__device__ __forceinline__ void insert_key(unsigned long long (&top)[KT], unsigned long long k) {
+  if (k <= top[KT - 1]) return;
+  top[KT - 1] = k;
+#pragma unroll
+  for (int j = KT - 1; j > 0; --j) {
+    if (top[j] > top[j - 1]) {
+      const unsigned long long t = top[j];
+      top[j] = top[j - 1];
+      top[j - 1] = t;
+    }
+  }
+}
+
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) {
+    m = m2;
+    s = s2;
+    return;
+  }
+  if (m2 > m) {
+    s = s * expf(m - m2) + s2;
+    m = m2;
+  } else {
+    s += s2 * expf(m2 - m);
+  }
+}
+
+// One round of a warp-wide tournament over per-lane lists sorted in
+// descending order: the largest head of the warp is returned and its lane
+// drops it.  Keys are distinct (they carry the vocabulary id) or zero (empty).
+template <int KT>
+__device__ __forceinline__ unsigned long long warp_pop_max(unsigned long long (&lst)[KT]) {
+  const unsigned long long best = warp_max_u64(lst[0]);
+  const unsigned ball = __ballot_sync(0xffffffffu, best != 0 && lst[0] == best);
+  if (ball && (int)(threadIdx.x & 31) == __ffs(ball) - 1) {
+#pragma unroll
+    for (int j = 0; j + 1 < KT; ++j) lst[j] = lst[j + 1];
+    lst[KT - 1] = 0;
+  }
+  return best;
+}
+
+// (max, sum of exp(x - max)) merged over the 32 lanes of a warp.
+__device__ __forceinline__ void warp_lse(float& m, float& s) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    lse_merge(m, s, m2, s2);
+  }
+}
+
 // ------------------------------------------------------ PTX: smem / mbarrier
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -343,6 +403,19 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T: A in tensor memory, one row per lane
+// (M = 128 rows on lanes 0-127), two 16-bit K elements per 32-bit column in
+// K order, starting at column a_tmem.
+__device__ __forceinline__ void tc_mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 

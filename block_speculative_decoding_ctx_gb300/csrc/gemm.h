@@ -110,8 +110,18 @@ struct GemmEpi {
   __half* xg;
   const float* xg_g;
   // EPI_F32: with out_gather = G > 0 only the MASK rows are written, token t
-  // to row (t / G) * (G - 1) + t % G - 1 (t % G == 0 skipped)
+  // to row (t / G) * (G - 1) + t % G - 1 (t % G == 0 skipped); out may be
+  // nullptr when only the top-k partials below are wanted
   int out_gather;
+  // EPI_F32 (the LM head): per weight tile and output row, the tile's top
+  // tk_k keys (ordered logit << 32 | ~id, descending, 0 = none) at
+  // tk_keys[(row * tk_tiles + tile) * tk_slots] and the tile's (max, sum of
+  // exp(logit - max)) at tk_ml[row * tk_tiles + tile]; or tk_keys nullptr
+  unsigned long long* tk_keys;
+  float2* tk_ml;
+  int tk_slots;  // 4 or 16
+  int tk_k;
+  int tk_tiles;
   int* status;      // device status word: argument errors found on the device, and fp16
                     // outputs (or ring entries) beyond the fp16 range (DFLASH_ERR_RANGE)
 };

@@ -5,9 +5,11 @@
 // is bound by the bytes of its weights; E4M3 halves them.  The activations
 // stay fp16 (an E4M3 activation would keep 4 significant bits), so the
 // tensor cores still run kind::f16: converter warps widen each weight stage
-// to fp16 in shared memory (every E4M3 value is exactly an fp16 value), the
-// MMAs read it like the fp16 path's weight tiles, and the epilogue multiplies
-// each accumulator row by its weight row's scale.
+// to fp16 into tensor memory (every E4M3 value is exactly an fp16 value; one
+// weight row per TMEM lane), the MMAs take their A operand from there, and
+// the epilogue multiplies each accumulator row by its weight row's scale.
+// Keeping the widened weights out of shared memory leaves it to the E4M3
+// stages in flight from HBM.
 //
 // One CTA = 8 warps per (weight tile, token tile, K split):
 //   warp 0 lane 0   TMA producer: a 128-row x 128-byte E4M3 box (128 K
@@ -17,8 +19,8 @@
 //                   64-deep fp16 slot and commits slots and stages back;
 //   warp 2          with a folded RMSNorm, the rstd of the tile's tokens;
 //   warps 4-7       converters: thread t widens weight row t of each stage,
-//                   16 codes per 16-byte load, into the fp16 slot ring in the
-//                   layout the MMA descriptors expect (128-byte swizzle);
+//                   16 codes per 16-byte load, into a ring of 64-deep fp16
+//                   slots in tensor memory (lane t, 32 columns per slot);
 //   all warps       epilogue in two groups (one_tile_epilogue), with split-K
 //                   reduced by ticket or inside a cluster as in gemm.cu.
 // Every wait is bounded (mbar_wait_bounded).
@@ -31,21 +33,26 @@ namespace {
 
 constexpr int kBK8 = 128;                 // K elements (bytes) of one E4M3 weight row per stage
 constexpr int kA8Bytes = 128 * kBK8;      // E4M3 weight box per stage (16 KiB)
-constexpr int kA16Bytes = 128 * kBK * 2;  // one 64-deep fp16 weight slot (16 KiB)
+constexpr int kSlotCols = kBK / 2;        // TMEM columns of one 64-deep fp16 slot (2 per column)
 
-// Stages and fp16 slots per token-tile width: two CTAs share an SM up to 32
-// tokens.  Measured at batch 1 (full dimensions): two CTAs per SM with three
-// stages and two fp16 slots each stream the pass's E4M3 weights at 2.8 TB/s;
-// one CTA per SM with nine stages and two slots at 1.8 TB/s (the converters
-// wait on the slots' round trip through the tensor cores, and half as many
-// converter warps run per SM).
+// Shape per token-tile width: two CTAs share an SM up to 32 tokens.  The
+// widened fp16 slots live in tensor memory, so shared memory holds only the
+// E4M3 stages in flight (and their token boxes).  Measured at batch 1 (full
+// dimensions) with the slots in shared memory instead: two CTAs per SM with
+// three stages and two slots streamed the pass's E4M3 weights at 2.8 TB/s,
+// one CTA per SM with nine stages and two slots at 1.8 TB/s — the converters
+// waited on the slots' round trip through the tensor cores.
 template <int BN>
 struct F8Shape {
-  static constexpr int S = 3;   // E4M3 stages
-  static constexpr int NC = 2;  // fp16 slots
+  static constexpr bool kTwo = BN <= 32;      // two CTAs per SM
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStage = kA8Bytes + 2 * kBBytes;
-  static constexpr size_t smem = (size_t)S * kStage + (size_t)NC * kA16Bytes + 1024;
+  static constexpr int S = kTwo ? 100 * 1024 / kStage : 192 * 1024 / kStage;  // E4M3 stages
+  static constexpr int NC = 6;                // fp16 slots in tensor memory
+  static constexpr int kAccCols = BN < 32 ? 32 : BN;
+  static constexpr uint32_t kTmemCols = tmem_cols(kAccCols + NC * kSlotCols);
+  static constexpr size_t smem = (size_t)S * kStage + 1024;
+  static_assert(!kTwo || kTmemCols <= 256, "two CTAs per SM share the 512 TMEM columns");
 };
 
 // Dequantization scale of this thread's weight row (row r of tile tile_n),
@@ -80,15 +87,15 @@ __global__ void __launch_bounds__(256, BN <= 32 ? 2 : 1)
   using Sh = F8Shape<BN>;
   constexpr int S = Sh::S, NC = Sh::NC;
   constexpr int kBBytes = Sh::kBBytes, kStage = Sh::kStage;
-  constexpr uint32_t kTmemCols = tmem_cols(BN);
+  constexpr uint32_t kTmemCols = Sh::kTmemCols;
   static_assert(kStage % 1024 == 0, "stage buffers must keep 1024-byte alignment");
-  static_assert((BN + 64) * 128 * 4 <= S * kStage + NC * kA16Bytes,
+  static_assert((BN + 64) * 128 * 4 <= S * kStage,
                 "split partials and exchange buffers must fit the stage buffers");
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[S];
   __shared__ __align__(8) uint64_t empty_bar[S];
-  __shared__ __align__(8) uint64_t cfull_bar[NC];   // fp16 slot converted
+  __shared__ __align__(8) uint64_t cfull_bar[NC];   // fp16 slot written to tensor memory
   __shared__ __align__(8) uint64_t cempty_bar[NC];  // fp16 slot consumed by the MMAs
   __shared__ __align__(8) uint64_t acc_bar;
   __shared__ uint32_t tmem_base_sh;
@@ -99,7 +106,6 @@ __global__ void __launch_bounds__(256, BN <= 32 ? 2 : 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile_n = blockIdx.x, tile_m = blockIdx.y, split = blockIdx.z;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* a16 = smem + S * kStage;
 
   const int kb_total = (args.K + kBK8 - 1) / kBK8;
   const int kb0 = (int)((long long)split * kb_total / args.splits);
@@ -130,7 +136,8 @@ __global__ void __launch_bounds__(256, BN <= 32 ? 2 : 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = tmem_base_sh;
+  const uint32_t tmem = tmem_base_sh;           // accumulator at columns 0 .. BN - 1
+  const uint32_t tslot = tmem + Sh::kAccCols;    // fp16 slot c at tslot + c * kSlotCols
   grid_dependents_launch();
 
   int issued = 0;
@@ -194,12 +201,11 @@ __global__ void __launch_bounds__(256, BN <= 32 ? 2 : 1)
           break;
         }
         tc_fence_after();
-        const uint32_t a_addr = smem_u32(a16 + c * kA16Bytes);
+        const uint32_t a_col = tslot + (uint32_t)(c * kSlotCols);
         const uint32_t b_addr = smem_u32(smem + s * kStage + kA8Bytes + h * kBBytes);
 #pragma unroll
         for (int k = 0; k < kBK / 16; ++k)
-          tc_mma_f16(tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), idesc,
-                     (i | h | k) ? 1u : 0u);
+          tc_mma_f16_ta(tmem, a_col + k * 8, smem_desc_sw128(b_addr + k * 32), idesc, (i | h | k) ? 1u : 0u);
         tc_commit(&cempty_bar[c]);
       }
       if (!ok) break;
@@ -208,12 +214,14 @@ __global__ void __launch_bounds__(256, BN <= 32 ? 2 : 1)
     tc_commit(&acc_bar);
   } else if (warp >= 4) {
     // ---------------------------------------------------------- converters
-    // thread t owns weight row t: its E4M3 row (128 bytes, 16-byte chunk j
-    // stored at chunk j ^ (t % 8) of the row) becomes two fp16 rows of 64
-    // (16-byte chunk j at j ^ (t % 8)), the layout TMA would have produced
+    // thread t owns weight row t (TMEM lane t: warp w reaches lanes
+    // 32 (w % 4) .. + 31): its E4M3 row (128 bytes, 16-byte chunk j stored at
+    // chunk j ^ (t % 8) of the row) becomes, per 64-deep half, 32 columns of
+    // fp16 pairs in K order
     const int t = threadIdx.x - 128;
     const uint32_t sw = (uint32_t)(t & 7);
     const uint32_t row_off = (uint32_t)(t >> 3) * 1024u + sw * 128u;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     for (int i = 0; i < nkb; ++i) {
       const int s = i % S;
       if (!mbar_wait_bounded(&full_bar[s], (uint32_t)(i / S) & 1u, &abort_sh, args.status)) break;
@@ -225,18 +233,28 @@ __global__ void __launch_bounds__(256, BN <= 32 ? 2 : 1)
           ok = false;
           break;
         }
-        uint8_t* dst = a16 + c * kA16Bytes + row_off;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t j = (uint32_t)(h * 4 + q);  // 16-code chunk of the E4M3 row
-          const uint4 raw = *reinterpret_cast<const uint4*>(a8 + ((j ^ sw) << 4));
-          uint4 lo, hi;
-          widen16(raw, lo, hi);
-          *reinterpret_cast<uint4*>(dst + (((2u * q) ^ sw) << 4)) = lo;
-          *reinterpret_cast<uint4*>(dst + (((2u * q + 1u) ^ sw) << 4)) = hi;
-        }
-        // generic-proxy writes must be visible to the tensor cores' reads
-        fence_proxy_async_smem();
+        tc_fence_after();
+        // the half's four 16-code chunks, loaded together, widened into two
+        // 16-column stores (register arrays indexed by constants only)
+        const uint32_t j0 = (uint32_t)(h * 4);
+        const uint4 r0 = *reinterpret_cast<const uint4*>(a8 + (((j0 + 0u) ^ sw) << 4));
+        const uint4 r1 = *reinterpret_cast<const uint4*>(a8 + (((j0 + 1u) ^ sw) << 4));
+        const uint4 r2 = *reinterpret_cast<const uint4*>(a8 + (((j0 + 2u) ^ sw) << 4));
+        const uint4 r3 = *reinterpret_cast<const uint4*>(a8 + (((j0 + 3u) ^ sw) << 4));
+        uint4 l0, h0, l1, h1, l2, h2, l3, h3;
+        widen16(r0, l0, h0);
+        widen16(r1, l1, h1);
+        widen16(r2, l2, h2);
+        widen16(r3, l3, h3);
+        const uint32_t w0[16] = {l0.x, l0.y, l0.z, l0.w, h0.x, h0.y, h0.z, h0.w,
+                                 l1.x, l1.y, l1.z, l1.w, h1.x, h1.y, h1.z, h1.w};
+        const uint32_t w1[16] = {l2.x, l2.y, l2.z, l2.w, h2.x, h2.y, h2.z, h2.w,
+                                 l3.x, l3.y, l3.z, l3.w, h3.x, h3.y, h3.z, h3.w};
+        const uint32_t dst = tslot + lane_base + (uint32_t)(c * kSlotCols);
+        tmem_st_x16(dst, w0);
+        tmem_st_x16(dst + 16, w1);
+        tc_wait_st();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&cfull_bar[c]);
       }

@@ -48,6 +48,65 @@ __device__ __forceinline__ void epi_sync(int bar) {
     asm volatile("bar.sync 2, 128;" ::: "memory");
 }
 
+// Output row of token tok for EPI_F32 (the MASK rows with out_gather), or -1.
+__device__ __forceinline__ int f32_out_row(const GemmEpi& e, int tok) {
+  if (e.out_gather <= 0) return tok;
+  const int G = e.out_gather, jj = tok % G;
+  return jj ? (tok / G) * (G - 1) + jj - 1 : -1;
+}
+
+// Top-k partial of one 16-token chunk of an LM-head tile (xchg = the chunk's
+// logits as [16 tokens][128 rows], rows beyond the vocabulary at -inf).  The
+// eight threads r = 8 jt .. 8 jt + 7 of the group serve token jt: each keeps
+// a sorted top-KT of 16 rows and their (max, sum of exp), the eight merge by
+// shuffles, and the first writes the tile's partial for the token's row.
+template <int KT>
+__device__ __forceinline__ void tile_topk_partial(const GemmEpi& e, const float* xchg, int tok_base,
+                                                  int tok_step, int ntok, int tile_n, int r) {
+  const int jt = r >> 3, part = r & 7;
+  unsigned long long top[KT];
+#pragma unroll
+  for (int j = 0; j < KT; ++j) top[j] = 0;
+  float m = -INFINITY, s = 0.0f;
+  const float* row = xchg + jt * 128 + part * 16;
+  float x[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    x[i] = row[i];
+    m = fmaxf(m, x[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    if (x[i] != -INFINITY) {
+      s += expf(x[i] - m);
+      insert_key<KT>(top, vkey(x[i], tile_n * 128 + part * 16 + i));
+    }
+  }
+  // merge the eight lists of the token (lanes differing in bits 0-2)
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) {
+    unsigned long long other[KT];
+#pragma unroll
+    for (int j = 0; j < KT; ++j) other[j] = __shfl_xor_sync(0xffffffffu, top[j], o);
+#pragma unroll
+    for (int j = 0; j < KT; ++j) insert_key<KT>(top, other[j]);
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    lse_merge(m, s, m2, s2);
+  }
+  const int tok = tok_base + jt * tok_step;
+  if (part == 0 && jt < ntok && tok < e.M) {
+    const int orow = f32_out_row(e, tok);
+    if (orow >= 0) {
+      const size_t slot = (size_t)orow * e.tk_tiles + tile_n;
+      unsigned long long* dst = e.tk_keys + slot * e.tk_slots;
+#pragma unroll
+      for (int j = 0; j < KT; ++j)
+        if (j < e.tk_k) dst[j] = top[j];
+      e.tk_ml[slot] = make_float2(m, s);
+    }
+  }
+}
+
 __device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const float (&v_in)[16],
                                int tok_base, int tok_step, int ntok, int tile_n, int r,
                                float* xchg, int bar, const float* rs = nullptr,
@@ -62,11 +121,19 @@ __device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] *= wscale;
   }
-  const bool needs_xchg = (kind == EPI_QKV || kind == EPI_SWIGLU || kind == EPI_KV_RING);
+  const bool topk = kind == EPI_F32 && e.tk_keys != nullptr;
+  const bool needs_xchg = (kind == EPI_QKV || kind == EPI_SWIGLU || kind == EPI_KV_RING || topk);
   if (needs_xchg) {
+    const bool live = !topk || tile_n * 128 + r < e.N;   // top-k: rows past the vocabulary lose
 #pragma unroll
-    for (int j = 0; j < 16; ++j) xchg[j * 128 + r] = v[j];
+    for (int j = 0; j < 16; ++j) xchg[j * 128 + r] = live ? v[j] : -INFINITY;
     epi_sync(bar);
+  }
+  if (topk) {
+    if (e.tk_slots == 16)
+      tile_topk_partial<16>(e, xchg, tok_base, tok_step, ntok, tile_n, r);
+    else
+      tile_topk_partial<4>(e, xchg, tok_base, tok_step, ntok, tile_n, r);
   }
   // Every kind loads what it needs for its 16 tokens into registers first and
   // stores afterwards: loads placed after stores that might alias them would
@@ -110,12 +177,8 @@ __device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int tok = tok_base + j * tok_step;
-          if (j < ntok && tok < e.M) {
-            int row = tok;
-            if (e.out_gather > 0) {  // MASK rows only
-              const int G = e.out_gather, jj = tok % G;
-              row = jj ? (tok / G) * (G - 1) + jj - 1 : -1;
-            }
+          if (j < ntok && tok < e.M && e.out) {
+            const int row = f32_out_row(e, tok);  // MASK rows only with out_gather
             if (row >= 0) {
               const size_t o = (size_t)row * e.ld + n;
               if (kind == EPI_F32)

@@ -52,9 +52,12 @@ __global__ void __launch_bounds__(kPThreads)
   __shared__ float redf[33];
   __shared__ unsigned long long redu[33];
   __shared__ float s_max, s_sum;                  // this CTA's partials, read by the cluster
-  __shared__ unsigned long long s_z, s_tie;
+  __shared__ unsigned long long s_z, s_tie, s_before;
   __shared__ unsigned long long hist[2][256];
   __shared__ unsigned histc[2][256];
+  __shared__ unsigned long long tot_m[256];     // the cluster's histogram, summed here
+  __shared__ unsigned tot_c[256];
+  __shared__ float s_part[kPC];                 // the CTAs' partials, gathered here
   __shared__ unsigned long long s_above, s_thr, s_ntie;
   __shared__ uint32_t s_prefix, s_mask;
 
@@ -82,8 +85,10 @@ __global__ void __launch_bounds__(kPThreads)
     if (tid == 0) s_max = t;
   }
   cl.sync();
+  if (tid < kPC) s_part[tid] = *cl.map_shared_rank(&s_max, tid);
+  __syncthreads();
   float M = -INFINITY;
-  for (int k = 0; k < kPC; ++k) M = fmaxf(M, *cl.map_shared_rank(&s_max, k));
+  for (int k = 0; k < kPC; ++k) M = fmaxf(M, s_part[k]);
 
   // ---- e = exp(l / T - M) (one fused rounding inside), S in rank order
   float s = 0.0f;
@@ -95,8 +100,10 @@ __global__ void __launch_bounds__(kPThreads)
   s = block_sum(s, redf);
   if (tid == 0) s_sum = s;
   cl.sync();
+  if (tid < kPC) s_part[tid] = *cl.map_shared_rank(&s_sum, tid);
+  __syncthreads();
   float S = 0.0f;
-  for (int k = 0; k < kPC; ++k) S += *cl.map_shared_rank(&s_sum, k);
+  for (int k = 0; k < kPC; ++k) S += s_part[k];
 
   // ---- p = e / S
   unsigned long long z = 0;
@@ -146,23 +153,30 @@ __global__ void __launch_bounds__(kPThreads)
       hist_add(hist[buf], histc[buf], i < n && (key & mask) == prefix, (key >> shift) & 255u, to_fixed45(p));
     }
     cl.sync();
+    if (tid < 256) {
+      // bin tid summed over the cluster (in rank order)
+      unsigned long long a = 0;
+      unsigned c = 0;
+#pragma unroll
+      for (int k = 0; k < kPC; ++k) {
+        a += cl.map_shared_rank(&hist[buf][0], k)[tid];
+        c += cl.map_shared_rank(&histc[buf][0], k)[tid];
+      }
+      tot_m[tid] = a;
+      tot_c[tid] = c;
+    }
+    __syncthreads();
     if (tid < 32) {
-      // lane l holds digits 255 - 8l - j, j = 0..7 (descending): sum the
-      // cluster's bins, then find the digit where the running mass from the
-      // top reaches thr
+      // lane l holds digits 255 - 8l - j, j = 0..7 (descending); find the
+      // digit where the running mass from the top reaches thr
       unsigned long long mass[8], tot = 0;
       unsigned cnt[8];
+#pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int d = 255 - 8 * tid - j;
-        unsigned long long a = 0;
-        unsigned c = 0;
-        for (int k = 0; k < kPC; ++k) {
-          a += cl.map_shared_rank(&hist[buf][0], k)[d];
-          c += cl.map_shared_rank(&histc[buf][0], k)[d];
-        }
-        mass[j] = a;
-        cnt[j] = c;
-        tot += a;
+        mass[j] = tot_m[d];
+        cnt[j] = tot_c[d];
+        tot += mass[j];
       }
       unsigned long long incl = tot;  // inclusive scan over lanes (lane 0 = top digits)
       for (int o = 1; o < 32; o <<= 1) {
@@ -220,7 +234,13 @@ __global__ void __launch_bounds__(kPThreads)
   unsigned long long rk = block_exclusive_scan(nt, redu, &tot);
   if (tid == 0) s_tie = tot;
   cl.sync();
-  for (int k = 0; k < rank; ++k) rk += *cl.map_shared_rank(&s_tie, k);
+  if (tid == 0) {
+    unsigned long long b0 = 0;
+    for (int k = 0; k < rank; ++k) b0 += *cl.map_shared_rank(&s_tie, k);
+    s_before = b0;
+  }
+  __syncthreads();
+  rk += s_before;
   for (int i = s0; i < s1; ++i) {
     const float p = vals[i];
     const uint32_t key = __float_as_uint(p);

@@ -142,64 +142,6 @@ __global__ void __launch_bounds__(256)
 
 constexpr int kTopkThreads = 256;
 
-// (value, id) packed so that a larger key is a larger value, ties to the lower id.
-__device__ __forceinline__ unsigned long long vkey(float v, int id) {
-  return ((unsigned long long)ordered_key(v) << 32) | (uint32_t)(~(uint32_t)id);
-}
-
-template <int KT>
-__device__ __forceinline__ void insert_key(unsigned long long (&top)[KT], unsigned long long k) {
-  if (k <= top[KT - 1]) return;
-  top[KT - 1] = k;
-#pragma unroll
-  for (int j = KT - 1; j > 0; --j) {
-    if (top[j] > top[j - 1]) {
-      const unsigned long long t = top[j];
-      top[j] = top[j - 1];
-      top[j - 1] = t;
-    }
-  }
-}
-
-__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
-  if (m2 == -INFINITY) return;
-  if (m == -INFINITY) {
-    m = m2;
-    s = s2;
-    return;
-  }
-  if (m2 > m) {
-    s = s * expf(m - m2) + s2;
-    m = m2;
-  } else {
-    s += s2 * expf(m2 - m);
-  }
-}
-
-// One round of a warp-wide tournament over per-lane lists sorted in
-// descending order: the largest head of the warp is returned and its lane
-// drops it.  Keys are distinct (they carry the vocabulary id) or zero (empty).
-template <int KT>
-__device__ __forceinline__ unsigned long long warp_pop_max(unsigned long long (&lst)[KT]) {
-  const unsigned long long best = warp_max_u64(lst[0]);
-  const unsigned ball = __ballot_sync(0xffffffffu, best != 0 && lst[0] == best);
-  if (ball && (int)(threadIdx.x & 31) == __ffs(ball) - 1) {
-#pragma unroll
-    for (int j = 0; j + 1 < KT; ++j) lst[j] = lst[j + 1];
-    lst[KT - 1] = 0;
-  }
-  return best;
-}
-
-// (max, sum of exp(x - max)) merged over the 32 lanes of a warp.
-__device__ __forceinline__ void warp_lse(float& m, float& s) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    lse_merge(m, s, m2, s2);
-  }
-}
-
 // Per-row top-k and log-sum-exp.  CTA (c, r) covers chunk c of row r: every
 // thread keeps a sorted top-KT of its 32 values and a running (max, sum);
 // warp tournaments reduce the lists to the CTA's top-k; the last CTA of the
@@ -310,6 +252,70 @@ __global__ void __launch_bounds__(kTopkThreads)
   }
 }
 
+// Row r's top-k and log-sum-exp from the LM head's per-tile partials (the
+// GEMM epilogue's top keys of each 128-row vocabulary tile, descending, and
+// the tile's (max, sum of exp)).  Every thread merges the tiles t = tid, tid +
+// 256, ... into a sorted top-KT and a running (max, sum); warp tournaments
+// reduce those to the CTA's, and warp 0 merges the warps' lists.
+template <int KT>
+__global__ void __launch_bounds__(kTopkThreads)
+    topk_merge_kernel(const unsigned long long* __restrict__ keys, const float2* __restrict__ ml, int tiles,
+                      int slots, int k, int32_t* __restrict__ ids, float* __restrict__ vals,
+                      float* __restrict__ lse, int32_t* __restrict__ draft) {
+  pdl_enter();
+  constexpr int kWarps = kTopkThreads / 32;
+  __shared__ unsigned long long wsel[kWarps][KT];
+  __shared__ float redm[kWarps], reds[kWarps];
+  const int r = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned long long top[KT];
+#pragma unroll
+  for (int j = 0; j < KT; ++j) top[j] = 0;
+  float m = -INFINITY, s = 0.0f;
+  for (int t = threadIdx.x; t < tiles; t += kTopkThreads) {
+    const unsigned long long* kp = keys + ((size_t)r * tiles + t) * slots;
+    for (int j = 0; j < k; ++j) {
+      const unsigned long long key = __ldcg(kp + j);
+      if (key <= top[KT - 1]) break;  // the tile's keys are descending
+      insert_key<KT>(top, key);
+    }
+    const float2 p = __ldcg(ml + (size_t)r * tiles + t);
+    lse_merge(m, s, p.x, p.y);
+  }
+  warp_lse(m, s);
+#pragma unroll
+  for (int j = 0; j < KT; ++j) {
+    if (j < k) {
+      const unsigned long long b = warp_pop_max(top);
+      if (lane == 0) wsel[warp][j] = b;
+    }
+  }
+  if (lane == 0) {
+    redm[warp] = m;
+    reds[warp] = s;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  unsigned long long lst[KT];
+#pragma unroll
+  for (int j = 0; j < KT; ++j) lst[j] = (lane < kWarps && j < k) ? wsel[lane][j] : 0ull;
+  float M = lane < kWarps ? redm[lane] : -INFINITY;
+  float S = lane < kWarps ? reds[lane] : 0.0f;
+  warp_lse(M, S);
+#pragma unroll
+  for (int j = 0; j < KT; ++j) {
+    if (j < k) {
+      const unsigned long long key = warp_pop_max(lst);
+      if (lane == 0) {
+        if (ids) ids[(size_t)r * k + j] = (int32_t)(~(uint32_t)(key & 0xFFFFFFFFull));
+        if (vals) vals[(size_t)r * k + j] = key_to_float((uint32_t)(key >> 32));
+        if (draft && j == 0) draft[r] = (int32_t)(~(uint32_t)(key & 0xFFFFFFFFull));
+      }
+    }
+  }
+  if (lane == 0 && lse) lse[r] = M + logf(S);
+}
+
 __global__ void add_lengths_kernel(int B, const int32_t* __restrict__ n_new, int64_t* ctx_len) {
   pdl_enter();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
@@ -367,6 +373,15 @@ int launch_topk_lse(const float* logits, int rows, int V, int k, unsigned long l
                       part_keys, part_ml, counters, ids, vals, lse, draft);
   return launch_pdl(topk_lse_kernel<16>, grid, dim3(kTopkThreads), 0, s, logits, V, k, chunks,
                     part_keys, part_ml, counters, ids, vals, lse, draft);
+}
+
+int launch_topk_merge(int rows, int tiles, int slots, int k, const unsigned long long* keys, const float2* ml,
+                      int32_t* ids, float* vals, float* lse, int32_t* draft, cudaStream_t s) {
+  if (slots == 4)
+    return launch_pdl(topk_merge_kernel<4>, dim3(rows), dim3(kTopkThreads), 0, s, keys, ml, tiles, slots, k, ids,
+                      vals, lse, draft);
+  return launch_pdl(topk_merge_kernel<16>, dim3(rows), dim3(kTopkThreads), 0, s, keys, ml, tiles, slots, k, ids,
+                    vals, lse, draft);
 }
 
 int launch_add_lengths(int B, const int32_t* n_new, int64_t* ctx_len, cudaStream_t s) {

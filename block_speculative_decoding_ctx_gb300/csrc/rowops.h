@@ -28,11 +28,16 @@ int launch_rmsnorm_rope(float* x, int rows, int d, const float* g, float eps, in
 // dst (fp16) = src (bf16), n elements (a multiple of 8, 16-byte aligned
 // pointers); *flag = 1 if a value is NaN or beyond the fp16 range.
 int launch_to_f16(const void* src, void* dst, size_t n, int* flag, int grid, cudaStream_t s);
-// Slots per row and chunk of the top-k partials (4 or 16).
+// Slots per row and tile of the top-k partials (4 or 16).
 int topk_slots(int k);
 int launch_topk_lse(const float* logits, int rows, int V, int k, unsigned long long* part_keys,
                     float* part_ml, int* counters, int32_t* ids, float* vals, float* lse,
                     int32_t* draft, cudaStream_t s);
+// Row r's top-k (ids, values; descending, ties to the lower id), log-sum-exp
+// and top-1 draft from the LM head's per-tile partials (GemmEpi::tk_*):
+// keys [rows][tiles][slots], ml [rows][tiles].  Any output may be nullptr.
+int launch_topk_merge(int rows, int tiles, int slots, int k, const unsigned long long* keys, const float2* ml,
+                      int32_t* ids, float* vals, float* lse, int32_t* draft, cudaStream_t s);
 int launch_add_lengths(int B, const int32_t* n_new, int64_t* ctx_len, cudaStream_t s);
 // quant.cu: E4M3 codes and per-row scales from bf16 weights [rows, cols]
 // (cols even), and the check of given codes (n bytes, a multiple of 16) and

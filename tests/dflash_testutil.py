@@ -49,7 +49,7 @@ def check_topk(ids, vals, logits_ref, tol):
         assert (np.diff(vals[r]) <= 0).all()
 
 
-def run_draft(h, anchor, ctx_len, rk, rv, gamma, topk, sampling=None, req_slot=None):
+def run_draft(h, anchor, ctx_len, rk, rv, gamma, topk, sampling=None, req_slot=None, with_logits=True):
     dev = torch.device("cuda")
     B = anchor.shape[0]
     V = h.cfg["vocab"]
@@ -58,7 +58,7 @@ def run_draft(h, anchor, ctx_len, rk, rv, gamma, topk, sampling=None, req_slot=N
                if topk else None,
                topk_vals=torch.full((B, gamma - 1, max(topk, 1)), -7.0, device=dev) if topk else None,
                lse=torch.full((B, gamma - 1), -7.0, device=dev),
-               logits=torch.full((B, gamma - 1, V), -7.0, device=dev),
+               logits=torch.full((B, gamma - 1, V), -7.0, device=dev) if with_logits else None,
                q=torch.full((B, gamma - 1, V), -7.0, device=dev) if sampling else None,
                draft=torch.full((B, gamma - 1), -7, dtype=torch.int32, device=dev))
     ws = dfl.workspace(dfl.dflash_draft_workspace_bytes(h))

@@ -306,10 +306,11 @@ def test_activation_beyond_fp16_range_is_reported():
 @pytest.mark.parametrize("gamma", [4, 16])
 def test_ring_key_beyond_fp16_range_is_reported(gamma):
     """Attention reads ring keys as fp16: a bf16 key beyond +-65504 written
-    into the ring by the caller is reported (DFLASH_ERR_RANGE), on the path
-    that widens keys in each consumer's registers (gamma 4: two row tiles) and
-    on the one where a converter warp widens them in shared memory (gamma 16:
-    five row tiles)."""
+    into the ring by the caller is not saturated silently — it becomes
+    infinite and the pass reports DFLASH_ERR_RANGE at its next fp16 store —
+    on the path that widens keys in each consumer's registers (gamma 4: two
+    row tiles) and on the one where a converter warp widens them in shared
+    memory (gamma 16: five row tiles)."""
     dims = synth.DIMS["small"]
     W = synth.weights(dims, 98)
     h = dfl.dflash_create(tu.lib_cfg(dims, batch_max=1, gamma_max=16), tu.to_dev(W))

@@ -65,6 +65,49 @@ def test_draft_block_matches_oracle(name, B, gamma, lens):
     np.testing.assert_array_equal(got["draft"], got["topk_ids"][..., 0])
 
 
+def test_draft_block_long_window_at_small_batch_matches_oracle():
+    """A long window at small batch: every KV head's keys split over a full
+    cluster of CTAs merged through distributed shared memory.  Contexts 2000,
+    700, 100 and 0 leave some splits without keys."""
+    dims = dict(synth.DIMS["small"], window=2048)
+    B, gamma = 4, 8
+    W = synth.weights(dims, 18, random_gains=True)
+    rk, rv = synth.ring(dims, B, 19)
+    anchor = synth.token_ids(B, dims["vocab"], 20)
+    L = torch.tensor([2000, 700, 100, 0], dtype=torch.int64)
+    ref = om.draft_pass(tu.oracle_cfg(dims), W, rk, rv, L.numpy(), anchor.numpy(), gamma)
+    h = dfl.dflash_create(tu.lib_cfg(dims, batch_max=B, gamma_max=gamma), tu.to_dev(W))
+    dev = torch.device("cuda")
+    ws = dfl.workspace(dfl.dflash_draft_workspace_bytes(h))
+    for _ in range(2):                    # one workspace, reused
+        logits = torch.full((B, gamma - 1, dims["vocab"]), -7.0, device=dev)
+        dfl.dflash_draft_block(h, anchor.to(dev), L.to(dev), rk.cuda(), rv.cuda(), gamma, ws,
+                               out=dict(logits=logits))
+        torch.cuda.synchronize()
+        assert dfl.dflash_read_status(ws) == 0
+        assert tu.rel_err(logits.cpu().numpy(), ref["logits"]) <= TOL
+
+
+@pytest.mark.parametrize("name,B,gamma,lens,k", [("small", 3, 8, [300, 17, 0], 4),
+                                                  ("wide", 32, 8, [300] * 31 + [40], 4),
+                                                  ("small128", 2, 16, [512, 3], 16)])
+def test_topk_without_logits_matches_oracle(name, B, gamma, lens, k):
+    """No logits requested: top-k, log-sum-exp and the top-1 draft come from
+    the LM head's per-tile partials alone (the fp32 logits are never written)."""
+    dims = synth.DIMS[name]
+    W = synth.weights(dims, 15, random_gains=True)
+    rk, rv = synth.ring(dims, B, 16)
+    anchor = synth.token_ids(B, dims["vocab"], 17)
+    L = torch.tensor(lens, dtype=torch.int64)
+    ref = om.draft_pass(tu.oracle_cfg(dims), W, rk, rv, L.numpy(), anchor.numpy(), gamma)
+    h = dfl.dflash_create(tu.lib_cfg(dims, batch_max=B, gamma_max=max(gamma, 8), topk_max=k), tu.to_dev(W))
+    got = tu.run_draft(h, anchor, L, rk.cuda(), rv.cuda(), gamma, topk=k, with_logits=False)
+    flat = ref["logits"].reshape(-1, ref["logits"].shape[-1])
+    tu.check_topk(got["topk_ids"].reshape(-1, k), got["topk_vals"].reshape(-1, k), flat, TOL)
+    assert np.abs(got["lse"].reshape(-1) - om.logsumexp(flat)).max() <= TOL * np.abs(flat).max()
+    np.testing.assert_array_equal(got["draft"], got["topk_ids"][..., 0])
+
+
 def test_draft_block_with_request_slots_and_topk16():
     dims = synth.DIMS["small"]
     B, gamma = 2, 8
