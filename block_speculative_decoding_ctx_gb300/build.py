@@ -48,7 +48,9 @@ def build(verbose=False, extra_flags=()):
     compile flags, e.g. -D defaults of the launch heuristics."""
     extra_flags = tuple(extra_flags) + tuple(os.environ.get("DFLASH_NVCC_FLAGS", "").split())
     os.makedirs(BUILD, exist_ok=True)
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    # the GEMM instantiation units take longest: start them first
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")),
+                  key=lambda p: (not os.path.basename(p).startswith("gemm_tiles"), -os.path.getsize(p), p))
     hdr_mtime = max([os.path.getmtime(h) for h in _headers()] + [0.0])
     cc = nvcc()
     jobs = []

@@ -180,10 +180,15 @@ int launch_gemm(const GemmAMaps& A, const GemmAOpts& ao, int n_tiles, const void
     if (rc) return rc;
     return launch_tile_pair(BN, A, tmBh, ao, args, epi, n_tiles, m_tiles, scratch.num_sms, s, pdl);
   }
-  if (BN >= 176)
-    return launch_tile_hi(BN, persistent, A, tmB, ao, args, epi, grid, n_tiles, m_tiles, scratch.num_sms, s, pdl);
-  if (BN >= 80)
-    return launch_tile_lo(BN, persistent, A, tmB, ao, args, epi, grid, n_tiles, m_tiles, scratch.num_sms, s, pdl);
+  if (BN >= 80) {
+    auto unit = BN >= 240   ? launch_tile_240
+                : BN >= 208 ? launch_tile_208
+                : BN >= 176 ? launch_tile_176
+                : BN >= 144 ? launch_tile_144
+                : BN >= 112 ? launch_tile_112
+                            : launch_tile_080;
+    return unit(BN, persistent, A, tmB, ao, args, epi, grid, n_tiles, m_tiles, scratch.num_sms, s, pdl);
+  }
   switch (BN) {
 #define DFL_ONE(bn, st) \
   case bn: return launch_one<bn, st>(A, tmB, ao, args, epi, grid, s, pdl);

@@ -1120,19 +1120,23 @@ int launch_pair(const GemmAMaps& A, const CUtensorMap& tmB, const GemmAOpts& ao,
 // Launch of one token-tile width: the non-persistent kernel on `grid`, or the
 // persistent one; defined by the translation unit that instantiates it.
 #define DFL_TILE_CASES_ONE(X) X(16, 6) X(32, 5) X(64, 4)
-#define DFL_TILE_CASES_LO(X) X(80, 6) X(96, 6) X(112, 6) X(128, 6) X(144, 5) X(160, 5)
-#define DFL_TILE_CASES_HI(X) X(176, 5) X(192, 4) X(208, 4) X(224, 4) X(240, 4) X(256, 4)
 // pair kernel: stages of 16 KiB + BN * 64 bytes within about 192 KiB
 #define DFL_PAIR_CASES(X)                                                                    \
   X(80, 8) X(96, 8) X(112, 8) X(128, 8) X(144, 7) X(160, 7) X(176, 7) X(192, 6) X(208, 6) \
   X(224, 6) X(240, 6) X(256, 6)
 
-int launch_tile_lo(int BN, bool persistent, const GemmAMaps& A, const CUtensorMap& tmB,
-                   const GemmAOpts& ao, const GemmArgs& args, const GemmEpi& epi, dim3 grid,
-                   int n_tiles, int m_tiles, int num_sms, cudaStream_t s, bool pdl);
-int launch_tile_hi(int BN, bool persistent, const GemmAMaps& A, const CUtensorMap& tmB,
-                   const GemmAOpts& ao, const GemmArgs& args, const GemmEpi& epi, dim3 grid,
-                   int n_tiles, int m_tiles, int num_sms, cudaStream_t s, bool pdl);
+// Token tiles of 80 to 256 (two widths per translation unit, gemm_tiles_*.cu).
+#define DFL_TILE_UNIT_DECL(name)                                                                 \
+  int name(int BN, bool persistent, const GemmAMaps& A, const CUtensorMap& tmB, const GemmAOpts& ao, \
+           const GemmArgs& args, const GemmEpi& epi, dim3 grid, int n_tiles, int m_tiles, int num_sms, \
+           cudaStream_t s, bool pdl);
+DFL_TILE_UNIT_DECL(launch_tile_080)
+DFL_TILE_UNIT_DECL(launch_tile_112)
+DFL_TILE_UNIT_DECL(launch_tile_144)
+DFL_TILE_UNIT_DECL(launch_tile_176)
+DFL_TILE_UNIT_DECL(launch_tile_208)
+DFL_TILE_UNIT_DECL(launch_tile_240)
+#undef DFL_TILE_UNIT_DECL
 // The pair kernel of one token-tile width; tmB_half describes boxes of BN / 2
 // token rows.
 int launch_tile_pair(int BN, const GemmAMaps& A, const CUtensorMap& tmB_half, const GemmAOpts& ao,
