@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(256, BN <= 32 ? 2 : 1)
   }
   __syncthreads();
   const float wscale = weight_row_scale(ao, epi, tile_n, (warp & 3) * 32 + lane);
-  one_tile_epilogue<BN, 2>(smem, tmem, abort_sh != 0 || !acc_ok, ao, args, epi, tile_n, tile_m, split,
+  one_tile_epilogue<BN, 2>(smem, S * kStage, tmem, abort_sh != 0 || !acc_ok, ao, args, epi, tile_n, tile_m, split,
                            (BN <= 32 && args.rs_ssq) ? rs_sh : nullptr, &last_sh, wscale);
   tc_fence_before();
   __syncthreads();

@@ -110,7 +110,9 @@ __device__ __forceinline__ void tile_topk_partial(const GemmEpi& e, const float*
 __device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts& ao, const float (&v_in)[16],
                                int tok_base, int tok_step, int ntok, int tile_n, int r,
                                float* xchg, int bar, const float* rs = nullptr,
-                               float wscale = 1.0f) {
+                               float wscale = 1.0f, const float* resid_pre = nullptr) {
+  // resid_pre (EPI_RESID): the residual stream's values of the chunk already
+  // in shared memory, [16 tokens][128 rows] of the tile, or nullptr
   const int kind = e.kind;
   // row scale of a folded RMSNorm: rs[j * tok_step] is token j's rstd; the
   // weight row's dequantization scale (E4M3 weights) multiplies every token
@@ -158,7 +160,9 @@ __device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int tok = tok_base + j * tok_step;
-          nw[j] = (j < ntok && tok < e.M) ? __ldcg(out + (size_t)tok * e.ld + n) + v[j] : 0.0f;
+          nw[j] = (j < ntok && tok < e.M)
+                      ? (resid_pre ? resid_pre[j * 128 + r] : __ldcg(out + (size_t)tok * e.ld + n)) + v[j]
+                      : 0.0f;
         }
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -316,9 +320,10 @@ __device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const GemmAOpts
 // memory and a ticket, or inside the thread-block cluster the splits form.
 // The stage buffers at `smem` are free by now and serve as scratch.  rs_tile:
 // the folded RMSNorm's rstd per local token, or nullptr; wscale: this thread's
-// weight-row dequantization scale (1 for fp16 weights).
+// weight-row dequantization scale (1 for fp16 weights).  free_bytes: the
+// size of the free buffers at `smem`.
 template <int BN, int kGroups>
-__device__ __forceinline__ void one_tile_epilogue(uint8_t* smem, uint32_t tmem, bool aborted,
+__device__ __forceinline__ void one_tile_epilogue(uint8_t* smem, int free_bytes, uint32_t tmem, bool aborted,
                                                   const GemmAOpts& ao, const GemmArgs& args,
                                                   const GemmEpi& epi, int tile_n, int tile_m, int split,
                                                   const float* rs_tile, int* last_sh, float wscale) {
@@ -352,11 +357,33 @@ __device__ __forceinline__ void one_tile_epilogue(uint8_t* smem, uint32_t tmem, 
   } else if (!args.cluster) {
     // Ticketed reduction: every split stores its fp32 partial [T][128] in
     // global memory; the last split of the tile to arrive (atomic ticket after
-    // a fence) sums them in split order and runs the epilogue.
+    // a fence) sums them in split order and runs the epilogue.  At batch 1 each
+    // global round trip on this path costs the tile's last split about a
+    // microsecond, so its reads are issued together as asynchronous copies
+    // into the free stage buffers: the residual stream (EPI_RESID) before the
+    // ticket, then the splits' partials (all at once when they fit).
     const int tile_lin = tile_m * gridDim.x + tile_n;
     const size_t per_split = (size_t)n_chunks * 16 * 128;
+    const int per16 = (int)(per_split / 4);  // 16-byte pieces of one partial
     float* part = args.partial + (size_t)tile_lin * args.splits * per_split;
     float* mine = part + (size_t)split * per_split;
+    float* land = reinterpret_cast<float*>(smem) + kGroups * 2 * kXchg;  // past the exchange buffers
+    const long long land_cap = (long long)free_bytes / 4 - kGroups * 2 * kXchg;
+    const float* xres = static_cast<const float*>(epi.out);
+    const bool resid_s = epi.kind == EPI_RESID && !aborted && (epi.N & 3) == 0 && (epi.ld & 3) == 0 &&
+                         (reinterpret_cast<uintptr_t>(xres) & 15) == 0 && land_cap >= 2 * (long long)per_split;
+    float* land_p = land + (resid_s ? per_split : 0);
+    const int batch = (int)((land_cap - (resid_s ? (long long)per_split : 0)) / (long long)per_split);
+    if (resid_s) {
+      // only this tile's last split writes these values, after every split
+      // has taken its ticket; the other splits discard what they read
+      for (int idx = threadIdx.x; idx < T * 32; idx += blockDim.x) {
+        const int tl = idx >> 5, q4 = (idx & 31) * 4;
+        const int tok = tile_m * T + tl, n = tile_n * 128 + q4;
+        const bool ok = tok < epi.M && n < epi.N;
+        cp_async16(land + tl * 128 + q4, ok ? xres + (size_t)tok * epi.ld + n : xres, ok);
+      }
+    }
     if (!aborted) {
       for (int c = grp; c < n_chunks; c += kGroups) {
         float v[16];
@@ -371,22 +398,67 @@ __device__ __forceinline__ void one_tile_epilogue(uint8_t* smem, uint32_t tmem, 
     __syncthreads();
     if (*last_sh) {
       __threadfence();
-      if (!aborted) {
+      const int S = args.splits;
+      if (!aborted && batch >= 1 && (S <= batch || n_chunks == 1)) {
+        // rounds of up to `batch` partials (one round unless a single chunk
+        // accumulates across several)
+        const int nb = S < batch ? S : batch;
+        float acc[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+        for (int s0 = 0; s0 < S; s0 += nb) {
+          const int cnt = S - s0 < nb ? S - s0 : nb;
+          for (int idx = threadIdx.x; idx < cnt * per16; idx += blockDim.x) {
+            const int sl = idx / per16, off = (idx - sl * per16) * 4;
+            cp_async16(land_p + (size_t)sl * per_split + off, part + (size_t)(s0 + sl) * per_split + off, true);
+          }
+          cp_async_wait_all();
+          __syncthreads();
+          if (n_chunks == 1) {
+            if (grp == 0)
+              for (int k = 0; k < cnt; ++k) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc[j] += land_p[(size_t)k * per_split + j * 128 + r];  // split order
+              }
+            if (s0 + nb < S) __syncthreads();  // the next round overwrites the landing zone
+          }
+        }
+        for (int c = grp, it = 0; c < n_chunks; c += kGroups, ++it) {
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = acc[j];
+          if (n_chunks > 1) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+            for (int k = 0; k < S; ++k) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] += land_p[(size_t)k * per_split + (c * 16 + j) * 128 + r];
+            }
+          }
+          epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg + (it & 1) * kXchg,
+                         bar, rs_tile ? rs_tile + c * 16 : nullptr, wscale,
+                         resid_s ? land + (size_t)(c * 16) * 128 : nullptr);
+        }
+      } else if (!aborted) {
+        cp_async_wait_all();  // the residual block
+        __syncthreads();
         for (int c = grp, it = 0; c < n_chunks; c += kGroups, ++it) {
           float v[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = 0.0f;
-          for (int s = 0; s < args.splits; ++s) {
+          for (int s = 0; s < S; ++s) {
             const float* ps = part + (size_t)s * per_split;
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] += __ldcg(ps + (c * 16 + j) * 128 + r);
           }
           epilogue_chunk(epi, ao, v, tile_m * T + c * 16, 1, ntok, tile_n, r, xchg + (it & 1) * kXchg,
-                         bar, rs_tile ? rs_tile + c * 16 : nullptr, wscale);
+                         bar, rs_tile ? rs_tile + c * 16 : nullptr, wscale,
+                         resid_s ? land + (size_t)(c * 16) * 128 : nullptr);
         }
       }
       if (threadIdx.x == 0) atomicExch(&args.counters[tile_lin], 0);
     }
+    cp_async_wait_all();  // no copy may land after the CTA has left
   } else {
     // The K splits of this tile form a thread-block cluster.  Each leaves its
     // fp32 partial [T tokens][128 rows] in its own shared memory (the stage
@@ -595,7 +667,7 @@ __global__ void __launch_bounds__(gemm_threads(BN), 1)
                               100000000ull);
   }
   __syncthreads();
-  one_tile_epilogue<BN, kGroups>(smem, tmem, abort_sh != 0 || !acc_ok, ao, args, epi, tile_n, tile_m,
+  one_tile_epilogue<BN, kGroups>(smem, STAGES * kStage, tmem, abort_sh != 0 || !acc_ok, ao, args, epi, tile_n, tile_m,
                                  split, (BN <= 32 && args.rs_ssq) ? rs_sh : nullptr, &last_sh, 1.0f);
   tc_fence_before();
   __syncthreads();
@@ -693,7 +765,7 @@ __global__ void __launch_bounds__(320, 1)
           }
           if (!waited) {  // activations come from the previous kernel
             grid_dependency_wait();
-            waited = true;
+                    waited = true;
           }
           tma_load_2d(sa + kABytes, &tmB, &full_bar[s], kc, tok0, pol_x);
         }
@@ -901,7 +973,7 @@ __global__ void __launch_bounds__(320, 1)
           }
           if (!waited) {  // activations come from the previous kernel
             grid_dependency_wait();
-            waited = true;
+                    waited = true;
           }
           tma_load_2d_pair(sa + kABytes, &tmB, fb, kc, tok0, pol_x);
         }
