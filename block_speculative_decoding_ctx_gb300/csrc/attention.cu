@@ -31,6 +31,7 @@
 #include <cmath>
 
 #include "attention.h"
+#include "attention_util.cuh"
 #include "common.cuh"
 #include "gemm.h"
 
@@ -38,6 +39,7 @@ namespace dfl {
 namespace {
 
 namespace cg = cooperative_groups;
+using namespace attn;
 
 // Largest thread-block cluster (key splits of one head) attention will use.
 // (8 measured faster than 16 at batch 1 on GB300: a 16-CTA cluster waits for
@@ -46,19 +48,18 @@ namespace cg = cooperative_groups;
 #define DFLASH_ATTN_MAX_CLUSTER 8
 #endif
 
-constexpr int kKeys = 64;      // keys per context tile
+constexpr int kKeys = 64;      // keys per context tile (both kernels)
+
+// 1: heads that fit it run on the tensor-core kernel (attention_tc.cu)
+#ifndef DFLASH_ATTN_TC
+#define DFLASH_ATTN_TC 1
+#endif
 
 // Stage buffers: each key-split group owns its own stages (2 each; 3 when
 // there is one group), so every consumer waits on its stages' phases in
 // order.  Key tile i goes to group i % KW, stage (i % KW) * SPG + (i / KW) % SPG.
 __host__ __device__ constexpr int attn_spg(int KW) { return KW == 1 ? 3 : 2; }
 __host__ __device__ constexpr int attn_stages(int KW) { return KW * attn_spg(KW); }
-
-// Byte offset of element (row, col) in a [rows][64] bf16 tile with the
-// 128-byte swizzle (16-byte chunk index XOR row % 8).
-__device__ __forceinline__ uint32_t swz(int row, int col) {
-  return (uint32_t)(row * 128 + ((((col >> 3) ^ row) & 7) << 4) + ((col & 7) << 1));
-}
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
@@ -88,48 +89,6 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1,
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-// Two bf16 values (one 32-bit register) as two fp16 values: exact for
-// magnitudes 2^-14 .. 65504, saturated to +-65504 beyond.
-// Ring keys (bf16) widened to fp16 for the score MMAs: exact within the fp16
-// range.  A key beyond +-65504 (a ring the caller filled itself; ctx_append
-// reports what it would write out of range) becomes infinite rather than
-// saturated: its scores and the head's attention output turn non-finite, and
-// the next fp16 store of the pass reports DFLASH_ERR_RANGE.  Keys in slots
-// outside the visible window are masked before the softmax and never matter.
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-  const float lo = __uint_as_float(w << 16);
-  const float hi = __uint_as_float(w & 0xFFFF0000u);
-  uint32_t r;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-__device__ __forceinline__ void store_h2(__half* out, size_t o, float y0, float y1) {
-  *reinterpret_cast<__half2*>(out + o) = __floats2half2_rn(y0, y1);
-}
-
-
-__device__ __forceinline__ void named_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-// Bounded wait taken by a whole warp: the warp goes on only if every lane saw
-// the phase complete, so that the warp-collective instructions after it
-// (ldmatrix, mma.sync) stay convergent even when a wait gives up.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
-  const bool ok = mbar_wait_bounded(bar, parity, abort_flag, status);
-  return __all_sync(0xffffffffu, ok);
-}
-
 template <int HD>
 struct WarpState {
   static constexpr int NT = HD / 8;  // output n-tiles of 8 dims
@@ -685,6 +644,7 @@ int launch_attention(const void* ring_k_layer, const void* ring_v_layer, const A
   if (rc) return rc;
   rc = encode_2d(&tv, ring_v_layer, OPND_BF16, (uint64_t)a.hd, rows, 64, kKeys);
   if (rc) return rc;
+  if (DFLASH_ATTN_TC && attention_tc_supported(a)) return launch_attention_tc(tk, tv, a, B, s);
   const int mt = attn_row_tiles(a.n_q, a.n_kv, a.gamma);
   if (a.hd == 128) {
     switch (mt) {

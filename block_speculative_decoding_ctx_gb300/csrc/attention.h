@@ -3,6 +3,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -26,7 +27,15 @@ struct AttnArgs {
 int attn_row_tiles(int n_q, int n_kv, int gamma);
 
 // ring_*_layer: the layer's slice of the ring, bf16 [ring_batch, Hkv, W, hd].
+// Runs the tensor-core kernel (attention_tc.cu) where attention_tc_supported,
+// else the mma.sync kernel (attention.cu).
 int launch_attention(const void* ring_k_layer, const void* ring_v_layer, const AttnArgs& a, int B,
                      cudaStream_t s);
+
+// Head dim 64 or 128, at most 128 query rows (query heads of a group x
+// gamma) and gamma <= 16.
+bool attention_tc_supported(const AttnArgs& a);
+int launch_attention_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a, int B,
+                        cudaStream_t s);
 
 }  // namespace dfl

@@ -307,10 +307,8 @@ def test_activation_beyond_fp16_range_is_reported():
 def test_ring_key_beyond_fp16_range_is_reported(gamma):
     """Attention reads ring keys as fp16: a bf16 key beyond +-65504 written
     into the ring by the caller is not saturated silently — it becomes
-    infinite and the pass reports DFLASH_ERR_RANGE at its next fp16 store —
-    on the path that widens keys in each consumer's registers (gamma 4: two
-    row tiles) and on the one where a converter warp widens them in shared
-    memory (gamma 16: five row tiles)."""
+    infinite and the pass reports DFLASH_ERR_RANGE at its next fp16 store
+    (gamma 4 and 16: 20 and 80 query rows per KV head)."""
     dims = synth.DIMS["small"]
     W = synth.weights(dims, 98)
     h = dfl.dflash_create(tu.lib_cfg(dims, batch_max=1, gamma_max=16), tu.to_dev(W))
@@ -328,3 +326,24 @@ def test_ring_key_beyond_fp16_range_is_reported(gamma):
     dfl.dflash_draft_block(h, anchor, L, rk.cuda(), rv.cuda(), gamma, ws2, out=out)
     torch.cuda.synchronize()
     assert dfl.dflash_read_status(ws2) == -9
+
+@pytest.mark.parametrize("gamma", [4, 16])
+def test_masked_ring_slots_holding_nan_change_nothing(gamma):
+    """Ring slots past the visible window that hold NaN in K and V change
+    nothing: the pass matches the oracle, whose definition ignores those
+    slots (it reads zeros there).  Context 200 of a 256-slot window: the last
+    key tile is partly visible."""
+    from oracle import model as om
+    dims = synth.DIMS["small"]
+    W = synth.weights(dims, 98)
+    rk, rv = synth.ring(dims, 1, 99)
+    L = torch.tensor([200], dtype=torch.int64)
+    anchor = torch.tensor([3], dtype=torch.int32)
+    ref = om.draft_pass(tu.oracle_cfg(dims), W, rk, rv, L.numpy(), anchor.numpy(), gamma)
+    want = ref["logits"].reshape(1, gamma - 1, -1)
+    rk_nan, rv_nan = rk.clone(), rv.clone()
+    rk_nan[:, 0, :, 200:, :] = float("nan")
+    rv_nan[:, 0, :, 230:, :] = float("nan")
+    h = dfl.dflash_create(tu.lib_cfg(dims, batch_max=1, gamma_max=16), tu.to_dev(W))
+    got = tu.run_draft(h, anchor, L, rk_nan.cuda(), rv_nan.cuda(), gamma, topk=4)
+    assert tu.rel_err(got["logits"], want) <= 1e-2
