@@ -1,4 +1,7 @@
-// Block attention of the drafter: the gamma block queries of every query
+// Block attention of the drafter on mma.sync, and the launcher that picks
+// between it and the tensor-core kernel (attention_tc.cu), which takes head
+// dims 64 and 128 with up to 128 query rows per KV head and gamma <= 16;
+// this kernel serves the other shapes.  The gamma block queries of every query
 // head attend over [context window ; whole block], non-causally inside the
 // block ("DFlash vs DFlash 2" blog, section "Conditioning on the target
 // model": K_i = [W^K H_t ; W^K H_d], V_i = [W^V H_t ; W^V H_d]; block
