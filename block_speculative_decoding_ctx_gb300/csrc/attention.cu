@@ -1,7 +1,8 @@
-// Block attention of the drafter on mma.sync, and the launcher that picks
-// between it and the tensor-core kernel (attention_tc.cu), which takes head
-// dims 64 and 128 with up to 128 query rows per KV head and gamma <= 16;
-// this kernel serves the other shapes.  The gamma block queries of every query
+// Block attention of the drafter on mma.sync, and the launcher.  The
+// tensor-core kernel (attention_tc.cu) takes every shape this one takes (head
+// dims 64 and 128, gamma <= 16; up to 128 query rows per KV head against 96
+// here) and runs by default; this one is built in for comparison and runs
+// when the library is compiled with DFLASH_ATTN_TC=0.  The gamma block queries of every query
 // head attend over [context window ; whole block], non-causally inside the
 // block ("DFlash vs DFlash 2" blog, section "Conditioning on the target
 // model": K_i = [W^K H_t ; W^K H_d], V_i = [W^V H_t ; W^V H_d]; block
@@ -53,7 +54,8 @@ using namespace attn;
 
 constexpr int kKeys = 64;      // keys per context tile (both kernels)
 
-// 1: heads that fit it run on the tensor-core kernel (attention_tc.cu)
+// 1: attention runs on the tensor-core kernel (attention_tc.cu); 0: on the
+// mma.sync kernel below (for comparison)
 #ifndef DFLASH_ATTN_TC
 #define DFLASH_ATTN_TC 1
 #endif

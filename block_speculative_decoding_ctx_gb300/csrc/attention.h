@@ -27,8 +27,8 @@ struct AttnArgs {
 int attn_row_tiles(int n_q, int n_kv, int gamma);
 
 // ring_*_layer: the layer's slice of the ring, bf16 [ring_batch, Hkv, W, hd].
-// Runs the tensor-core kernel (attention_tc.cu) where attention_tc_supported,
-// else the mma.sync kernel (attention.cu).
+// Runs the tensor-core kernel (attention_tc.cu) where attention_tc_supported
+// (every shape the library accepts), else the mma.sync kernel (attention.cu).
 int launch_attention(const void* ring_k_layer, const void* ring_v_layer, const AttnArgs& a, int B,
                      cudaStream_t s);
 
