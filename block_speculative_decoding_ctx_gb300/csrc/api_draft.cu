@@ -81,8 +81,8 @@ int validate_config(const dflash_config& c) {
   if (!(c.eps > 0.0f) || !(c.rope_theta > 0.0f)) return DFLASH_ERR_ARG;
   if (c.mask_id < -1 || c.mask_id >= c.vocab) return DFLASH_ERR_ARG;
   if (c.weight_format != DFLASH_WEIGHTS_BF16 && c.weight_format != DFLASH_WEIGHTS_E4M3) return DFLASH_ERR_ARG;
-  // query-group rows of one KV head must fit the attention kernel's tiles
-  if (attn_row_tiles(c.n_q_heads, c.n_kv_heads, c.gamma_max) > 6) return DFLASH_ERR_UNSUPPORTED;
+  // query-group rows of one KV head are the rows of the attention MMAs
+  if ((c.n_q_heads / c.n_kv_heads) * c.gamma_max > attn_max_rows()) return DFLASH_ERR_UNSUPPORTED;
   return DFLASH_OK;
 }
 

@@ -1,4 +1,5 @@
-// Internal interface of the block-attention kernel (attention.cu).
+// Internal interface of the block attention (launcher attention.cu, kernel
+// attention_tc.cu).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -23,12 +24,12 @@ struct AttnArgs {
   int* status;
 };
 
-// 16-row MMA tiles needed for the (query group x gamma) rows.
-int attn_row_tiles(int n_q, int n_kv, int gamma);
+// Largest number of query rows (query heads of a KV head's group x gamma).
+int attn_max_rows();
 
 // ring_*_layer: the layer's slice of the ring, bf16 [ring_batch, Hkv, W, hd].
-// Runs the tensor-core kernel (attention_tc.cu) where attention_tc_supported
-// (every shape the library accepts), else the mma.sync kernel (attention.cu).
+// Runs the tensor-core kernel (attention_tc.cu); DFLASH_ERR_UNSUPPORTED for
+// shapes it does not take (dflash_create rejects those configurations).
 int launch_attention(const void* ring_k_layer, const void* ring_v_layer, const AttnArgs& a, int B,
                      cudaStream_t s);
 

@@ -1,13 +1,13 @@
-// Block attention of the drafter on the 5th-generation tensor cores: the same
-// operation as attention.cu ("DFlash vs DFlash 2" blog, section "Conditioning
+// Block attention of the drafter on the 5th-generation tensor cores
+// ("DFlash vs DFlash 2" blog, section "Conditioning
 // on the target model": the gamma block queries of each head attend over
 // [context window ; whole block], non-causally inside the block; model card
 // "Beam-1.0-501B-A23B-DFlash2", section "Model": 4,096-token sliding window,
 // 40 query / 8 KV heads), for head dims 64 and 128 and at most 128 query rows
 // per KV head (query heads of the group x gamma).
 //
-// One CTA serves one (request, KV head, key split), as in attention.cu; the
-// splits of a head form a thread-block cluster and merge their partial
+// One CTA serves one (request, KV head, key split); the splits of a head form
+// a thread-block cluster and merge their partial
 // softmax states through distributed shared memory in split order.  Inside a
 // CTA the query rows are the 128 rows of every MMA (zero-padded), so one K/V
 // byte read from HBM serves every query head of the group:

@@ -1,5 +1,6 @@
-// Helpers shared by the two block-attention kernels (attention.cu on
-// mma.sync, attention_tc.cu on the 5th-generation tensor cores).
+// Small device helpers of the block-attention kernel (attention_tc.cu):
+// swizzled tile offsets, bf16 -> fp16 widening, 16-bit packing, 2^x, and a
+// warp-wide bounded wait.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -58,7 +59,7 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
 
 // Bounded wait taken by a whole warp: the warp goes on only if every lane saw
 // the phase complete, so that the warp-collective instructions after it
-// (ldmatrix, mma.sync, tcgen05.ld/st) stay convergent even when a wait gives up.
+// (tcgen05.ld/st) stay convergent even when a wait gives up.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int* status) {
   const bool ok = mbar_wait_bounded(bar, parity, abort_flag, status);

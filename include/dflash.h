@@ -101,7 +101,8 @@ enum { DFLASH_VERIFY_GREEDY = 0, DFLASH_VERIFY_SAMPLED = 1 };
 
 /* Drafter dimensions.  Constraints checked by dflash_create: head_dim is 64
  * or 128; hidden, ffn, n_q_heads*head_dim and n_feat*feat_dim are multiples
- * of 64; hidden <= 12288; n_q_heads is a multiple of n_kv_heads; 1 <= gamma_max <= 16;
+ * of 64; hidden <= 12288; n_q_heads is a multiple of n_kv_heads; 2 <= gamma_max <= 16;
+ * (n_q_heads / n_kv_heads) * gamma_max <= 128 (the query rows of one KV head);
  * 1 <= topk_max <= 16; window >= 1. */
 typedef struct dflash_config {
   int hidden;      /* d */
