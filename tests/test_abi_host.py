@@ -75,5 +75,11 @@ def test_create_validates_the_configuration(L):
                       (dict(hidden=200), -4), (dict(mask_id=5000), -1), (dict(topk_max=0), -4)):
         assert L.dflash_create(ctypes.byref(_cfg(**bad)), ctypes.byref(w), ctypes.byref(out)) == code
         assert not out.value
+    # query rows of one KV head (group x gamma_max) are the rows of the attention MMAs: 144 > 128
+    assert L.dflash_create(ctypes.byref(_cfg(n_q_heads=18, gamma_max=16)), ctypes.byref(w),
+                           ctypes.byref(out)) == -4
     lw[0].w_o = 4100                       # misaligned weight
     assert L.dflash_create(ctypes.byref(_cfg()), ctypes.byref(w), ctypes.byref(out)) == -3
+    # 128 rows pass the shape checks (the call then stops at the misaligned weight)
+    assert L.dflash_create(ctypes.byref(_cfg(n_q_heads=16, gamma_max=16)), ctypes.byref(w),
+                           ctypes.byref(out)) == -3
