@@ -65,6 +65,24 @@ def test_draft_block_matches_oracle(name, B, gamma, lens):
     np.testing.assert_array_equal(got["draft"], got["topk_ids"][..., 0])
 
 
+def test_draft_block_at_the_largest_query_group_matches_oracle():
+    """128 query rows per KV head, the largest a configuration may have: 8
+    query heads per KV head at gamma 16, so every tensor-memory lane quarter
+    of the attention holds query rows (contexts 300 and 7: a split with a
+    partly visible last tile, and one with only part of a tile)."""
+    dims = dict(synth.DIMS["small"], n_q=16, n_kv=2)
+    B, gamma = 2, 16
+    W = synth.weights(dims, 21, random_gains=True)
+    rk, rv = synth.ring(dims, B, 22)
+    anchor = synth.token_ids(B, dims["vocab"], 23)
+    L = torch.tensor([300, 7], dtype=torch.int64)
+    ref = om.draft_pass(tu.oracle_cfg(dims), W, rk, rv, L.numpy(), anchor.numpy(), gamma)
+    h = dfl.dflash_create(tu.lib_cfg(dims, batch_max=B, gamma_max=gamma), tu.to_dev(W))
+    got = tu.run_draft(h, anchor, L, rk.cuda(), rv.cuda(), gamma, topk=4)
+    want = ref["logits"].reshape(B, gamma - 1, -1)
+    assert tu.rel_err(got["logits"], want) <= TOL
+
+
 def test_draft_block_long_window_at_small_batch_matches_oracle():
     """A long window at small batch: every KV head's keys split over a full
     cluster of CTAs merged through distributed shared memory.  Contexts 2000,
