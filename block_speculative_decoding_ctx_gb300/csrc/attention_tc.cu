@@ -1,17 +1,17 @@
-// Block attention of the drafter on the 5th-generation tensor cores
-// ("DFlash vs DFlash 2" blog, section "Conditioning
-// on the target model": the gamma block queries of each head attend over
-// [context window ; whole block], non-causally inside the block; model card
-// "Beam-1.0-501B-A23B-DFlash2", section "Model": 4,096-token sliding window,
-// 40 query / 8 KV heads), for head dims 64 and 128 and at most 128 query rows
-// per KV head (query heads of the group x gamma).
+// Block attention of the drafter on the 5th-generation tensor cores ("DFlash
+// vs DFlash 2" blog, section "Conditioning on the target model": the gamma
+// block queries of each head attend over [context window ; whole block],
+// non-causally inside the block; model card "Beam-1.0-501B-A23B-DFlash2",
+// section "Model": 4,096-token sliding window, 40 query / 8 KV heads), for
+// head dims 64 and 128 and at most 128 query rows per KV head (query heads of
+// the group x gamma).
 //
 // One CTA serves one (request, KV head, key split); the splits of a head form
-// a thread-block cluster and merge their partial
-// softmax states through distributed shared memory in split order.  Inside a
-// CTA the query rows are the 128 rows of every MMA (zero-padded), so one K/V
-// byte read from HBM serves every query head of the group:
-//   warp 0       TMA producer: 64-key K/V tiles of the ring, STAGES deep
+// a thread-block cluster and merge their partial softmax states through
+// distributed shared memory in split order.  Inside a CTA the query rows are
+// the 128 rows of every MMA (zero-padded), so one K/V byte read from HBM
+// serves every query head of the group:
+//   warp 0       TMA producer: 64-key K/V tiles of the ring, 5 stages
 //   warp 1       tensor-memory allocation; lane 0 issues the MMAs
 //                  S_i = Q K_i^T     (fp16, A = Q and B = K_i in shared memory)
 //                  O  += P_i V_i     (bf16 for ring tiles, fp16 for the block's
@@ -27,6 +27,8 @@
 //                m) into tensor memory, running sum.  O lives in tensor memory
 //                and is rescaled only when a row's maximum grows by more than
 //                2^8 (P <= 256 meanwhile), which happens a few times per row.
+//                A warp whose lanes hold only padding rows just keeps the
+//                barriers' phases.
 // Before the loop warps 2-7 load Q (and the block's own K/V) with
 // asynchronous copies.  All waits are bounded (mbar_wait_bounded); a CTA that
 // gives up still meets its cluster barriers and frees its tensor memory.
